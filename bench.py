@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Throughput of one routed-MoE layer step over a partial expert set on GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic tokens:
+router scores + resident-only top-k with substitution, demand accumulation,
+the heavy-miss list, and the grouped MXFP4 SwiGLU expert FFN with weighted
+combine (TideLM README, "How adaptive expert loading works", items 1-3).
+
+Headline workload: the DeepSeek-like decode layer (E=256, top-8, d=4096,
+ffn=2048, 166 of 256 experts resident, router bias sigma=1.5) at T=64 tokens.
+The sweep adds T=1, 8, 32 and the 8192-token prefill layer.
+
+Timing: W warm-up steps, then K steps replayed from a CUDA graph, each timed
+with CUDA events on the launching stream; between steps the next batch of
+hidden states is copied in and L2 is flushed by writing 256 MiB (outside the
+timed events). `--gpus N` under torchrun runs N independent replicas (the
+layer does not shard across GPUs here) and reports the summed throughput over
+the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/sec (decode T=1..64, prefill 8K); % HBM / FP4 roofline"
+GATE_UP_BYTES_PER_EXPERT = None   # filled from the slot record
+
+
+# ------------------------------------------------------------------ setup
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return dict(hbm_gbs=float(j["hbm_gbs"]), bf16_tflops=float(j["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, source="fallback")
+
+
+class Layer:
+    """Device-resident inputs of one layer workload (weights, tables, arena, hidden-state pool)."""
+
+    def __init__(self, cfg: synth.LayerConfig, T: int, pool: int, drift: bool = False):
+        import torch
+        import resident_expert_routed_gb300 as moe
+        from resident_expert_routed_gb300.layer import LayerBuffers
+        self.cfg, self.T = cfg, T
+        W = synth.router_weights(cfg.seed, cfg.E, cfg.d)
+        b = synth.router_bias(cfg.seed, cfg.E, cfg.sigma)
+        res = synth.resident_set(cfg, b)
+        self.n_slots = cfg.resident + cfg.n_ring
+        self.slot_of_np = synth.slot_table(cfg, res, self.n_slots)
+        owner = np.full(self.n_slots, -1, np.int32)
+        owner[self.slot_of_np[res]] = res
+        self.owner_np = owner
+        if drift:
+            b = synth.drifted_bias(cfg, b)
+        self.W_np, self.b_np = W, b
+        self.W = torch.from_numpy(W).cuda()
+        self.bias = torch.from_numpy(b).cuda()
+        self.slot_of = torch.from_numpy(self.slot_of_np).cuda()
+        rec = synth.slot_record(cfg.d, cfg.ffn)
+        self.rec = rec
+        buf = torch.zeros(self.n_slots * rec["slot_bytes"], dtype=torch.uint8, device="cuda")
+        synth.fill_slots_device(buf, cfg.d, cfg.ffn, cfg.seed, cfg.E, torch.from_numpy(owner).cuda())
+        self.arena = moe.Arena(buf, rec["slot_bytes"], self.n_slots, cfg.d, cfg.ffn, rec["off_gu_codes"],
+                               rec["off_gu_scales"], rec["off_dn_codes"], rec["off_dn_scales"])
+        self.pool_np = [synth.hidden_bf16(cfg.seed, T, cfg.d, stream=100 + i) for i in range(pool)]
+        self.pool = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in self.pool_np]
+        self.hidden = torch.empty((T, cfg.d), dtype=torch.bfloat16, device="cuda")
+        self.buf = LayerBuffers(T, cfg.k, cfg.E, cfg.d, cfg.ffn, self.n_slots)
+        self.demand = torch.zeros((1, cfg.E), dtype=torch.int64, device="cuda")
+        self.miss = torch.zeros((1, cfg.E), dtype=torch.float32, device="cuda")
+
+    def step(self, stream=None):
+        from resident_expert_routed_gb300.layer import layer_step, step_end
+        layer_step(self.hidden, self.W, self.bias, self.slot_of, self.arena, self.demand, self.miss, 0, self.buf,
+                   stream)
+        step_end(self.miss, self.buf, 0.2, stream)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) >= 9:
+                    rows.append(f)
+        except OSError:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max((num(r[2]) for r in rows if num(r[2]) is not None), default=None),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) for r in rows if num(r[3]) is not None), default=None)}
+
+
+def flush_l2(scratch):
+    scratch.add_(1)
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, ws, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ timed runs
+
+def timed_graph_steps(layer: Layer, K: int, W: int, scratch, ws: int):
+    """Returns (per-step ms list, launches per step, distinct slots per step)."""
+    import torch
+    import resident_expert_routed_gb300 as moe
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(max(W, 1)):
+            layer.hidden.copy_(layer.pool[i % len(layer.pool)])
+            layer.step(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    n0 = moe.moe_kernel_launches()
+    with torch.cuda.graph(graph, stream=stream):
+        layer.step(stream)
+    launches = moe.moe_kernel_launches() - n0
+    torch.cuda.synchronize()
+    for i in range(3):                     # graph warm-up
+        layer.hidden.copy_(layer.pool[i % len(layer.pool)])
+        graph.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    slots_used = []
+    barrier(ws)
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    for i in range(K):
+        layer.hidden.copy_(layer.pool[i % len(layer.pool)])
+        flush_l2(scratch)
+        ev[i][0].record(cur)
+        graph.replay()
+        ev[i][1].record(cur)
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    for i in range(min(K, len(layer.pool))):   # distinct slots touched per batch (for the byte count)
+        layer.hidden.copy_(layer.pool[i])
+        graph.replay()
+        torch.cuda.synchronize()
+        s = layer.buf.sel_slot.cpu().numpy()
+        slots_used.append(int(len(np.unique(s[s >= 0]))))
+    return ms, launches, slots_used, graph
+
+
+def profiled_steps(layer: Layer, K: int, scratch):
+    """Per-kernel device time (events around each launch), eager steps with the same L2 flush."""
+    import torch
+    import resident_expert_routed_gb300 as moe
+    moe.moe_profile_reset()
+    moe.moe_profile_enable(True)
+    stream = torch.cuda.current_stream()
+    used = []
+    for i in range(K):
+        layer.hidden.copy_(layer.pool[i % len(layer.pool)])
+        flush_l2(scratch)
+        layer.step(stream)
+    torch.cuda.synchronize()
+    prof = moe.moe_profile_read()
+    moe.moe_profile_enable(False)
+    return prof
+
+
+def e2e_steps(layer: Layer, K: int, scratch):
+    """Same metric through the public API with host buffers: pinned H2D of the batch, the step, D2H of out."""
+    import torch
+    host_in = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in layer.pool_np]
+    host_out = torch.empty((layer.T, layer.cfg.d), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    total = 0.0
+    for i in range(K):
+        flush_l2(scratch)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        layer.hidden.copy_(host_in[i % len(host_in)], non_blocking=True)
+        layer.step(stream)
+        host_out.copy_(layer.buf.out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        total += a.elapsed_time(b)
+    h2d = layer.T * layer.cfg.d * 2
+    d2h = layer.T * layer.cfg.d * 4
+    return total / K, h2d, d2h
+
+
+# ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
+
+def oracle_sample_run(cfg: synth.LayerConfig, x_bits, W, bias, slot_of, owner, n_tok: int) -> float:
+    """Seconds for the oracle to run the whole step (route, demand, heavy misses, FFN) on n_tok tokens."""
+    import oracle
+    x = x_bits[:n_tok]
+    t0 = time.perf_counter()
+    r = oracle.route(x, W, bias, slot_of, cfg.k)
+    D = np.zeros((1, cfg.E))
+    M = np.zeros((1, cfg.E))
+    oracle.demand(r["want_e"], r["want_s"], slot_of, 0, D, M)
+    oracle.hot_miss_select(M, 0.2, 16)
+    used = sorted({int(s) for s in r["sel_slot"].ravel() if s >= 0})
+    index = {s: i for i, s in enumerate(used)}
+    sel_u = np.vectorize(lambda s: index.get(int(s), -1))(r["sel_slot"]).astype(np.int32)
+    experts = [synth.expert_weights(cfg.seed, int(owner[s]) // cfg.E, int(owner[s]) % cfg.E, cfg.d, cfg.ffn)
+               for s in used]
+    oracle.ffn(x, sel_u, r["sel_w"], experts, cfg.d, cfg.ffn)
+    return time.perf_counter() - t0
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def run_reference(args, rank, ws):
+    """The oracle, as it stands, on the host cores: each step a bounded sample of the headline workload."""
+    if rank != 0:
+        return
+    cfg, T = synth.DECODE, args.T
+    W = synth.router_weights(cfg.seed, cfg.E, cfg.d)
+    b = synth.router_bias(cfg.seed, cfg.E, cfg.sigma)
+    res = synth.resident_set(cfg, b)
+    slot_of = synth.slot_table(cfg, res, cfg.resident)
+    owner = np.full(cfg.resident, -1, np.int32)
+    owner[slot_of[res]] = res
+    n_tok = 2
+    for i in range(args.warmup):
+        oracle_sample_run(cfg, synth.hidden_bf16(cfg.seed, T, cfg.d, stream=100 + i), W, b, slot_of, owner, n_tok)
+    secs = 0.0
+    for i in range(args.steps):
+        secs += oracle_sample_run(cfg, synth.hidden_bf16(cfg.seed, T, cfg.d, stream=100 + i), W, b, slot_of, owner,
+                                  n_tok)
+    value = n_tok * args.steps / secs
+    sample = f"{n_tok} of the {T} tokens of each batch: route, demand, heavy misses and FFN (float64)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{cfg.name}, T={T}", "reference": "the C++ oracle (no runnable reference code "
+                       "exists: the method's pages hold no code)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
+                             "cpu": cpu_model()},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main
+
+def run_ours(args, rank, ws, local):
+    import torch
+    import resident_expert_routed_gb300 as moe
+    moe.load()
+    pk = peaks()
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    cfg, T = synth.DECODE, args.T
+    layer = Layer(cfg, T, pool=8)
+    rec = layer.rec
+    gate_up_bytes = rec["gu_codes_bytes"] + rec["gu_scales_bytes"]
+    expert_bytes = gate_up_bytes + rec["dn_codes_bytes"] + rec["dn_scales_bytes"]
+
+    t_wall = time.perf_counter()
+    with ClockSampler(local) as clk:
+        ms, launches, slots_used, _ = timed_graph_steps(layer, args.steps, args.warmup, scratch, ws)
+    wall = time.perf_counter() - t_wall
+    clocks = clk.summary()
+    step_ms = sum(ms) / len(ms)
+    step_ms_max = max_over_ranks(step_ms, ws)
+    value = ws * T / (step_ms_max / 1000.0)
+
+    prof = profiled_steps(layer, min(args.steps, 16), scratch)
+    dom = max(prof.items(), key=lambda kv: kv[1][1])
+    gu = prof.get("ffn_gemm_gate_up", (1, float("nan")))
+    u_mean = float(np.mean(slots_used))
+    achieved = u_mean * gate_up_bytes / (gu[1] / gu[0] / 1000.0) / 1e9
+    roofline = {"bound": "hbm", "kernel": "ffn_gemm_gate_up", "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                "peak_source": f"{pk['source']} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if pk["source"] == "measured" else "fallback 6800 GB/s",
+                "algorithmic_bytes_per_launch": u_mean * gate_up_bytes,
+                "units": f"{u_mean:.1f} distinct experts x {gate_up_bytes} B gate/up codes+scales",
+                "kernel_ms": gu[1] / gu[0], "dominant_kernel": dom[0]}
+    step_bytes = u_mean * expert_bytes + cfg.E * cfg.d * 4
+    kernels = {k: {"launches": n, "avg_us": 1000.0 * t / n} for k, (n, t) in prof.items()}
+
+    e2e_ms, h2d, d2h = e2e_steps(layer, min(args.steps, 20), scratch)
+
+    sweep = {}
+    if not args.no_sweep:
+        for Ts in (1, 8, 32):
+            ls = Layer(cfg, Ts, pool=4)
+            m, _, su, _ = timed_graph_steps(ls, 20, 3, scratch, 1)
+            sm = sum(m) / len(m)
+            sweep[f"decode_T{Ts}"] = {"tokens_per_s": Ts / (sm / 1000.0), "ms_per_step": sm,
+                                      "distinct_experts": float(np.mean(su)),
+                                      "step_hbm_frac": (np.mean(su) * expert_bytes + cfg.E * cfg.d * 4) / (sm / 1000.0)
+                                      / 1e9 / pk["hbm_gbs"]}
+            del ls
+        sweep[f"decode_T{T}"] = {"tokens_per_s": T / (step_ms / 1000.0), "ms_per_step": step_ms,
+                                 "distinct_experts": u_mean,
+                                 "step_hbm_frac": step_bytes / (step_ms / 1000.0) / 1e9 / pk["hbm_gbs"]}
+        if not args.no_prefill:
+            lp = Layer(synth.PREFILL, 8192, pool=2)
+            m, _, su, _ = timed_graph_steps(lp, 5, 2, scratch, 1)
+            sm = sum(m) / len(m)
+            flops = 8192 * cfg.k * 6 * cfg.d * cfg.ffn
+            sweep["prefill_T8192"] = {"tokens_per_s": 8192 / (sm / 1000.0), "ms_per_step": sm,
+                                      "ffn_tflops": flops / (sm / 1000.0) / 1e12, "distinct_experts": float(np.mean(su))}
+            del lp
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n_tok = 3
+        secs = oracle_sample_run(cfg, layer.pool_np[0], layer.W_np, layer.b_np, layer.slot_of_np, layer.owner_np,
+                                 n_tok)
+        cpu = {"value": n_tok / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n_tok} tokens of one T={T} batch: route, demand, heavy misses and FFN in float64 "
+                         f"({secs:.1f} s)", "cpu": cpu_model()}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "mxfp4", "data": "synthetic",
+                "config": {"workload": f"{cfg.name}, T={T} tokens per layer step (one step = route + demand + "
+                                       f"heavy-miss list + expert FFN)",
+                           "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                           "timing": "CUDA graph replay per step, CUDA events on the launching stream",
+                           "parallelism": f"replicas x{ws}"},
+                "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": {"value": T / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                        "path": "pinned host batch -> layer_step/step_end (C ABI) -> pinned host output"},
+                "gpu_launches": launches * args.steps, "clocks": clocks, "kernels": kernels, "sweep": sweep,
+                "wall_s": wall}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--T", type=int, default=64)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)      # at least three untimed warm-up steps
+    rank, ws, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, ws)
+    else:
+        run_ours(args, rank, ws, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,224 @@
+/*
+ * moe_resident.h -- C ABI of one routed-MoE layer step over a partial,
+ * demand-learned set of resident experts (hand-written CUDA for sm_103a).
+ *
+ * The method is the adaptive expert loading of the TideLM README, section
+ * "How adaptive expert loading works":
+ *   item 1  demand learned from the router's own picks, per (layer, expert),
+ *           weighted by routing score; one arena shared by all layers,
+ *           re-planned from that history;
+ *   item 2  the router only picks resident experts; a missing pick is
+ *           replaced by the next-best resident expert for that token, and
+ *           its demand still counts;
+ *   item 3  heavy misses (>= 0.2 of the routing weight, at most 16 a step)
+ *           feed hot reads into a ring of slots of their own.
+ * The experts are "native MXFP4" (README profile table): OCP MX v1.0 e2m1
+ * elements with one e8m0 scale per 32 elements.
+ *
+ * Conventions for every call
+ *   - Pointers are DEVICE pointers owned by the caller unless a comment says
+ *     "host". The library never allocates, frees or synchronises on these
+ *     calls; all work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and runs asynchronously.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns MOE_EINVAL (or MOE_ENOMEM for a short workspace,
+ *     MOE_EUNSUPPORTED for a size past a documented limit) and launches
+ *     nothing. A CUDA launch error returns MOE_ECUDA.
+ *   - Data-dependent faults found on the device (a slot id past the arena, an
+ *     e8m0 scale byte 0xFF, a bounded wait that ran out) are recorded in a
+ *     per-device error word; device code never traps. moe_device_status()
+ *     reads and clears it.
+ *   - Layouts are row-major. bf16 hidden states are raw 16-bit patterns.
+ *   - Ties: equal router scores order by the lower expert index.
+ */
+#ifndef MOE_RESIDENT_H
+#define MOE_RESIDENT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_EINVAL = 1,        /* bad argument (null pointer, size out of range) */
+    MOE_ECUDA = 2,         /* a CUDA runtime call or launch failed */
+    MOE_ENOMEM = 3,        /* workspace smaller than the matching *_workspace_bytes() */
+    MOE_ETIMEOUT = 4,      /* device error word: a bounded wait in a kernel ran out */
+    MOE_EDEVICE = 5,       /* device error word: bad slot id / NaN scale / bad table */
+    MOE_EUNSUPPORTED = 6   /* a size past a documented limit */
+} moe_status;
+
+/* Bits of the device error word (moe_device_status). */
+#define MOE_DEV_BAD_SLOT    0x1u   /* a slot id >= arena n_slots was routed */
+#define MOE_DEV_NAN_SCALE   0x2u   /* an e8m0 weight scale byte 0xFF (NaN) was read */
+#define MOE_DEV_TIMEOUT     0x4u   /* a pipeline wait gave up after its limit */
+#define MOE_DEV_BAD_TABLE   0x8u   /* slot_of / owner tables inconsistent (re-plan, ring) */
+#define MOE_DEV_RESIDENT    0x10u  /* ring install of an expert that is already resident */
+
+/*
+ * The shared slot arena (README item 1: "one arena is shared by all layers").
+ * Passed by HOST pointer; `base` is a device pointer to n_slots records of
+ * slot_bytes each. Slots [0, n_main) form the main arena and the rest the
+ * hot-read ring (README item 3); the FFN treats them alike.
+ * One slot record holds one expert in MXFP4 (two e2m1 codes per byte, the
+ * even element in the LOW nibble, K contiguous; one e8m0 byte per 32 K):
+ *   off_gu_codes   [2*ffn, d/2]   gate rows 0..ffn-1, then up rows ffn..2ffn-1
+ *   off_gu_scales  [2*ffn, d/32]
+ *   off_dn_codes   [d, ffn/2]
+ *   off_dn_scales  [d, ffn/32]
+ * Requirements: base and every offset 256-byte aligned, slot_bytes a multiple
+ * of 256, d and ffn multiples of 128.
+ */
+typedef struct {
+    void*   base;
+    int64_t slot_bytes;
+    int32_t n_slots;
+    int32_t d;
+    int32_t ffn;
+    int32_t reserved;
+    int64_t off_gu_codes;
+    int64_t off_gu_scales;
+    int64_t off_dn_codes;
+    int64_t off_dn_scales;
+} moe_arena;
+
+/*
+ * Router scoring and resident-only top-k with substitution.
+ * README items 1-2: the router scores every token against all E experts; the
+ * wanted picks are the top-k over all experts; the router only picks resident
+ * experts, replacing a missing pick with the next-best resident one.
+ *   logit[t,e] = sum_i x[t,i] * W[e,i] + bias[e]   (fp32 accumulation)
+ *   score[t,e] = softmax over e of logit[t,e]
+ *   want  = top-k of score over all E                (score desc, index asc)
+ *   sel   = top-k of score over {e : slot_of[e] >= 0}
+ * hidden_bf16 [T,d] bf16; w_router [E,d] fp32; bias [E] fp32 or NULL;
+ * slot_of [E] int32 (slot id, -1 = not resident) for this layer.
+ * Outputs [T,k]: want_e int32, want_s fp32 (its score); sel_e int32,
+ * sel_slot int32, sel_w fp32 (the pick's own score, not renormalised);
+ * when fewer than k experts are resident the tail is (-1, -1, 0).
+ * workspace: >= moe_workspace_bytes(T, k, d, ffn, E, S) bytes (any ffn, S).
+ * Limits: 1 <= k <= 32, k <= E <= 1024, d % 32 == 0, T >= 1.
+ */
+moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, const float* bias,
+                              const int32_t* slot_of, int T, int d, int E, int k,
+                              int32_t* want_e, float* want_s,
+                              int32_t* sel_e, int32_t* sel_slot, float* sel_w,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Demand accumulation (README item 1: every wanted pick, resident or not,
+ * recorded per (layer, expert) weighted by its routing score; item 2: the
+ * demand of a substituted pick still counts) and the miss share (item 3: a
+ * miss "would have carried a large share of a token's routing weight").
+ *   demand[layer, e]   += round(s * 2^40)   for each wanted pick (t, j)
+ *   miss_max[layer, e]  = max(miss_max, s)  for each wanted pick with slot_of[e] < 0
+ * want_e, want_s [T,k] as written by moe_route_resident; slot_of [E] of this
+ * layer; demand uint64 [L,E] in units of 2^-40 (order-free, deterministic);
+ * miss_max fp32 [L,E] (>= 0). Limits: 0 <= layer < L, E <= 1024.
+ */
+moe_status moe_demand_accumulate(const int32_t* want_e, const float* want_s, const int32_t* slot_of,
+                                 int T, int k, int layer, int L, int E,
+                                 uint64_t* demand, float* miss_max, void* stream);
+
+/*
+ * Heavy-miss list for one step (README item 3: the heaviest misses, >= 0.2 of
+ * the routing weight, at most 16 a step; "every lane's misses feed one
+ * plan"). Candidates are (layer, expert) with miss_max >= threshold, ordered
+ * by miss_max descending, then flat index layer*E + e ascending; the first
+ * `cap` are written. Afterwards miss_max is reset to zero for the next step.
+ * out_flat int32 [cap], out_share fp32 [cap], n_out: device int32 (count).
+ * Limits: 0 <= cap <= 1024, L*E <= 2^24.
+ */
+moe_status moe_hot_miss_select(float* miss_max, int L, int E, float threshold, int cap,
+                               int32_t* out_flat, float* out_share, int32_t* n_out, void* stream);
+
+/*
+ * Grouped SwiGLU expert FFN over the MXFP4 arena with weighted combine
+ * (README items 1-2 and the "native MXFP4" experts of the profile table).
+ * For every pick (t, j) with sel_slot[t,j] >= 0, with W the expert in that slot:
+ *   xq   = MXFP4(x[t])      (OCP MX: exponent floor(log2 amax) - 2, RNE, saturate)
+ *   g, u = Wg xq, Wu xq     (tcgen05 block-scaled MXFP4 MMA, fp32 accumulation)
+ *   h    = silu(g) * u,  hq = MXFP4(h)  (blocks of 32 along ffn)
+ *   y    = Wd hq
+ *   out[t] = sum_j sel_w[t,j] * y(t, j)   (j = 0..k-1 in order: deterministic)
+ * hidden_bf16 [T,d]; sel_slot, sel_w [T,k] (as from moe_route_resident);
+ * arena: HOST pointer, see moe_arena; out fp32 [T,d] (fully overwritten;
+ * a token with no pick gets zeros).
+ * workspace: >= moe_workspace_bytes(T, k, d, ffn, E, arena->n_slots).
+ * Limits: 1 <= k <= 32, T*k <= 2^20, n_slots <= 16384, d and ffn multiples of
+ * 128, d <= 16384, ffn <= 16384.
+ */
+moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot, const float* sel_w,
+                                const moe_arena* arena, int T, int k, float* out,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Re-plan of the one shared arena from the demand history (README item 1: the
+ * arena is filled from the history and re-planned; "a busy layer takes slots
+ * from a quiet one").
+ *   1. rank every flat id f = layer*E + e by (demand desc, currently in a main
+ *      slot first, f asc); the first n_main form the new main set;
+ *   2. survivors keep their slots; main-set members that drop out lose theirs;
+ *   3. newcomers, in rank order, take the free main slots in ascending order;
+ *      a newcomer that sat in a ring slot (>= n_main) leaves it;
+ *   4. loads[] lists the main slots given to newcomers (to be refilled by the
+ *      caller with the new owners' weights), *n_loads their count.
+ * demand uint64 [L,E] (< 2^62); slot_of int32 [L*E] in/out; owner int32
+ * [n_slots] in/out (flat id or -1); loads int32 [n_main]; n_loads device int32.
+ * workspace: >= moe_replan_workspace_bytes(L, E).
+ * Limits: 1 <= n_main <= n_slots, L*E <= 2^22.
+ */
+moe_status moe_arena_replan(const uint64_t* demand, int L, int E, int n_main, int n_slots,
+                            int32_t* slot_of, int32_t* owner, int32_t* loads, int32_t* n_loads,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Ring install (README item 3, DeepSeek: after a step the heaviest misses go
+ * into a ring of slots of their own, routable from the step after until the
+ * ring wraps). Makes flat id `flat_id` resident in `ring_slot`; the slot's
+ * previous owner becomes non-resident. The slot's bytes are written by the
+ * caller. An expert that is already resident is left alone and sets
+ * MOE_DEV_RESIDENT in the device error word.
+ * slot_of int32 [n_flat], owner int32 [n_slots].
+ */
+moe_status moe_ring_install(int32_t* slot_of, int32_t* owner, int ring_slot, int flat_id,
+                            int n_flat, int n_slots, void* stream);
+
+/* Workspace sizes (bytes) for the calls above. */
+size_t moe_workspace_bytes(int T, int k, int d, int ffn, int E, int n_slots);
+size_t moe_replan_workspace_bytes(int L, int E);
+
+/*
+ * Reads and clears the current device's error word (synchronises `stream`).
+ * Returns MOE_OK, MOE_ETIMEOUT (timeout bit set) or MOE_EDEVICE (any other
+ * bit); *bits (host, may be NULL) receives the raw word.
+ */
+moe_status moe_device_status(void* stream, uint32_t* bits);
+
+/* Static English text for a status code. */
+const char* moe_status_str(moe_status s);
+
+/* Number of kernels this library has launched in this process (host counter). */
+uint64_t moe_kernel_launches(void);
+
+/*
+ * Per-kernel device timing (tracing). When enabled, every kernel launch is
+ * bracketed by two CUDA events on its stream; moe_profile_read() waits for
+ * the recorded events and returns, per kernel kind, the launch count and the
+ * summed device time since the last reset. Off by default; not for use while
+ * a stream is being captured into a CUDA graph. The events are created by the
+ * library on first use and reused.
+ * kind: 0 .. moe_profile_kernel_count()-1; *name is a static string.
+ */
+moe_status moe_profile_enable(int on);
+int        moe_profile_kernel_count(void);
+moe_status moe_profile_read(int kind, const char** name, int64_t* launches, double* total_ms);
+void       moe_profile_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_RESIDENT_H */

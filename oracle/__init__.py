@@ -59,7 +59,7 @@ def _declare(L):
     L.or_demand.argtypes = [_P, _P, _P, _I, _I, _I, _I, _P, _P]
     L.or_hot_miss_select.argtypes = [_P, _I, _I, _D, _I, _P, _P, _P]
     L.or_expert_pair.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
-    L.or_ffn.argtypes = [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]
+    L.or_ffn.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]
     L.or_replan.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P]
     L.or_ring_install.restype = _I
     L.or_ring_install.argtypes = [_P, _P, _I, _I]
@@ -192,7 +192,7 @@ def ffn(x_bf16: np.ndarray, sel_u: np.ndarray, sel_w: np.ndarray, experts: list,
     dc = _c(np.stack([e["dn_codes"] for e in experts]), np.uint8)
     ds = _c(np.stack([e["dn_scales"] for e in experts]), np.uint8)
     out = np.zeros((T, d), np.float64)
-    lib().or_ffn(_ptr(x), _ptr(su), _ptr(sw), T, k, d, F, _ptr(gc), _ptr(gs), _ptr(dc), _ptr(ds), _ptr(out))
+    lib().or_ffn(_ptr(x), _ptr(su), _ptr(sw), T, k, d, F, len(experts), _ptr(gc), _ptr(gs), _ptr(dc), _ptr(ds), _ptr(out))
     return out
 
 

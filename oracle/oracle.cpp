@@ -97,9 +97,14 @@ void or_quantise_mxfp4(const double* v, int n, uint8_t* codes, uint8_t* scales) 
 
 // Dequantise an MXFP4 vector of length n (codes n/2 bytes, scales n/32 bytes).
 void or_dequantise_mxfp4(const uint8_t* codes, const uint8_t* scales, int n, double* out) {
-    for (int i = 0; i < n; ++i) {
-        int c = (i % 2 == 0) ? (codes[i / 2] & 0xF) : (codes[i / 2] >> 4);
-        out[i] = or_e2m1_value(c) * or_e8m0_value(scales[i / 32]);
+    double value[16];
+    for (int c = 0; c < 16; ++c) value[c] = or_e2m1_value(c);
+    for (int b = 0; b < n / 32; ++b) {
+        double sc = or_e8m0_value(scales[b]);
+        for (int i = b * 32; i < b * 32 + 32; ++i) {
+            int c = (i % 2 == 0) ? (codes[i / 2] & 0xF) : (codes[i / 2] >> 4);
+            out[i] = value[c] * sc;
+        }
     }
 }
 
@@ -209,38 +214,50 @@ void or_hot_miss_select(double* M, int L, int E, double threshold, int cap,
 
 // ---------------------------------------------------------------- expert FFN
 
+// An expert's weights dequantised once to f64: gate/up [2F, d] and down [d, F].
+struct DeqExpert {
+    std::vector<double> gu, dn;
+};
+
+static void dequantise_expert(const uint8_t* gu_codes, const uint8_t* gu_scales, const uint8_t* dn_codes,
+                              const uint8_t* dn_scales, int d, int F, DeqExpert* e) {
+    e->gu.resize((size_t)2 * F * d);
+    e->dn.resize((size_t)d * F);
+    for (int r = 0; r < 2 * F; ++r)
+        or_dequantise_mxfp4(gu_codes + (size_t)r * (d / 2), gu_scales + (size_t)r * (d / 32), d,
+                            e->gu.data() + (size_t)r * d);
+    for (int o = 0; o < d; ++o)
+        or_dequantise_mxfp4(dn_codes + (size_t)o * (F / 2), dn_scales + (size_t)o * (F / 32), F,
+                            e->dn.data() + (size_t)o * F);
+}
+
 // One (token, expert) pair of the SwiGLU expert FFN over MXFP4 weights.
 //   xq      = MXFP4(x)                           (activation quantised, OCP rule)
 //   g_f     = sum_i Wg[f,i] * xq_i,  u_f = sum_i Wu[f,i] * xq_i   (f64, exact products)
 //   h_f     = silu(g_f) * u_f,  silu(z) = z / (1 + e^-z)
 //   hq      = MXFP4(h)  (blocks of 32 along the ffn dimension)
 //   y_o     = sum_f Wd[o,f] * hq_f
-// Weights: gate/up codes [2F, d/2] (rows 0..F-1 gate, F..2F-1 up), scales
-// [2F, d/32]; down codes [d, F/2], scales [d, F/32].
-// Optional outputs (may be null): xq codes/scales, h (f64), hq codes/scales.
-void or_expert_pair(const uint16_t* x_bf16, int d, int F,
-                    const uint8_t* gu_codes, const uint8_t* gu_scales,
-                    const uint8_t* dn_codes, const uint8_t* dn_scales,
-                    double* y,
-                    uint8_t* xq_codes, uint8_t* xq_scales, double* h_out,
-                    uint8_t* hq_codes, uint8_t* hq_scales) {
-    std::vector<double> x(d), xq(d), w(d), h(F), hq(F), wd(F);
+// Weights: gate/up rows 0..F-1 gate, F..2F-1 up; down [d, F].
+static void expert_pair_deq(const uint16_t* x_bf16, int d, int F, const DeqExpert& e, double* y,
+                            uint8_t* xq_codes, uint8_t* xq_scales, double* h_out,
+                            uint8_t* hq_codes, uint8_t* hq_scales) {
+    std::vector<double> x(d), xq(d), h(F), hq(F);
     std::vector<uint8_t> xc(d / 2), xs(d / 32), hc(F / 2), hs(F / 32);
     for (int i = 0; i < d; ++i) x[i] = bf16_to_double(x_bf16[i]);
     or_quantise_mxfp4(x.data(), d, xc.data(), xs.data());
     or_dequantise_mxfp4(xc.data(), xs.data(), d, xq.data());
     for (int f = 0; f < F; ++f) {
+        const double* wg = e.gu.data() + (size_t)f * d;
+        const double* wu = e.gu.data() + (size_t)(F + f) * d;
         double g = 0.0, u = 0.0;
-        or_dequantise_mxfp4(gu_codes + (size_t)f * (d / 2), gu_scales + (size_t)f * (d / 32), d, w.data());
-        for (int i = 0; i < d; ++i) g += w[i] * xq[i];
-        or_dequantise_mxfp4(gu_codes + (size_t)(F + f) * (d / 2), gu_scales + (size_t)(F + f) * (d / 32), d, w.data());
-        for (int i = 0; i < d; ++i) u += w[i] * xq[i];
+        for (int i = 0; i < d; ++i) g += wg[i] * xq[i];
+        for (int i = 0; i < d; ++i) u += wu[i] * xq[i];
         h[f] = g / (1.0 + std::exp(-g)) * u;
     }
     or_quantise_mxfp4(h.data(), F, hc.data(), hs.data());
     or_dequantise_mxfp4(hc.data(), hs.data(), F, hq.data());
     for (int o = 0; o < d; ++o) {
-        or_dequantise_mxfp4(dn_codes + (size_t)o * (F / 2), dn_scales + (size_t)o * (F / 32), F, wd.data());
+        const double* wd = e.dn.data() + (size_t)o * F;
         double acc = 0.0;
         for (int f = 0; f < F; ++f) acc += wd[f] * hq[f];
         y[o] = acc;
@@ -252,30 +269,50 @@ void or_expert_pair(const uint16_t* x_bf16, int d, int F,
     if (hq_scales) std::memcpy(hq_scales, hs.data(), F / 32);
 }
 
+void or_expert_pair(const uint16_t* x_bf16, int d, int F,
+                    const uint8_t* gu_codes, const uint8_t* gu_scales,
+                    const uint8_t* dn_codes, const uint8_t* dn_scales,
+                    double* y,
+                    uint8_t* xq_codes, uint8_t* xq_scales, double* h_out,
+                    uint8_t* hq_codes, uint8_t* hq_scales) {
+    DeqExpert e;
+    dequantise_expert(gu_codes, gu_scales, dn_codes, dn_scales, d, F, &e);
+    expert_pair_deq(x_bf16, d, F, e, y, xq_codes, xq_scales, h_out, hq_codes, hq_scales);
+}
+
 // The routed FFN with score-weighted combine for T tokens (README items 1-2;
 // the combine adds a token's picks in its rank order j = 0..k-1).
 // sel_u[t,j] indexes the expert arrays (n_u experts, stacked), -1 = no pick.
 //   out[t] = sum_j sel_w[t,j] * y(t, sel_u[t,j])
+// Each expert is dequantised once; every pick's y is kept, then combined.
 void or_ffn(const uint16_t* x_bf16, const int32_t* sel_u, const double* sel_w,
-            int T, int k, int d, int F,
+            int T, int k, int d, int F, int n_u,
             const uint8_t* gu_codes, const uint8_t* gu_scales,
             const uint8_t* dn_codes, const uint8_t* dn_scales,
             double* out) {
     size_t guc = (size_t)2 * F * (d / 2), gus = (size_t)2 * F * (d / 32);
     size_t dnc = (size_t)d * (F / 2), dns = (size_t)d * (F / 32);
-    std::vector<double> y(d);
+    std::vector<double> y((size_t)T * k * d, 0.0);
+    DeqExpert e;
+    for (int u = 0; u < n_u; ++u) {
+        bool used = false;
+        for (size_t p = 0; p < (size_t)T * k; ++p) used = used || sel_u[p] == u;
+        if (!used) continue;
+        dequantise_expert(gu_codes + u * guc, gu_scales + u * gus, dn_codes + u * dnc, dn_scales + u * dns,
+                          d, F, &e);
+        for (size_t p = 0; p < (size_t)T * k; ++p)
+            if (sel_u[p] == u)
+                expert_pair_deq(x_bf16 + (p / k) * d, d, F, e, y.data() + p * d,
+                                nullptr, nullptr, nullptr, nullptr, nullptr);
+    }
     for (int t = 0; t < T; ++t) {
         double* o = out + (size_t)t * d;
         for (int i = 0; i < d; ++i) o[i] = 0.0;
         for (int j = 0; j < k; ++j) {
-            int u = sel_u[(size_t)t * k + j];
-            if (u < 0) continue;
-            or_expert_pair(x_bf16 + (size_t)t * d, d, F,
-                           gu_codes + u * guc, gu_scales + u * gus,
-                           dn_codes + u * dnc, dn_scales + u * dns,
-                           y.data(), nullptr, nullptr, nullptr, nullptr, nullptr);
-            double w = sel_w[(size_t)t * k + j];
-            for (int i = 0; i < d; ++i) o[i] += w * y[i];
+            size_t p = (size_t)t * k + j;
+            if (sel_u[p] < 0) continue;
+            double w = sel_w[p];
+            for (int i = 0; i < d; ++i) o[i] += w * y[p * d + i];
         }
     }
 }

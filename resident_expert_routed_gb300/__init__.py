@@ -1,0 +1,216 @@
+"""Resident-expert routed MoE layer step on GB300 (sm_103a): Python binding.
+
+Same names as the C ABI in ``include/moe_resident.h``. This module only
+marshals arguments (torch tensors -> device pointers and sizes) and raises on a
+non-OK status; every step of the computation runs in the CUDA kernels of
+``libmoe_resident.so``. There is no CPU path: importing this package without
+the built library raises.
+
+The method is the adaptive expert loading of the TideLM README ("How adaptive
+expert loading works", items 1-3): routing restricted to resident experts with
+next-best substitution, score-weighted demand per (layer, expert), heavy-miss
+extraction for the hot-read ring, and the grouped MXFP4 SwiGLU expert FFN over
+one shared slot arena.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_resident.so")
+
+MOE_OK, MOE_EINVAL, MOE_ECUDA, MOE_ENOMEM, MOE_ETIMEOUT, MOE_EDEVICE, MOE_EUNSUPPORTED = range(7)
+MOE_DEV_BAD_SLOT, MOE_DEV_NAN_SCALE, MOE_DEV_TIMEOUT, MOE_DEV_BAD_TABLE, MOE_DEV_RESIDENT = 0x1, 0x2, 0x4, 0x8, 0x10
+
+# Every symbol the header declares (checked by the CPU test suite).
+EXPORTS = ("moe_route_resident", "moe_demand_accumulate", "moe_hot_miss_select", "moe_expert_ffn_mxfp4",
+           "moe_arena_replan", "moe_ring_install", "moe_workspace_bytes", "moe_replan_workspace_bytes",
+           "moe_device_status", "moe_status_str", "moe_kernel_launches", "moe_profile_enable",
+           "moe_profile_kernel_count", "moe_profile_read", "moe_profile_reset")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn}: {text} (status {status})")
+        self.status = status
+
+
+class MoeArena(ctypes.Structure):
+    """Mirror of ``moe_arena`` (passed by host pointer)."""
+    _fields_ = [("base", ctypes.c_void_p), ("slot_bytes", ctypes.c_int64), ("n_slots", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("ffn", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("off_gu_codes", ctypes.c_int64), ("off_gu_scales", ctypes.c_int64),
+                ("off_dn_codes", ctypes.c_int64), ("off_dn_scales", ctypes.c_int64)]
+
+
+_P, _I, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(path)
+    L.moe_route_resident.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_demand_accumulate.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]
+    L.moe_hot_miss_select.argtypes = [_P, _I, _I, _F, _I, _P, _P, _P, _P]
+    L.moe_expert_ffn_mxfp4.argtypes = [_P, _P, _P, ctypes.POINTER(MoeArena), _I, _I, _P, _P, _SZ, _P]
+    L.moe_arena_replan.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_ring_install.argtypes = [_P, _P, _I, _I, _I, _I, _P]
+    L.moe_workspace_bytes.restype = _SZ
+    L.moe_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
+    L.moe_replan_workspace_bytes.restype = _SZ
+    L.moe_replan_workspace_bytes.argtypes = [_I, _I]
+    L.moe_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
+    L.moe_status_str.restype = ctypes.c_char_p
+    L.moe_status_str.argtypes = [_I]
+    L.moe_kernel_launches.restype = ctypes.c_uint64
+    L.moe_kernel_launches.argtypes = []
+    L.moe_profile_enable.argtypes = [_I]
+    L.moe_profile_kernel_count.restype = _I
+    L.moe_profile_kernel_count.argtypes = []
+    L.moe_profile_read.argtypes = [_I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_int64),
+                                   ctypes.POINTER(ctypes.c_double)]
+    L.moe_profile_reset.restype = None
+    L.moe_profile_reset.argtypes = []
+    for name in ("moe_route_resident", "moe_demand_accumulate", "moe_hot_miss_select", "moe_expert_ffn_mxfp4",
+                 "moe_arena_replan", "moe_ring_install", "moe_device_status", "moe_profile_enable",
+                 "moe_profile_read"):
+        L[name].restype = _I
+    _lib = L
+    return L
+
+
+def _check(fn: str, st: int) -> None:
+    if st != MOE_OK:
+        raise MoeError(fn, st, load().moe_status_str(st).decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+@dataclass
+class Arena:
+    """A device slot arena: ``buf`` uint8 [n_slots * slot_bytes] plus its record layout."""
+    buf: torch.Tensor
+    slot_bytes: int
+    n_slots: int
+    d: int
+    ffn: int
+    off_gu_codes: int
+    off_gu_scales: int
+    off_dn_codes: int
+    off_dn_scales: int
+
+    def struct(self) -> MoeArena:
+        return MoeArena(ctypes.c_void_p(self.buf.data_ptr()), self.slot_bytes, self.n_slots, self.d, self.ffn, 0,
+                        self.off_gu_codes, self.off_gu_scales, self.off_dn_codes, self.off_dn_scales)
+
+
+# ------------------------------------------------------------------ entry points (same names as the C ABI)
+
+def moe_workspace_bytes(T: int, k: int, d: int, ffn: int, E: int, n_slots: int) -> int:
+    return int(load().moe_workspace_bytes(T, k, d, ffn, E, n_slots))
+
+
+def moe_replan_workspace_bytes(L: int, E: int) -> int:
+    return int(load().moe_replan_workspace_bytes(L, E))
+
+
+def moe_route_resident(hidden_bf16, w_router, bias, slot_of, k, want_e, want_s, sel_e, sel_slot, sel_w,
+                       workspace, stream=None) -> None:
+    T, d = hidden_bf16.shape
+    E = w_router.shape[0]
+    _check("moe_route_resident", load().moe_route_resident(
+        _ptr(hidden_bf16), _ptr(w_router), _ptr(bias), _ptr(slot_of), T, d, E, k, _ptr(want_e), _ptr(want_s),
+        _ptr(sel_e), _ptr(sel_slot), _ptr(sel_w), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def moe_demand_accumulate(want_e, want_s, slot_of, layer, demand, miss_max, stream=None) -> None:
+    T, k = want_e.shape
+    L, E = demand.shape
+    _check("moe_demand_accumulate", load().moe_demand_accumulate(
+        _ptr(want_e), _ptr(want_s), _ptr(slot_of), T, k, layer, L, E, _ptr(demand), _ptr(miss_max),
+        _stream(stream)))
+
+
+def moe_hot_miss_select(miss_max, threshold, cap, out_flat, out_share, n_out, stream=None) -> None:
+    L, E = miss_max.shape
+    _check("moe_hot_miss_select", load().moe_hot_miss_select(
+        _ptr(miss_max), L, E, float(threshold), cap, _ptr(out_flat), _ptr(out_share), _ptr(n_out),
+        _stream(stream)))
+
+
+def moe_expert_ffn_mxfp4(hidden_bf16, sel_slot, sel_w, arena: Arena, out, workspace, stream=None) -> None:
+    T = hidden_bf16.shape[0]
+    k = sel_slot.shape[1]
+    st = arena.struct()
+    _check("moe_expert_ffn_mxfp4", load().moe_expert_ffn_mxfp4(
+        _ptr(hidden_bf16), _ptr(sel_slot), _ptr(sel_w), ctypes.byref(st), T, k, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_arena_replan(demand, n_main, slot_of, owner, loads, n_loads, workspace, stream=None) -> None:
+    L, E = demand.shape
+    _check("moe_arena_replan", load().moe_arena_replan(
+        _ptr(demand), L, E, n_main, owner.numel(), _ptr(slot_of), _ptr(owner), _ptr(loads), _ptr(n_loads),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_ring_install(slot_of, owner, ring_slot: int, flat_id: int, stream=None) -> None:
+    _check("moe_ring_install", load().moe_ring_install(
+        _ptr(slot_of), _ptr(owner), ring_slot, flat_id, slot_of.numel(), owner.numel(), _stream(stream)))
+
+
+def moe_device_status(stream=None) -> tuple[int, int]:
+    """(status, raw error bits); reads and clears the device error word."""
+    bits = ctypes.c_uint32(0)
+    st = load().moe_device_status(_stream(stream), ctypes.byref(bits))
+    return st, bits.value
+
+
+def moe_kernel_launches() -> int:
+    return int(load().moe_kernel_launches())
+
+
+def moe_profile_enable(on: bool) -> None:
+    _check("moe_profile_enable", load().moe_profile_enable(1 if on else 0))
+
+
+def moe_profile_reset() -> None:
+    load().moe_profile_reset()
+
+
+def moe_profile_read() -> dict:
+    """{kernel name: (launches, total device ms)} for the launches recorded since the last reset."""
+    L = load()
+    out = {}
+    for kind in range(L.moe_profile_kernel_count()):
+        name = ctypes.c_char_p()
+        n = ctypes.c_int64()
+        ms = ctypes.c_double()
+        _check("moe_profile_read", L.moe_profile_read(kind, ctypes.byref(name), ctypes.byref(n), ctypes.byref(ms)))
+        if n.value:
+            out[name.value.decode()] = (n.value, ms.value)
+    return out

@@ -1,0 +1,344 @@
+// C ABI of the resident-expert routed MoE layer step (include/moe_resident.h).
+//
+// Host-side argument checks, workspace carving, the per-device error word and
+// the launch sequence of each entry point. Every step of the computation runs
+// in the kernels of route.cu, demand.cu, ffn_plan.cu, ffn_gemm.cu and
+// replan.cu; nothing here computes on the host.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+size_t replan_workspace(int n);
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+// One error word per device; its device address is looked up once per device.
+__device__ uint32_t g_err_word;
+
+constexpr int MAX_DEV = 64;
+uint32_t* g_err_ptr[MAX_DEV] = {};
+int g_sm_count[MAX_DEV] = {};
+std::mutex g_mu;
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev < MAX_DEV ? dev : -1;
+}
+
+uint32_t* err_word() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    if (g_err_ptr[dev]) return g_err_ptr[dev];
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<uint32_t*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int bn_for(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128; }
+
+// Workspace of the FFN, carved in this order (every piece 256-byte aligned).
+struct FfnCarve {
+    size_t rank, pair_of_pos, offsets, tile_off, work, n_work, xq, xs, hq, hs, Y, total;
+    int work_max;
+};
+
+FfnCarve ffn_carve(int T, int k, int d, int F, int S) {
+    FfnCarve c{};
+    const size_t P = (size_t)T * k;
+    c.work_max = (int)((P < (size_t)S ? P : (size_t)S) + P / 16 + 1);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+    c.rank = take(P * 4);
+    c.pair_of_pos = take(P * 4);
+    c.offsets = take(((size_t)S + 1) * 4);
+    c.tile_off = take((size_t)S * 4);
+    c.work = take((size_t)c.work_max * 16);
+    c.n_work = take(4);
+    c.xq = take((size_t)T * d / 2);
+    c.xs = take((size_t)T * d / 32);
+    c.hq = take(P * F / 2);
+    c.hs = take(P * F / 32);
+    c.Y = take(P * d * 4);
+    c.total = o;
+    return c;
+}
+
+size_t route_bytes(int T, int E, int d) {
+    return align_up((size_t)route_splits(T, E, d) * T * E * 4, 256);
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ECUDA; }
+
+// ------------------------------------------------------------------ optional per-launch event timing
+const char* const kKernelNames[MK_COUNT] = {"router_logits_partial", "route_select", "demand_accumulate",
+                                            "hot_miss_select", "ffn_plan_quant", "ffn_gemm_gate_up",
+                                            "ffn_gemm_down", "ffn_combine", "arena_replan", "ring_install"};
+struct ProfRec {
+    int kind;
+    cudaEvent_t a, b;
+};
+std::atomic<bool> g_prof_on{false};
+std::mutex g_prof_mu;
+std::vector<ProfRec> g_prof_open;        // recorded, not yet read
+std::vector<cudaEvent_t> g_prof_pool;    // free events
+cudaEvent_t g_prof_pending = nullptr;    // begin event of the launch in flight (per library; one host thread)
+int64_t g_prof_n[MK_COUNT] = {};
+double g_prof_ms[MK_COUNT] = {};
+
+cudaEvent_t prof_event() {
+    if (!g_prof_pool.empty()) {
+        cudaEvent_t e = g_prof_pool.back();
+        g_prof_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+}  // namespace
+
+void moe_prof_begin(int kind, cudaStream_t s) {
+    (void)kind;
+    if (!g_prof_on.load(std::memory_order_relaxed)) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_pending = prof_event();
+    cudaEventRecord(g_prof_pending, s);
+}
+
+void moe_prof_end(int kind, cudaStream_t s) {
+    if (!g_prof_on.load(std::memory_order_relaxed)) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_pending) return;
+    cudaEvent_t b = prof_event();
+    cudaEventRecord(b, s);
+    g_prof_open.push_back({kind, g_prof_pending, b});
+    g_prof_pending = nullptr;
+}
+
+static void prof_drain() {   // caller holds g_prof_mu
+    for (const ProfRec& r : g_prof_open) {
+        float ms = 0.f;
+        cudaEventSynchronize(r.b);
+        cudaEventElapsedTime(&ms, r.a, r.b);
+        g_prof_n[r.kind] += 1;
+        g_prof_ms[r.kind] += ms;
+        g_prof_pool.push_back(r.a);
+        g_prof_pool.push_back(r.b);
+    }
+    g_prof_open.clear();
+}
+
+void moe_count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int moe_sm_count() {
+    const int dev = current_device();
+    if (dev < 0) return 148;
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = n > 0 ? n : 148;
+    }
+    return g_sm_count[dev];
+}
+
+extern "C" {
+
+const char* moe_status_str(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_EINVAL: return "invalid argument";
+        case MOE_ECUDA: return "CUDA error";
+        case MOE_ENOMEM: return "workspace too small";
+        case MOE_ETIMEOUT: return "device wait timed out";
+        case MOE_EDEVICE: return "device reported bad data (slot id, scale byte or table)";
+        case MOE_EUNSUPPORTED: return "size beyond a documented limit";
+    }
+    return "unknown status";
+}
+
+uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status moe_profile_enable(int on) {
+    g_prof_on.store(on != 0);
+    return MOE_OK;
+}
+
+int moe_profile_kernel_count(void) { return MK_COUNT; }
+
+moe_status moe_profile_read(int kind, const char** name, int64_t* launches, double* total_ms) {
+    if (kind < 0 || kind >= MK_COUNT) return MOE_EINVAL;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    prof_drain();
+    if (name) *name = kKernelNames[kind];
+    if (launches) *launches = g_prof_n[kind];
+    if (total_ms) *total_ms = g_prof_ms[kind];
+    return MOE_OK;
+}
+
+void moe_profile_reset(void) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    prof_drain();
+    for (int i = 0; i < MK_COUNT; ++i) { g_prof_n[i] = 0; g_prof_ms[i] = 0.0; }
+}
+
+size_t moe_workspace_bytes(int T, int k, int d, int ffn, int E, int n_slots) {
+    if (T < 1 || k < 1 || d < 1 || E < 1) return 0;
+    size_t r = route_bytes(T, E, d);
+    if (ffn > 0 && n_slots > 0) {
+        const size_t f = ffn_carve(T, k, d, ffn, n_slots).total;
+        if (f > r) r = f;
+    }
+    return r;
+}
+
+size_t moe_replan_workspace_bytes(int L, int E) {
+    if (L < 1 || E < 1) return 0;
+    return replan_workspace(L * E);
+}
+
+moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, const float* bias,
+                              const int32_t* slot_of, int T, int d, int E, int k, int32_t* want_e, float* want_s,
+                              int32_t* sel_e, int32_t* sel_slot, float* sel_w, void* workspace, size_t ws_bytes,
+                              void* stream) {
+    if (!hidden_bf16 || !w_router || !slot_of || !want_e || !want_s || !sel_e || !sel_slot || !sel_w || !workspace)
+        return MOE_EINVAL;
+    if (T < 1 || d < 32 || d % 32 || E < 1 || k < 1 || k > 32 || k > E) return MOE_EINVAL;
+    if (E > 1024) return MOE_EUNSUPPORTED;
+    if ((size_t)T * E > ((size_t)1 << 31)) return MOE_EUNSUPPORTED;
+    if (ws_bytes < route_bytes(T, E, d)) return MOE_ENOMEM;
+    RouteLaunch a{};
+    a.x = static_cast<const uint16_t*>(hidden_bf16);
+    a.w = w_router;
+    a.bias = bias;
+    a.slot_of = slot_of;
+    a.T = T; a.d = d; a.E = E; a.k = k;
+    a.splits = route_splits(T, E, d);
+    a.want_e = want_e; a.want_s = want_s; a.sel_e = sel_e; a.sel_slot = sel_slot; a.sel_w = sel_w;
+    a.partial = static_cast<float*>(workspace);
+    return cuda_status(launch_route(a, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_demand_accumulate(const int32_t* want_e, const float* want_s, const int32_t* slot_of, int T, int k,
+                                 int layer, int L, int E, uint64_t* demand, float* miss_max, void* stream) {
+    if (!want_e || !want_s || !slot_of || !demand || !miss_max) return MOE_EINVAL;
+    if (T < 1 || k < 1 || k > 32 || E < 1 || L < 1 || layer < 0 || layer >= L) return MOE_EINVAL;
+    if (E > 1024) return MOE_EUNSUPPORTED;
+    return cuda_status(launch_demand(want_e, want_s, slot_of, T, k, layer, E,
+                                     reinterpret_cast<unsigned long long*>(demand), miss_max,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_hot_miss_select(float* miss_max, int L, int E, float threshold, int cap, int32_t* out_flat,
+                               float* out_share, int32_t* n_out, void* stream) {
+    if (!miss_max || !n_out || L < 1 || E < 1 || cap < 0) return MOE_EINVAL;
+    if (cap > 0 && (!out_flat || !out_share)) return MOE_EINVAL;
+    if (cap > 1024 || (long)L * E > (1L << 24)) return MOE_EUNSUPPORTED;
+    return cuda_status(launch_hot_miss(miss_max, L * E, threshold, cap, out_flat, out_share, n_out,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot, const float* sel_w,
+                                const moe_arena* arena, int T, int k, float* out, void* workspace, size_t ws_bytes,
+                                void* stream) {
+    if (!hidden_bf16 || !sel_slot || !sel_w || !arena || !out || !workspace || !arena->base) return MOE_EINVAL;
+    const int d = arena->d, F = arena->ffn, S = arena->n_slots;
+    if (T < 1 || k < 1 || k > 32 || d < 128 || F < 128 || d % 128 || F % 128 || S < 1) return MOE_EINVAL;
+    if (arena->slot_bytes <= 0 || arena->slot_bytes % 256) return MOE_EINVAL;
+    const uintptr_t b = reinterpret_cast<uintptr_t>(arena->base);
+    if (b % 256 || arena->off_gu_codes % 256 || arena->off_gu_scales % 256 || arena->off_dn_codes % 256 ||
+        arena->off_dn_scales % 256)
+        return MOE_EINVAL;
+    const int64_t guc = (int64_t)2 * F * d / 2, gus = (int64_t)2 * F * d / 32;
+    const int64_t dnc = (int64_t)d * F / 2, dns = (int64_t)d * F / 32;
+    auto inside = [&](int64_t off, int64_t len) { return off >= 0 && off + len <= arena->slot_bytes; };
+    if (!inside(arena->off_gu_codes, guc) || !inside(arena->off_gu_scales, gus) || !inside(arena->off_dn_codes, dnc) ||
+        !inside(arena->off_dn_scales, dns))
+        return MOE_EINVAL;
+    if (S > 16384 || d > 16384 || F > 16384 || (long)T * k > (1L << 20)) return MOE_EUNSUPPORTED;
+    const FfnCarve c = ffn_carve(T, k, d, F, S);
+    if (ws_bytes < c.total) return MOE_ENOMEM;
+    uint32_t* err = err_word();
+    if (!err) return MOE_ECUDA;
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    FfnLaunch a{};
+    a.x = static_cast<const uint16_t*>(hidden_bf16);
+    a.sel_slot = sel_slot;
+    a.sel_w = sel_w;
+    a.arena = arena;
+    a.T = T; a.k = k; a.d = d; a.F = F; a.S = S;
+    a.bn = bn_for(T);
+    a.out = out;
+    a.rank = reinterpret_cast<int32_t*>(w + c.rank);
+    a.pair_of_pos = reinterpret_cast<int32_t*>(w + c.pair_of_pos);
+    a.offsets = reinterpret_cast<int32_t*>(w + c.offsets);
+    a.tile_off = reinterpret_cast<int32_t*>(w + c.tile_off);
+    a.work = reinterpret_cast<int4*>(w + c.work);
+    a.n_work = reinterpret_cast<int32_t*>(w + c.n_work);
+    a.xq = w + c.xq;
+    a.xs = w + c.xs;
+    a.hq = w + c.hq;
+    a.hs = w + c.hs;
+    a.Y = reinterpret_cast<float*>(w + c.Y);
+    a.work_max = c.work_max;
+    a.err = err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_ffn_plan(a, s);
+    if (e == cudaSuccess) e = launch_ffn_gemms(a, s, nullptr);
+    if (e == cudaSuccess) e = launch_ffn_combine(a, s);
+    return cuda_status(e);
+}
+
+moe_status moe_arena_replan(const uint64_t* demand, int L, int E, int n_main, int n_slots, int32_t* slot_of,
+                            int32_t* owner, int32_t* loads, int32_t* n_loads, void* workspace, size_t ws_bytes,
+                            void* stream) {
+    if (!demand || !slot_of || !owner || !loads || !n_loads || !workspace) return MOE_EINVAL;
+    if (L < 1 || E < 1 || n_main < 1 || n_slots < n_main) return MOE_EINVAL;
+    if ((long)L * E > (1L << 22)) return MOE_EUNSUPPORTED;
+    if (n_main > L * E) return MOE_EINVAL;
+    if (ws_bytes < replan_workspace(L * E)) return MOE_ENOMEM;
+    uint32_t* err = err_word();
+    if (!err) return MOE_ECUDA;
+    return cuda_status(launch_replan(reinterpret_cast<const unsigned long long*>(demand), L * E, n_main, n_slots,
+                                     slot_of, owner, loads, n_loads, workspace, static_cast<cudaStream_t>(stream),
+                                     err));
+}
+
+moe_status moe_ring_install(int32_t* slot_of, int32_t* owner, int ring_slot, int flat_id, int n_flat, int n_slots,
+                            void* stream) {
+    if (!slot_of || !owner || n_flat < 1 || n_slots < 1) return MOE_EINVAL;
+    if (ring_slot < 0 || ring_slot >= n_slots || flat_id < 0 || flat_id >= n_flat) return MOE_EINVAL;
+    uint32_t* err = err_word();
+    if (!err) return MOE_ECUDA;
+    return cuda_status(launch_ring_install(slot_of, owner, ring_slot, flat_id, static_cast<cudaStream_t>(stream), err));
+}
+
+moe_status moe_device_status(void* stream, uint32_t* bits) {
+    uint32_t* err = err_word();
+    if (!err) return MOE_ECUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t h = 0;
+    if (cudaMemcpyAsync(&h, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ECUDA;
+    if (h) {
+        const uint32_t zero = 0;
+        if (cudaMemcpyAsync(err, &zero, 4, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ECUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ECUDA;
+    }
+    if (bits) *bits = h;
+    if (!h) return MOE_OK;
+    return (h & MOE_DEV_TIMEOUT) ? MOE_ETIMEOUT : MOE_EDEVICE;
+}
+
+}  // extern "C"

@@ -1,0 +1,287 @@
+// Shared device helpers for the resident-expert routed MoE kernels (sm_103a).
+//
+// Thin inline-PTX wrappers for mbarriers, TMA, cp.async, and the tcgen05
+// tensor-core / tensor-memory instructions, plus the launcher prototypes each
+// kernel file exports to the C-ABI layer (abi.cu). Nothing here allocates.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_resident.h"
+
+#define MOE_DEV __device__ __forceinline__
+
+// Wall-clock bound on any spin-wait inside a kernel (ns). A healthy wait ends
+// in microseconds; this only exists so that a broken pipeline returns with
+// MOE_DEV_TIMEOUT instead of hanging the GPU.
+#define MOE_WAIT_LIMIT_NS 2000000000ull
+
+// ------------------------------------------------------------------ basic
+
+MOE_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+MOE_DEV uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+MOE_DEV float bf16_bits_to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// 2^p as a float for p in [-127, 127] (exact; 2^-127 is subnormal).
+MOE_DEV float exp2_int(int p) {
+    return (p >= -126) ? __uint_as_float((uint32_t)(p + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// floor(log2(a)) for finite a > 0, from the bit pattern.
+MOE_DEV int floor_log2_pos(float a) {
+    uint32_t u = __float_as_uint(a);
+    int e = (int)((u >> 23) & 0xFF);
+    if (e != 0) return e - 127;
+    uint32_t m = u & 0x7FFFFF;                  // subnormal: value m * 2^-149
+    return (31 - __clz(m)) - 149;
+}
+
+// OCP MX v1.0 MXFP4: shared exponent of a block from its amax, clamped to
+// [-127, 127]; an all-zero block takes -127 (scale byte 0).
+MOE_DEV int mx_shared_exp(float amax) {
+    if (!(amax > 0.0f)) return -127;
+    int X = floor_log2_pos(amax) - 2;
+    return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+
+// Round |a| to the e2m1 grid {0,.5,1,1.5,2,3,4,6}: nearest, ties to the even
+// code, saturating at 6. Midpoints between codes c and c+1 round up when c is
+// odd (>=) and down when c is even (>).
+MOE_DEV uint32_t e2m1_mag_code(float a) {
+    return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) + (uint32_t)(a >= 1.75f) +
+           (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
+}
+
+MOE_DEV uint32_t e2m1_code(float v, float inv_scale) {
+    return e2m1_mag_code(fabsf(v * inv_scale)) | (v < 0.0f ? 8u : 0u);
+}
+
+MOE_DEV void record_error(uint32_t* err, uint32_t bits) {
+    if (err) atomicOr(err, bits);
+}
+
+// ------------------------------------------------------------------ mbarrier
+
+MOE_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+MOE_DEV void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+MOE_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity. Returns false (after
+// raising the CTA's abort flag) when the wall-clock limit passes or another
+// role of the CTA has already aborted.
+MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 255u) {
+            if (*abort_flag) return false;
+            uint64_t now = global_timer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > MOE_WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// The same wait for all 32 lanes of a warp; the outcome is made warp-uniform
+// so that a time-out can never split a warp across different sync points.
+MOE_DEV bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    const bool ok = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xFFFFFFFFu, ok) != 0;
+}
+
+MOE_DEV void fence_barrier_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+MOE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+MOE_DEV void named_bar_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------------ TMA and cp.async
+
+MOE_DEV void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+MOE_DEV void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 16-byte async copy global -> shared; src_bytes < 16 zero-fills the rest.
+MOE_DEV void cp_async_16(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(src_bytes)
+                 : "memory");
+}
+
+MOE_DEV void cp_async_4(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(src_bytes)
+                 : "memory");
+}
+
+MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+MOE_DEV void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05
+
+MOE_DEV void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+MOE_DEV void tmem_relinquish() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory"); }
+MOE_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+MOE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Arrive (once) on an mbarrier when every tcgen05 op issued so far by this thread has completed.
+MOE_DEV void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Copy one 32-row x 16-byte scale-factor atom from shared memory into four
+// TMEM columns, replicated into all four 32-lane quadrants.
+MOE_DEV void tc_cp_sf_atom(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, e2m1 x e2m1 with e8m0 block-32 scales from TMEM.
+MOE_DEV void tc_mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
+                         uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Each lane of the warp reads 16 consecutive 32-bit columns of its own TMEM lane.
+MOE_DEV void tc_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+MOE_DEV void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major operand tile with 128-byte rows in
+// the 128-byte swizzle layout written by TMA (8-row groups 1024 B apart).
+MOE_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(16u >> 4) << 16;      // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024u >> 4) << 32;    // stride byte offset: next 8-row group
+    d |= (uint64_t)1 << 46;               // descriptor version for the sm_100 family
+    d |= (uint64_t)2 << 61;               // 128-byte swizzle
+    return d;
+}
+
+// Descriptor of a 32-row x 16-byte scale atom stored densely (no swizzle).
+MOE_DEV uint64_t smem_desc_sf(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(128u >> 4) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Instruction descriptor for kind::mxf4 (e2m1 x e2m1, e8m0 scales, fp32
+// accumulator), both operands K-major, M = 128, N = n; sfid selects the byte
+// pair of the scale column used by this MMA (0 or 2).
+__host__ __device__ constexpr uint32_t idesc_mxf4(int n, int sfid_a, int sfid_b) {
+    return ((uint32_t)(sfid_b & 3) << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(128 >> 4) << 24) | ((uint32_t)(sfid_a & 3) << 29);
+}
+
+// ------------------------------------------------------------------ launchers (host side)
+
+struct RouteLaunch {
+    const uint16_t* x; const float* w; const float* bias; const int32_t* slot_of;
+    int T, d, E, k, splits;
+    int32_t* want_e; float* want_s; int32_t* sel_e; int32_t* sel_slot; float* sel_w;
+    float* partial;
+};
+cudaError_t launch_route(const RouteLaunch& a, cudaStream_t s);
+int route_splits(int T, int E, int d);
+
+cudaError_t launch_demand(const int32_t* want_e, const float* want_s, const int32_t* slot_of, int T, int k,
+                          int layer, int E, unsigned long long* demand, float* miss_max, cudaStream_t s);
+cudaError_t launch_hot_miss(float* miss_max, int n, float threshold, int cap, int32_t* out_flat, float* out_share,
+                            int32_t* n_out, cudaStream_t s);
+
+struct FfnLaunch {
+    const uint16_t* x; const int32_t* sel_slot; const float* sel_w; const moe_arena* arena;
+    int T, k, d, F, S, bn;
+    float* out;
+    // workspace
+    int32_t* rank; int32_t* pair_of_pos; int32_t* offsets; int32_t* tile_off; int4* work; int32_t* n_work;
+    uint8_t* xq; uint8_t* xs; uint8_t* hq; uint8_t* hs; float* Y;
+    int work_max;
+    uint32_t* err;
+};
+cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s);
+cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches);
+cudaError_t launch_ffn_combine(const FfnLaunch& a, cudaStream_t s);
+
+cudaError_t launch_replan(const unsigned long long* demand, int n, int n_main, int n_slots, int32_t* slot_of,
+                          int32_t* owner, int32_t* loads, int32_t* n_loads, void* ws, cudaStream_t s,
+                          uint32_t* err);
+cudaError_t launch_ring_install(int32_t* slot_of, int32_t* owner, int ring_slot, int flat, cudaStream_t s,
+                                uint32_t* err);
+
+// Kernel launch counter kept by abi.cu.
+void moe_count_launches(int n);
+int moe_sm_count();
+
+// Kernel kinds for the optional per-launch event timing (abi.cu).
+enum MoeKernelKind {
+    MK_ROUTER_LOGITS = 0, MK_ROUTE_SELECT, MK_DEMAND, MK_HOT_MISS, MK_PLAN_QUANT, MK_GEMM_GATE_UP,
+    MK_GEMM_DOWN, MK_COMBINE, MK_REPLAN, MK_RING, MK_COUNT
+};
+void moe_prof_begin(int kind, cudaStream_t s);
+void moe_prof_end(int kind, cudaStream_t s);

@@ -1,0 +1,119 @@
+// Demand accumulation and the heavy-miss list.
+//
+// TideLM README, "How adaptive expert loading works":
+//   item 1  every routed pick the router wants, resident or not, is recorded
+//           per (layer, expert) weighted by its routing score;
+//   item 2  the demand of a substituted (missing) pick still counts;
+//   item 3  a miss that would have carried a large share of a token's routing
+//           weight (>= 0.2, at most 16 a step) is a candidate for a hot read.
+//
+// demand_accumulate: shared-memory histograms over the E experts of one layer
+// (u64 fixed point in units of 2^-40, and the max miss share as float bits),
+// flushed with one global atomic per touched expert. Integer sums make the
+// result independent of the order of the adds.
+// hot_miss_select: one CTA ranks the (layer, expert) miss shares with a
+// 64-bit key (share bits, inverted flat index) in `cap` block-wide arg-max
+// rounds, then clears the shares for the next step.
+#include "common.cuh"
+
+namespace {
+
+__global__ void __launch_bounds__(512) demand_accumulate(const int32_t* __restrict__ want_e,
+                                                         const float* __restrict__ want_s,
+                                                         const int32_t* __restrict__ slot_of, int P, int E,
+                                                         unsigned long long* __restrict__ demand,
+                                                         float* __restrict__ miss_max) {
+    extern __shared__ unsigned long long hist[];                 // [E] demand, then [E] miss bits
+    uint32_t* mbits = reinterpret_cast<uint32_t*>(hist + E);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) { hist[e] = 0ull; mbits[e] = 0u; }
+    __syncthreads();
+    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P; p += gridDim.x * blockDim.x) {
+        const int e = want_e[p];
+        if (e < 0 || e >= E) continue;
+        const float s = want_s[p];
+        atomicAdd(&hist[e], __float2ull_rn(s * 1099511627776.0f));      // s * 2^40
+        if (slot_of[e] < 0) atomicMax(&mbits[e], __float_as_uint(s));   // s >= 0: bits order = value order
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        if (hist[e]) atomicAdd(&demand[e], hist[e]);
+        if (mbits[e]) atomicMax(reinterpret_cast<uint32_t*>(miss_max) + e, mbits[e]);
+    }
+}
+
+__device__ __forceinline__ unsigned long long miss_key(const float* M, int f, float thr) {
+    const float m = M[f];
+    if (!(m >= thr)) return 0ull;
+    return ((unsigned long long)__float_as_uint(m) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)f);
+}
+
+__global__ void __launch_bounds__(1024) hot_miss_select(float* __restrict__ M, int n, float thr, int cap,
+                                                        int32_t* __restrict__ out_flat,
+                                                        float* __restrict__ out_share, int32_t* __restrict__ n_out) {
+    __shared__ unsigned long long wbest[32];
+    __shared__ unsigned long long picked;
+    __shared__ int count;
+    if (threadIdx.x == 0) { picked = ~0ull; count = 0; }
+    __syncthreads();
+    for (int j = 0; j < cap; ++j) {
+        const unsigned long long prev = picked;
+        unsigned long long best = 0ull;
+        for (int f = threadIdx.x; f < n; f += blockDim.x) {
+            const unsigned long long key = miss_key(M, f, thr);
+            if (key < prev && key > best) best = key;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+            best = o > best ? o : best;
+        }
+        if ((threadIdx.x & 31) == 0) wbest[threadIdx.x >> 5] = best;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            unsigned long long b = threadIdx.x < (blockDim.x >> 5) ? wbest[threadIdx.x] : 0ull;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, b, off);
+                b = o > b ? o : b;
+            }
+            if (threadIdx.x == 0) {
+                if (b != 0ull) {
+                    out_flat[count] = (int32_t)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
+                    out_share[count] = __uint_as_float((uint32_t)(b >> 32));
+                    ++count;
+                }
+                picked = b;
+            }
+        }
+        __syncthreads();
+        if (picked == 0ull) break;
+    }
+    if (threadIdx.x == 0) *n_out = count;
+    __syncthreads();
+    for (int f = threadIdx.x; f < n; f += blockDim.x) M[f] = 0.0f;
+}
+
+}  // namespace
+
+cudaError_t launch_demand(const int32_t* want_e, const float* want_s, const int32_t* slot_of, int T, int k,
+                          int layer, int E, unsigned long long* demand, float* miss_max, cudaStream_t s) {
+    const int P = T * k;
+    int grid = (P + 511) / 512;
+    if (grid > 2 * moe_sm_count()) grid = 2 * moe_sm_count();
+    const size_t smem = (size_t)E * (sizeof(unsigned long long) + sizeof(uint32_t));
+    moe_prof_begin(MK_DEMAND, s);
+    demand_accumulate<<<grid, 512, smem, s>>>(want_e, want_s, slot_of, P, E, demand + (size_t)layer * E,
+                                              miss_max + (size_t)layer * E);
+    moe_prof_end(MK_DEMAND, s);
+    moe_count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_hot_miss(float* miss_max, int n, float threshold, int cap, int32_t* out_flat, float* out_share,
+                            int32_t* n_out, cudaStream_t s) {
+    moe_prof_begin(MK_HOT_MISS, s);
+    hot_miss_select<<<1, 1024, 0, s>>>(miss_max, n, threshold, cap, out_flat, out_share, n_out);
+    moe_prof_end(MK_HOT_MISS, s);
+    moe_count_launches(1);
+    return cudaGetLastError();
+}

@@ -1,0 +1,420 @@
+// Grouped expert GEMMs over the MXFP4 slot arena on the 5th-generation tensor
+// cores (tcgen05, kind::mxf4 block-scaled MMA, accumulators in TMEM).
+//
+// TideLM README: the experts are "native MXFP4" (profile table) and live in
+// one arena of slots shared by all layers (item 1); the picks of a step are
+// routed only to resident slots (item 2). One launch per GEMM covers every
+// used slot: the work list from ffn_plan names (slot, first row, rows) groups.
+//
+//   gate/up (MODE 1): for 64 ffn features f0..f0+63 of one slot, D = [Wg; Wu]
+//       rows (64 gate + 64 up = M 128) x the group's activation rows (N), K = d;
+//       epilogue: h = silu(g) * u, re-quantised to MXFP4 in blocks of 32
+//       features (OCP MX v1.0 rule) into the hq workspace.
+//   down (MODE 2): for 128 output rows d0..d0+127, D = Wd rows x hq rows,
+//       K = ffn; epilogue: fp32 rows Y[pair] (combined later in pick order).
+//
+// The weight tile is the MMA's A operand (M = 128) and the few routed rows the
+// B operand (N = 16..128), so a decode-sized group still streams whole weight
+// tiles at full width. Per CTA (persistent over work items, 192 threads):
+//   warp 4     producer: TMA (128-byte swizzle) of the weight codes from the
+//              slot; cp.async of the routed activation rows (gathered by index,
+//              swizzled by hand), of the weight scales and of the activation
+//              scales into 32x16-byte scale atoms;
+//   warp 5     TMEM allocator; lane 0 issues tcgen05.cp (scales -> TMEM) and
+//              tcgen05.mma, and commits to the stage / accumulator barriers;
+//   warps 0-3  epilogue: tcgen05.ld of their 32-lane quadrant of the
+//              double-buffered accumulator, then the per-mode epilogue.
+// Every wait is bounded (MOE_WAIT_LIMIT_NS); on expiry the CTA raises its
+// abort flag, every role leaves its loop, TMEM is freed and the device error
+// word gets MOE_DEV_TIMEOUT.
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace {
+
+struct GemmArgs {
+    const uint8_t* arena;
+    int64_t slot_bytes;
+    int64_t off_scales;          // this GEMM's weight scales within a slot
+    int K;                       // reduction length: d (gate/up) or ffn (down)
+    int m_tiles;
+    int F;                       // ffn
+    int d;                       // hidden size
+    int k;                       // picks per token
+    const int4* work;
+    const int32_t* n_work;
+    const int32_t* pair_of_pos;
+    const uint8_t* b_codes;      // gate/up: xq [T, d/2];  down: hq [P, ffn/2]
+    const uint8_t* b_scales;     // gate/up: xs [T, d/32]; down: hs [P, ffn/32]
+    uint8_t* hq;
+    uint8_t* hs;
+    float* Y;
+    uint32_t* err;
+};
+
+template <int MODE, int BN, int NS>
+struct Cfg {
+    static constexpr int A_BYTES = 128 * 128;     // 128 rows x 128 B = 256 e2m1 along K
+    static constexpr int B_BYTES = BN * 128;
+    static constexpr int SF_BYTES = 2048;         // A atom 0, A atom 1, B atom 0, B atom 1 (512 B each)
+    static constexpr int XCH_FLOATS = MODE == 1 ? 128 * (BN + 1) : 0;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + NS * A_BYTES;
+    static constexpr int OFF_SF = OFF_B + NS * B_BYTES;
+    static constexpr int OFF_XCH = OFF_SF + NS * SF_BYTES;
+    static constexpr int OFF_ROWB = OFF_XCH + XCH_FLOATS * 4;
+    static constexpr int OFF_BAR = (OFF_ROWB + BN * 4 + 7) / 8 * 8;
+    static constexpr int N_BARS = 2 * NS + 4 + 2;
+    static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+    static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
+    static constexpr int TMEM_USED = 2 * BN + 16 * NS;
+    static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
+                                   : TMEM_USED <= 256 ? 256 : 512;
+    static constexpr int LAG = NS - 1 < 2 ? NS - 1 : 2;   // cp.async groups kept in flight
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "BN");
+    static_assert(TMEM_USED <= 512, "TMEM");
+};
+
+template <int MODE, int BN, int NS>
+__global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant__ CUtensorMap tmap, const GemmArgs a) {
+    using C = Cfg<MODE, BN, NS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* empty = full + NS;
+    uint64_t* accf = empty + NS;
+    uint64_t* acce = accf + 2;
+    uint64_t* xw = acce + 2;
+    uint64_t* xr = xw + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    int32_t* rowB = reinterpret_cast<int32_t*>(smem + C::OFF_ROWB);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 33); mbar_init(&empty[s], 1); }
+        for (int b = 0; b < 2; ++b) { mbar_init(&accf[b], 1); mbar_init(&acce[b], 4); }
+        mbar_init(xw, 4);
+        mbar_init(xr, 4);
+        *abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&tmap);
+    }
+    if (warp == 5) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_items = *a.n_work * a.m_tiles;
+    const int nk = (a.K + 255) / 256;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        const int K2 = a.K / 2, K32 = a.K / 32;
+        uint32_t it = 0;
+        bool ok_run = true;
+        for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x) {
+            const int4 w = a.work[item / a.m_tiles];
+            const int mt = item % a.m_tiles;
+            const int slot = w.x, pos0 = w.y, nv = w.z;
+            __syncwarp();
+            for (int n = lane; n < BN; n += 32) {
+                int r = -1;
+                if (n < nv) r = MODE == 1 ? a.pair_of_pos[pos0 + n] / a.k : pos0 + n;
+                rowB[n] = r;
+            }
+            __syncwarp();
+            const uint8_t* sfa = a.arena + (size_t)slot * a.slot_bytes + a.off_scales;
+            const int yA0 = MODE == 1 ? mt * 64 : mt * 128;
+            const int yA1 = MODE == 1 ? a.F + mt * 64 : mt * 128 + 64;
+            for (int kc = 0; kc < nk; ++kc, ++it) {
+                const int s = (int)(it % NS);
+                const uint32_t r = it / NS;
+                if (!warp_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
+                uint8_t* As = smem + C::OFF_A + s * C::A_BYTES;
+                uint8_t* Bs = smem + C::OFF_B + s * C::B_BYTES;
+                uint8_t* SFs = smem + C::OFF_SF + s * C::SF_BYTES;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[s], C::A_BYTES);
+                    tma_load_3d(As, &tmap, &full[s], kc * 128, yA0, slot);
+                    tma_load_3d(As + 64 * 128, &tmap, &full[s], kc * 128, yA1, slot);
+                }
+                for (int idx = lane; idx < BN * 8; idx += 32) {          // activation rows, 16 B chunks
+                    const int n = idx >> 3, c = idx & 7;
+                    const int row = rowB[n];
+                    const int kb = kc * 128 + c * 16;
+                    const bool ok = row >= 0 && kb < K2;
+                    const uint8_t* src = ok ? a.b_codes + (size_t)row * K2 + kb : a.b_codes;
+                    cp_async_16(Bs + n * 128 + ((c ^ (n & 7)) << 4), src, ok ? 16u : 0u);
+                }
+                for (int idx = lane; idx < 256; idx += 32) {             // weight scales: 128 rows x 2 groups
+                    const int row = idx >> 1, g = idx & 1;
+                    const int kb = kc * 8 + g * 4;
+                    const bool ok = kb < K32;
+                    const int grow = MODE == 1 ? (row < 64 ? mt * 64 + row : a.F + mt * 64 + (row - 64))
+                                               : mt * 128 + row;
+                    const uint8_t* src = ok ? sfa + (size_t)grow * K32 + kb : sfa;
+                    cp_async_4(SFs + g * 512 + (row & 31) * 16 + (row >> 5) * 4, src, ok ? 4u : 0u);
+                }
+                for (int idx = lane; idx < BN * 2; idx += 32) {          // activation scales
+                    const int n = idx >> 1, g = idx & 1;
+                    const int row = rowB[n];
+                    const int kb = kc * 8 + g * 4;
+                    const bool ok = row >= 0 && kb < K32;
+                    const uint8_t* src = ok ? a.b_scales + (size_t)row * K32 + kb : a.b_scales;
+                    cp_async_4(SFs + 1024 + g * 512 + (n & 31) * 16 + (n >> 5) * 4, src, ok ? 4u : 0u);
+                }
+                cp_async_commit();
+                if (it >= (uint32_t)C::LAG) {
+                    cp_async_wait<C::LAG>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(&full[(it - C::LAG) % NS]);
+                }
+            }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        for (uint32_t j = it > (uint32_t)C::LAG ? it - C::LAG : 0u; j < it; ++j) mbar_arrive(&full[j % NS]);
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, j = 0;
+            bool ok_run = true;
+            for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x, ++j) {
+                const int nv = a.work[item / a.m_tiles].z;
+                const int N = (nv + 15) & ~15;
+                const int b = j & 1;
+                const uint32_t u = j >> 1;
+                if (!mbar_wait(&acce[b], (u & 1) ^ 1, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t dt = tmem + b * BN;
+                for (int kc = 0; kc < nk; ++kc, ++it) {
+                    const int s = (int)(it % NS);
+                    const uint32_t r = it / NS;
+                    if (!mbar_wait(&full[s], r & 1, abort_flag)) { ok_run = false; break; }
+                    tc_fence_after();
+                    const int rem = (a.K - kc * 256) / 64;
+                    const int ksteps = rem < 4 ? rem : 4;
+                    const uint32_t sfc = tmem + 2 * BN + s * 16;
+                    const uint32_t sfs = smem_u32(smem + C::OFF_SF + s * C::SF_BYTES);
+                    tc_cp_sf_atom(sfc + 0, smem_desc_sf(sfs));
+                    tc_cp_sf_atom(sfc + 8, smem_desc_sf(sfs + 1024));
+                    if (ksteps > 2) {
+                        tc_cp_sf_atom(sfc + 4, smem_desc_sf(sfs + 512));
+                        tc_cp_sf_atom(sfc + 12, smem_desc_sf(sfs + 1536));
+                    }
+                    const uint32_t as = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
+                    const uint32_t bs = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
+                    for (int kk = 0; kk < ksteps; ++kk) {
+                        const int sfid = (kk & 1) * 2;
+                        tc_mma_mxf4(dt, smem_desc_sw128(as + kk * 32), smem_desc_sw128(bs + kk * 32),
+                                    idesc_mxf4(N, sfid, sfid), sfc + (kk >> 1) * 4, sfc + 8 + (kk >> 1) * 4,
+                                    (kc | kk) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(&empty[s]);
+                }
+                if (ok_run) tc_commit(&accf[b]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 0..3)
+        float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
+        uint32_t j = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
+            const int4 w = a.work[item / a.m_tiles];
+            const int mt = item % a.m_tiles;
+            const int pos0 = w.y, nv = w.z;
+            const int b = j & 1;
+            const uint32_t u = j >> 1;
+            if (!warp_wait(&accf[b], u & 1, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16) + b * BN;
+            if (MODE == 1) {
+                if (!warp_wait(xr, (j & 1) ^ 1, abort_flag)) break;
+                for (int c0 = 0; c0 < BN && c0 < nv; c0 += 16) {
+                    uint32_t v[16];
+                    tc_ld_x16(trow + c0, v);
+                    tc_wait_ld();
+                    float* dst = xch + (warp * 32 + lane) * (BN + 1) + c0;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) dst[i] = __uint_as_float(v[i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) { mbar_arrive(&acce[b]); mbar_arrive(xw); }
+                if (!warp_wait(xw, j & 1, abort_flag)) break;
+                for (int uu = warp; uu < nv * 2; uu += 4) {
+                    const int n = uu >> 1, bb = uu & 1;
+                    const int fl = bb * 32 + lane;
+                    const float g = xch[fl * (BN + 1) + n];
+                    const float up = xch[(64 + fl) * (BN + 1) + n];
+                    const float h = g / (1.0f + expf(-g)) * up;
+                    float amax = fabsf(h);
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+                    const int X = mx_shared_exp(amax);
+                    const uint32_t code = e2m1_code(h, exp2_int(-X));
+                    const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+                    const uint32_t byte = (code | (hi << 4)) & 0xFFu;
+                    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
+                    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
+                    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 6);
+                    const size_t pos = (size_t)(pos0 + n);
+                    const int f0 = mt * 64 + bb * 32;
+                    if ((lane & 7) == 0)
+                        *reinterpret_cast<uint32_t*>(a.hq + pos * (a.F / 2) + f0 / 2 + (lane >> 3) * 4) =
+                            byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                    if (lane == 0) a.hs[pos * (a.F / 32) + f0 / 32] = (uint8_t)(X + 127);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xr);
+            } else {
+                const int dr = mt * 128 + warp * 32 + lane;
+                for (int c0 = 0; c0 < BN && c0 < nv; c0 += 16) {
+                    uint32_t v[16];
+                    tc_ld_x16(trow + c0, v);
+                    tc_wait_ld();
+                    const int myp = (lane < 16 && c0 + lane < nv) ? a.pair_of_pos[pos0 + c0 + lane] : 0;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int pp = __shfl_sync(0xFFFFFFFFu, myp, i);
+                        if (c0 + i < nv) a.Y[(size_t)pp * a.d + dr] = __uint_as_float(v[i]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acce[b]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag) record_error(a.err, MOE_DEV_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D view of one weight region of every slot: (row bytes, rows, slots); box
+// 128 bytes x 64 rows x 1 slot, 128-byte swizzle.
+cudaError_t make_weight_map(CUtensorMap* m, const uint8_t* base, uint64_t row_bytes, uint64_t rows, uint64_t slots,
+                            uint64_t slot_bytes) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[3] = {row_bytes, rows, slots};
+    cuuint64_t strides[2] = {row_bytes, slot_bytes};
+    cuuint32_t box[3] = {128, 64, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int MODE, int BN, int NS>
+cudaError_t launch_one(const CUtensorMap& map, const GemmArgs& g, long max_items, cudaStream_t s) {
+    using C = Cfg<MODE, BN, NS>;
+    auto kern = ffn_gemm_kernel<MODE, BN, NS>;
+    static int occ_cache[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int occ = dev < 64 ? occ_cache[dev] : 0;
+    if (occ == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 192, C::SMEM);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+        const int tmem_fit = 512 / C::TMEM_COLS;
+        if (occ > tmem_fit) occ = tmem_fit;
+        if (dev < 64) occ_cache[dev] = occ;
+    }
+    if (max_items <= 0) return cudaSuccess;
+    long grid = (long)occ * moe_sm_count();
+    if (grid > max_items) grid = max_items;
+    moe_prof_begin(MODE == 1 ? MK_GEMM_GATE_UP : MK_GEMM_DOWN, s);
+    kern<<<(unsigned)grid, 192, C::SMEM, s>>>(map, g);
+    moe_prof_end(MODE == 1 ? MK_GEMM_GATE_UP : MK_GEMM_DOWN, s);
+    moe_count_launches(1);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& map, const GemmArgs& g, long max_items, int bn, cudaStream_t s) {
+    switch (bn) {
+        case 16: return launch_one<MODE, 16, 4>(map, g, max_items, s);
+        case 32: return launch_one<MODE, 32, 4>(map, g, max_items, s);
+        case 64: return MODE == 1 ? launch_one<MODE, 64, 3>(map, g, max_items, s)
+                                  : launch_one<MODE, 64, 4>(map, g, max_items, s);
+        default: return launch_one<MODE, 128, 4>(map, g, max_items, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches) {
+    const moe_arena& ar = *a.arena;
+    const uint8_t* base = static_cast<const uint8_t*>(ar.base);
+    CUtensorMap map_gu, map_dn;
+    cudaError_t e = make_weight_map(&map_gu, base + ar.off_gu_codes, (uint64_t)a.d / 2, (uint64_t)2 * a.F,
+                                    (uint64_t)ar.n_slots, (uint64_t)ar.slot_bytes);
+    if (e != cudaSuccess) return e;
+    e = make_weight_map(&map_dn, base + ar.off_dn_codes, (uint64_t)a.F / 2, (uint64_t)a.d, (uint64_t)ar.n_slots,
+                        (uint64_t)ar.slot_bytes);
+    if (e != cudaSuccess) return e;
+
+    GemmArgs g{};
+    g.arena = base;
+    g.slot_bytes = ar.slot_bytes;
+    g.F = a.F;
+    g.d = a.d;
+    g.k = a.k;
+    g.work = a.work;
+    g.n_work = a.n_work;
+    g.pair_of_pos = a.pair_of_pos;
+    g.err = a.err;
+
+    GemmArgs g1 = g;       // gate/up + SwiGLU
+    g1.off_scales = ar.off_gu_scales;
+    g1.K = a.d;
+    g1.m_tiles = a.F / 64;
+    g1.b_codes = a.xq;
+    g1.b_scales = a.xs;
+    g1.hq = a.hq;
+    g1.hs = a.hs;
+    e = launch_mode<1>(map_gu, g1, (long)a.work_max * g1.m_tiles, a.bn, s);
+    if (e != cudaSuccess) return e;
+
+    GemmArgs g2 = g;       // down
+    g2.off_scales = ar.off_dn_scales;
+    g2.K = a.F;
+    g2.m_tiles = a.d / 128;
+    g2.b_codes = a.hq;
+    g2.b_scales = a.hs;
+    g2.Y = a.Y;
+    e = launch_mode<2>(map_dn, g2, (long)a.work_max * g2.m_tiles, a.bn, s);
+    if (n_launches) *n_launches = 2;
+    return e;
+}

@@ -1,0 +1,198 @@
+// Router scoring and resident-only top-k with substitution.
+//
+// TideLM README, "How adaptive expert loading works", items 1-2: the router
+// scores every token against all experts; the wanted picks are the top-k over
+// all of them, and the picks actually routed are the top-k over the resident
+// experts only, so a missing pick is replaced by the next-best resident one.
+//
+// Two kernels:
+//   router_logits_partial  fp32 register-tiled GEMM over a K slice:
+//                          partial[z, t, e] = sum_{i in slice z} x[t,i] W[e,i]
+//   route_select           one warp per token: sum the slices in a fixed order
+//                          (+ bias), softmax, wanted and resident top-k by
+//                          warp-shuffle arg-max rounds.
+// The K split keeps >= ~256 CTAs streaming W_r at decode sizes; the partials
+// are small and stay in L2.
+#include "common.cuh"
+
+namespace {
+
+constexpr int BT = 64, BE = 64, BK = 32;
+
+__global__ void __launch_bounds__(256) router_logits_partial(const uint16_t* __restrict__ x,
+                                                             const float* __restrict__ W, int T, int d, int E,
+                                                             int kslice, float* __restrict__ partial) {
+    __shared__ float xs[BK][BT + 4];
+    __shared__ float ws[BK][BE + 4];
+    const int tid = threadIdx.x;
+    const int tx = tid & 15, ty = tid >> 4;       // 16 x 16 threads, 4 x 4 outputs each
+    const int e0 = blockIdx.x * BE, t0 = blockIdx.y * BT;
+    const int kbeg = blockIdx.z * kslice, kend = kbeg + kslice;
+    float acc[4][4] = {};
+    const int lr = tid >> 2, lc = (tid & 3) * 8;   // loader: row, 8 consecutive k
+    for (int k0 = kbeg; k0 < kend; k0 += BK) {
+        {   // x tile: 64 tokens x 32 bf16 -> xs[k][t]
+            int t = t0 + lr;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (t < T) v = *reinterpret_cast<const uint4*>(x + (size_t)t * d + k0 + lc);
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xs[lc + i][lr] = bf16_bits_to_float(h[i]);
+        }
+        {   // W tile: 64 experts x 32 fp32 -> ws[k][e]
+            int e = e0 + lr;
+            float4 a = make_float4(0, 0, 0, 0), b = a;
+            if (e < E) {
+                a = *reinterpret_cast<const float4*>(W + (size_t)e * d + k0 + lc);
+                b = *reinterpret_cast<const float4*>(W + (size_t)e * d + k0 + lc + 4);
+            }
+            ws[lc + 0][lr] = a.x; ws[lc + 1][lr] = a.y; ws[lc + 2][lr] = a.z; ws[lc + 3][lr] = a.w;
+            ws[lc + 4][lr] = b.x; ws[lc + 5][lr] = b.y; ws[lc + 6][lr] = b.z; ws[lc + 7][lr] = b.w;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < BK; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+    float* out = partial + (size_t)blockIdx.z * T * E;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int t = t0 + ty * 4 + i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            int e = e0 + tx * 4 + j;
+            if (e < E) out[(size_t)t * E + e] = acc[i][j];
+        }
+    }
+}
+
+// Arg-max across the warp of (value, index): larger value wins, ties to the
+// lower index. Index INT_MAX marks "nothing left".
+__device__ __forceinline__ void warp_argmax(float& v, int& idx) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        float ov = __shfl_xor_sync(0xFFFFFFFFu, v, off);
+        int oi = __shfl_xor_sync(0xFFFFFFFFu, idx, off);
+        if (ov > v || (ov == v && oi < idx)) { v = ov; idx = oi; }
+    }
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256) route_select(const float* __restrict__ partial, int splits,
+                                                    const float* __restrict__ bias,
+                                                    const int32_t* __restrict__ slot_of, int T, int E, int k,
+                                                    int32_t* __restrict__ want_e, float* __restrict__ want_s,
+                                                    int32_t* __restrict__ sel_e, int32_t* __restrict__ sel_slot,
+                                                    float* __restrict__ sel_w) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const float NEG = -__int_as_float(0x7F800000);   // -inf
+    float lg[VPL];
+    int slot[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        int e = lane + 32 * i;
+        lg[i] = NEG;
+        slot[i] = -1;
+        if (e < E) {
+            float acc = 0.0f;
+            for (int z = 0; z < splits; ++z) acc += partial[((size_t)z * T + t) * E + e];
+            lg[i] = acc + (bias ? bias[e] : 0.0f);
+            slot[i] = slot_of[e];
+        }
+    }
+    // softmax over all E: max, then sum of exp(l - max)
+    float mx = NEG;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) mx = fmaxf(mx, lg[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+    float z = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+        if (lane + 32 * i < E) z += expf(lg[i] - mx);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
+    const float inv_z = 1.0f / z;
+
+    // wanted top-k over all experts, then resident top-k; order by logit
+    // (monotone in the score), ties to the lower expert index.
+    for (int pass = 0; pass < 2; ++pass) {
+        uint32_t taken = 0;
+        for (int j = 0; j < k; ++j) {
+            float bv = NEG;
+            int bi = 0x7FFFFFFF;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                int e = lane + 32 * i;
+                bool ok = e < E && !((taken >> i) & 1u) && (pass == 0 || slot[i] >= 0);
+                if (ok && (lg[i] > bv || bi == 0x7FFFFFFF)) { bv = lg[i]; bi = e; }
+            }
+            warp_argmax(bv, bi);
+            const size_t o = (size_t)t * k + j;
+            if (bi == 0x7FFFFFFF) {           // fewer resident experts than k
+                if (lane == 0) { sel_e[o] = -1; sel_slot[o] = -1; sel_w[o] = 0.0f; }
+                continue;
+            }
+            const float s = expf(bv - mx) * inv_z;
+            if ((bi & 31) == lane) {
+                const int i = bi >> 5;
+                taken |= 1u << i;
+                if (pass == 0) { want_e[o] = bi; want_s[o] = s; }
+                else {
+                    int sl = 0;
+#pragma unroll
+                    for (int q = 0; q < VPL; ++q) if (q == i) sl = slot[q];
+                    sel_e[o] = bi; sel_slot[o] = sl; sel_w[o] = s;
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+int route_splits(int T, int E, int d) {
+    const int gx = (E + BE - 1) / BE, gy = (T + BT - 1) / BT;
+    int splits = 1;
+    const int kblocks = d / BK;
+    while (splits * 2 <= 32 && gx * gy * splits * 2 <= 256 && kblocks % (splits * 2) == 0) splits *= 2;
+    return splits;
+}
+
+cudaError_t launch_route(const RouteLaunch& a, cudaStream_t s) {
+    dim3 g1((a.E + BE - 1) / BE, (a.T + BT - 1) / BT, a.splits);
+    moe_prof_begin(MK_ROUTER_LOGITS, s);
+    router_logits_partial<<<g1, 256, 0, s>>>(a.x, a.w, a.T, a.d, a.E, a.d / a.splits, a.partial);
+    moe_prof_end(MK_ROUTER_LOGITS, s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int vpl = (a.E + 31) / 32;
+    dim3 g2((a.T + 7) / 8);
+#define MOE_SEL(V)                                                                                       \
+    route_select<V><<<g2, 256, 0, s>>>(a.partial, a.splits, a.bias, a.slot_of, a.T, a.E, a.k, a.want_e, \
+                                       a.want_s, a.sel_e, a.sel_slot, a.sel_w)
+    moe_prof_begin(MK_ROUTE_SELECT, s);
+    if (vpl <= 1) MOE_SEL(1);
+    else if (vpl <= 2) MOE_SEL(2);
+    else if (vpl <= 4) MOE_SEL(4);
+    else if (vpl <= 8) MOE_SEL(8);
+    else if (vpl <= 16) MOE_SEL(16);
+    else MOE_SEL(32);
+#undef MOE_SEL
+    moe_prof_end(MK_ROUTE_SELECT, s);
+    moe_count_launches(2);
+    return cudaGetLastError();
+}

@@ -265,3 +265,56 @@ def ring_candidates(cfg: LayerConfig, step: int, slot_of: np.ndarray, count: int
         return absent.astype(np.int32)
     perm = seeded_permutation(cfg.seed, T_RING, step, len(absent))
     return absent[perm[:min(count, len(absent))]].astype(np.int32)
+
+
+# --------------------------------------------------------------------------- device fill of big arenas
+
+_FILL_SRC = __import__("os").path.join(__import__("os").path.dirname(__file__), "csrc", "synth_fill.cu")
+_FILL_LIB = __import__("os").path.join(__import__("os").path.dirname(__file__), "libsynth_fill.so")
+_fill = None
+
+
+def build_fill(force: bool = False) -> str:
+    """Compile the device fill kernel (same hash as above) for sm_103a."""
+    import os
+    import subprocess
+    if force or not os.path.exists(_FILL_LIB) or os.path.getmtime(_FILL_LIB) < os.path.getmtime(_FILL_SRC):
+        tmp = _FILL_LIB + f".tmp{os.getpid()}"
+        subprocess.check_call([os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc"), "-gencode",
+                               "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
+                               "-shared", "-o", tmp, _FILL_SRC])
+        os.replace(tmp, _FILL_LIB)
+    return _FILL_LIB
+
+
+def _fill_lib():
+    global _fill
+    if _fill is None:
+        import ctypes
+        _fill = ctypes.CDLL(build_fill())
+        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        _fill.synth_fill_slots.restype = I
+        _fill.synth_fill_slots.argtypes = [P, I64, I64, I64, I64, I64, I, I, P, P, I, I, I, ctypes.c_uint64, P]
+    return _fill
+
+
+def fill_slots_device(arena_buf, d: int, ffn: int, seed: int, E: int, flats, slots=None, slot_begin: int = 0,
+                      n: int | None = None, stream=None) -> None:
+    """Write seeded experts into a device arena (torch uint8 tensor of n_slots * slot_bytes).
+
+    slots is None: slots [slot_begin, slot_begin + n) take expert flats[slot] (an owner table, -1 skips);
+    otherwise slot slots[i] takes expert flats[i]. ``flats``/``slots`` are int32 CUDA tensors.
+    """
+    import ctypes
+    import torch
+    rec = slot_record(d, ffn)
+    if n is None:
+        n = int(slots.numel()) if slots is not None else int(flats.numel()) - slot_begin
+    s = torch.cuda.current_stream() if stream is None else stream
+    err = _fill_lib().synth_fill_slots(
+        ctypes.c_void_p(arena_buf.data_ptr()), rec["slot_bytes"], rec["off_gu_codes"], rec["off_gu_scales"],
+        rec["off_dn_codes"], rec["off_dn_scales"], d, ffn,
+        None if slots is None else ctypes.c_void_p(slots.data_ptr()), ctypes.c_void_p(flats.data_ptr()),
+        slot_begin, n, E, ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), ctypes.c_void_p(s.cuda_stream))
+    if err != 0:
+        raise RuntimeError(f"synth_fill_slots: cudaError {err}")

@@ -1,0 +1,97 @@
+// Device-side fill of arena slots with seeded synthetic MXFP4 experts.
+//
+// Input generation only (no part of the method): the same counter-based
+// SplitMix64 streams as synth/__init__.py, so that any expert written here can
+// be regenerated on the host byte for byte. Expert (layer, expert) is keyed by
+// its flat id layer * E + expert.
+//   codes byte j  = byte (j % 8) of hash(j / 8)            (uniform nibbles)
+//   scale byte j  = 121 + ((hash(j / 32) >> 2 * (j % 32)) & 3)   (2^U, U in -6..-3)
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace {
+
+constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
+
+__host__ __device__ inline uint64_t mix(uint64_t z) {
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+__host__ __device__ inline uint64_t stream_base(uint64_t seed, uint32_t tid, uint32_t a, uint32_t b) {
+    const uint64_t key = ((uint64_t)(tid & 0xFF) << 56) ^ ((uint64_t)(a & 0xFFFFFFF) << 28) ^ (uint64_t)(b & 0xFFFFFFF);
+    return mix(seed ^ mix(key));
+}
+
+__device__ inline uint64_t hash_at(uint64_t base, uint64_t idx) { return mix(base + (idx + 1) * kGamma); }
+
+struct Region {
+    int64_t off;
+    int64_t bytes;
+    uint32_t tid;
+    int scales;
+};
+
+__global__ void fill_slots(uint8_t* arena, int64_t slot_bytes, Region r0, Region r1, Region r2, Region r3,
+                           const int32_t* slots, const int32_t* flats, int slot_begin, int n, int E, uint64_t seed) {
+    const int item = blockIdx.y;
+    if (item >= n) return;
+    const int slot = slots ? slots[item] : slot_begin + item;
+    const int flat = flats[slots ? item : slot];
+    if (slot < 0 || flat < 0) return;
+    const uint32_t layer = (uint32_t)(flat / E), expert = (uint32_t)(flat % E);
+    uint8_t* rec = arena + (size_t)slot * slot_bytes;
+    const Region rs[4] = {r0, r1, r2, r3};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const Region r = rs[q];
+        const uint64_t base = stream_base(seed, r.tid, layer, expert);
+        uint64_t* dst = reinterpret_cast<uint64_t*>(rec + r.off);
+        if (!r.scales) {
+            const int64_t words = r.bytes / 8;
+            for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < words; w += (int64_t)gridDim.x * blockDim.x)
+                dst[w] = hash_at(base, (uint64_t)w);
+        } else {
+            const int64_t groups = r.bytes / 32;                 // one hash -> 32 scale bytes
+            for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += (int64_t)gridDim.x * blockDim.x) {
+                const uint64_t h = hash_at(base, (uint64_t)g);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    uint64_t word = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int j = w * 8 + i;
+                        word |= (uint64_t)(121u + (uint32_t)((h >> (2 * j)) & 3u)) << (8 * i);
+                    }
+                    dst[g * 4 + w] = word;
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+// Fill slots with seeded experts.
+//   slots == NULL : slots [slot_begin, slot_begin + n), expert flats[slot] (flats = owner table, -1 skips)
+//   slots != NULL : slot slots[i] gets expert flats[i], i < n
+// All pointers are device pointers except the scalar arguments. Returns a cudaError_t value.
+int synth_fill_slots(void* arena_base, int64_t slot_bytes, int64_t off_gu_codes, int64_t off_gu_scales,
+                     int64_t off_dn_codes, int64_t off_dn_scales, int d, int ffn, const int32_t* slots,
+                     const int32_t* flats, int slot_begin, int n, int E, uint64_t seed, void* stream) {
+    if (n <= 0) return 0;
+    Region r0{off_gu_codes, (int64_t)2 * ffn * d / 2, 4, 0};
+    Region r1{off_gu_scales, (int64_t)2 * ffn * d / 32, 5, 1};
+    Region r2{off_dn_codes, (int64_t)d * ffn / 2, 6, 0};
+    Region r3{off_dn_scales, (int64_t)d * ffn / 32, 7, 1};
+    dim3 grid(64, n);
+    fill_slots<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint8_t*>(arena_base), slot_bytes,
+                                                                    r0, r1, r2, r3, slots, flats, slot_begin, n, E,
+                                                                    seed);
+    return (int)cudaGetLastError();
+}
+
+}  // extern "C"
