@@ -14,9 +14,9 @@
 // The number formats follow the OCP Microscaling (MX) Formats v1.0 spec:
 // e2m1 elements, e8m0 shared scales, blocks of 32.
 //
-// Readings where the pages are silent are listed in the design doc; the short
-// form is repeated beside each function. Every function is pinned by the
-// tests under tests/ (test_oracle_*.py), except where noted there.
+// Where the pages leave a step open, the reading taken is stated beside the
+// function that takes it. Every function is pinned by tests/test_oracle_pins.py
+// against hand-worked cases, closed forms, invariants or brute force.
 
 #include <algorithm>
 #include <cmath>

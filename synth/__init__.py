@@ -13,9 +13,8 @@ hash for expert weight bytes).
 Normals come from Box-Muller in float64 on the host only and are then rounded
 to fp32 / bf16, so both sides see the same bits.
 
-Workload recipe (shapes from the layer configurations this package tests and
-times; distributions as stated there, with the readings written out in
-DESIGN.md):
+Workload recipe (shapes and distributions of the layer configurations this
+repository tests and times):
 
 * hidden  x ~ N(0, 1), rounded to bf16 (round to nearest even);
 * router  W ~ N(0, 1/d) fp32, bias b = sigma * z, z ~ N(0, 1) (so e^b is
