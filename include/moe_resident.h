@@ -65,10 +65,18 @@ typedef enum {
  * hot-read ring (README item 3); the FFN treats them alike.
  * One slot record holds one expert in MXFP4 (two e2m1 codes per byte, the
  * even element in the LOW nibble, K contiguous; one e8m0 byte per 32 K):
- *   off_gu_codes   [2*ffn, d/2]   gate rows 0..ffn-1, then up rows ffn..2ffn-1
- *   off_gu_scales  [2*ffn, d/32]
- *   off_dn_codes   [d, ffn/2]
- *   off_dn_scales  [d, ffn/32]
+ *   off_gu_codes   [2*ffn, d/2]   row-major; gate rows 0..ffn-1, then up rows ffn..2ffn-1
+ *   off_gu_scales  2*ffn*d/32 bytes, tile-atom order (below)
+ *   off_dn_codes   [d, ffn/2]     row-major
+ *   off_dn_scales  d*ffn/32 bytes, tile-atom order
+ * Tile-atom order of a scale matrix S[row, kb] (kb = K-block of 32): rows are
+ * grouped in 128-row tiles -- for gate/up, tile g is gate rows 64g..64g+63
+ * followed by up rows ffn+64g..ffn+64g+63; for down, rows 128g..128g+127 --
+ * and each tile's scales are stored as consecutive 512-byte atoms of four
+ * K-blocks: S[row, 4a + k] of tile row r sits at byte
+ *   (g * (K/128) + a) * 512 + (r % 32) * 16 + (r / 32) * 4 + k.
+ * (This is the order in which the tensor cores take block scales, so a stage
+ * of scales is one contiguous copy.)
  * Requirements: base and every offset 256-byte aligned, slot_bytes a multiple
  * of 256, d and ffn multiples of 128.
  */

@@ -138,6 +138,13 @@ MOE_DEV void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, 
         : "memory");
 }
 
+// 1-D bulk async copy global -> shared (16-byte aligned addresses, size a multiple of 16).
+MOE_DEV void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 MOE_DEV void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

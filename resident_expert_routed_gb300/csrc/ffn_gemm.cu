@@ -15,15 +15,20 @@
 //
 // The weight tile is the MMA's A operand (M = 128) and the few routed rows the
 // B operand (N = 16..128), so a decode-sized group still streams whole weight
-// tiles at full width. Per CTA (persistent over work items, 192 threads):
-//   warp 4     producer: TMA (128-byte swizzle) of the weight codes from the
-//              slot; cp.async of the routed activation rows (gathered by index,
-//              swizzled by hand), of the weight scales and of the activation
-//              scales into 32x16-byte scale atoms;
+// tiles at full width. Per CTA (persistent over work items, 224 threads):
+//   warp 4     TMA: per stage, two 64-row boxes of weight codes (128-byte
+//              swizzle) and one 1-D bulk copy of the stage's weight scales,
+//              which the arena keeps in the tensor cores' scale-atom order;
+//              it never waits on anything but a free stage;
+//   warp 6     gather: cp.async of the routed activation rows (named by
+//              index, swizzled by hand) and of their scales into 32x16-byte
+//              atoms; signals a stage once its copies have landed;
 //   warp 5     TMEM allocator; lane 0 issues tcgen05.cp (scales -> TMEM) and
 //              tcgen05.mma, and commits to the stage / accumulator barriers;
 //   warps 0-3  epilogue: tcgen05.ld of their 32-lane quadrant of the
-//              double-buffered accumulator, then the per-mode epilogue.
+//              double-buffered accumulator, then the per-mode epilogue (the
+//              up-projection rows reach the gate rows' warps through a small
+//              shared-memory exchange, 16 columns at a time).
 // Every wait is bounded (MOE_WAIT_LIMIT_NS); on expiry the CTA raises its
 // abort flag, every role leaves its loop, TMEM is freed and the device error
 // word gets MOE_DEV_TIMEOUT.
@@ -57,29 +62,33 @@ struct GemmArgs {
 
 template <int MODE, int BN, int NS>
 struct Cfg {
+    static constexpr int THREADS = 224;           // warps 0-3 epilogue, 4 TMA, 5 MMA, 6 gather
     static constexpr int A_BYTES = 128 * 128;     // 128 rows x 128 B = 256 e2m1 along K
     static constexpr int B_BYTES = BN * 128;
     static constexpr int SF_BYTES = 2048;         // A atom 0, A atom 1, B atom 0, B atom 1 (512 B each)
-    static constexpr int XCH_FLOATS = MODE == 1 ? 128 * (BN + 1) : 0;
+    static constexpr int XCH_STRIDE = 17;         // floats per exchange row (16 columns + pad)
+    static constexpr int XCH_BYTES = MODE == 1 ? 64 * XCH_STRIDE * 4 : 0;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + NS * A_BYTES;
     static constexpr int OFF_SF = OFF_B + NS * B_BYTES;
     static constexpr int OFF_XCH = OFF_SF + NS * SF_BYTES;
-    static constexpr int OFF_ROWB = OFF_XCH + XCH_FLOATS * 4;
+    static constexpr int OFF_ROWB = OFF_XCH + XCH_BYTES;
     static constexpr int OFF_BAR = (OFF_ROWB + BN * 4 + 7) / 8 * 8;
-    static constexpr int N_BARS = 2 * NS + 4 + 2;
+    static constexpr int N_BARS = 2 * NS + 6;
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
     static constexpr int TMEM_USED = 2 * BN + 16 * NS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
-    static constexpr int LAG = NS - 1 < 2 ? NS - 1 : 2;   // cp.async groups kept in flight
+    static constexpr int LAG = 2;                 // cp.async groups the gather warp keeps in flight
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "BN");
+    static_assert(NS > LAG, "stages");
     static_assert(TMEM_USED <= 512, "TMEM");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 template <int MODE, int BN, int NS>
-__global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant__ CUtensorMap tmap, const GemmArgs a) {
+__global__ void __launch_bounds__(224, 1) ffn_gemm_kernel(const __grid_constant__ CUtensorMap tmap, const GemmArgs a) {
     using C = Cfg<MODE, BN, NS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -87,18 +96,18 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
     uint64_t* empty = full + NS;
     uint64_t* accf = empty + NS;
     uint64_t* acce = accf + 2;
-    uint64_t* xw = acce + 2;
-    uint64_t* xr = xw + 1;
+    uint64_t* uready = acce + 2;       // gate/up exchange: up values written (warps 2, 3)
+    uint64_t* uread = uready + 1;      // gate/up exchange: up values consumed (warps 0, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     int32_t* rowB = reinterpret_cast<int32_t*>(smem + C::OFF_ROWB);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 33); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1 + 32); mbar_init(&empty[s], 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(&accf[b], 1); mbar_init(&acce[b], 4); }
-        mbar_init(xw, 4);
-        mbar_init(xr, 4);
+        mbar_init(uready, 2);
+        mbar_init(uread, 2);
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tmap);
@@ -113,37 +122,55 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
     const int nk = (a.K + 255) / 256;
 
     if (warp == 4) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ TMA: weight codes + packed weight scales
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok_run = true;
+            for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x) {
+                const int4 w = a.work[item / a.m_tiles];
+                const int mt = item % a.m_tiles;
+                const int slot = w.x;
+                const uint8_t* sfa = a.arena + (size_t)slot * a.slot_bytes + a.off_scales +
+                                     (size_t)mt * (a.K / 128) * 512;
+                const int yA0 = MODE == 1 ? mt * 64 : mt * 128;
+                const int yA1 = MODE == 1 ? a.F + mt * 64 : mt * 128 + 64;
+                for (int kc = 0; kc < nk; ++kc, ++it) {
+                    const int s = (int)(it % NS);
+                    const uint32_t r = it / NS;
+                    if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
+                    uint8_t* As = smem + C::OFF_A + s * C::A_BYTES;
+                    uint8_t* SFs = smem + C::OFF_SF + s * C::SF_BYTES;
+                    const uint32_t sf_bytes = (a.K - kc * 256 >= 256) ? 1024u : 512u;
+                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + sf_bytes);
+                    tma_load_3d(As, &tmap, &full[s], kc * 128, yA0, slot);
+                    tma_load_3d(As + 64 * 128, &tmap, &full[s], kc * 128, yA1, slot);
+                    bulk_load(SFs, sfa + (size_t)kc * 1024, sf_bytes, &full[s]);
+                }
+            }
+        }
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ gather: routed activation rows + scales
         const int K2 = a.K / 2, K32 = a.K / 32;
         uint32_t it = 0;
         bool ok_run = true;
         for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x) {
             const int4 w = a.work[item / a.m_tiles];
-            const int mt = item % a.m_tiles;
-            const int slot = w.x, pos0 = w.y, nv = w.z;
+            const int pos0 = w.y, nv = w.z;
+            const int N = (nv + 15) & ~15;
             __syncwarp();
-            for (int n = lane; n < BN; n += 32) {
+            for (int n = lane; n < N; n += 32) {
                 int r = -1;
                 if (n < nv) r = MODE == 1 ? a.pair_of_pos[pos0 + n] / a.k : pos0 + n;
                 rowB[n] = r;
             }
             __syncwarp();
-            const uint8_t* sfa = a.arena + (size_t)slot * a.slot_bytes + a.off_scales;
-            const int yA0 = MODE == 1 ? mt * 64 : mt * 128;
-            const int yA1 = MODE == 1 ? a.F + mt * 64 : mt * 128 + 64;
             for (int kc = 0; kc < nk; ++kc, ++it) {
                 const int s = (int)(it % NS);
                 const uint32_t r = it / NS;
                 if (!warp_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
-                uint8_t* As = smem + C::OFF_A + s * C::A_BYTES;
                 uint8_t* Bs = smem + C::OFF_B + s * C::B_BYTES;
                 uint8_t* SFs = smem + C::OFF_SF + s * C::SF_BYTES;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[s], C::A_BYTES);
-                    tma_load_3d(As, &tmap, &full[s], kc * 128, yA0, slot);
-                    tma_load_3d(As + 64 * 128, &tmap, &full[s], kc * 128, yA1, slot);
-                }
-                for (int idx = lane; idx < BN * 8; idx += 32) {          // activation rows, 16 B chunks
+                for (int idx = lane; idx < N * 8; idx += 32) {           // 16-byte chunks, 128-byte swizzle
                     const int n = idx >> 3, c = idx & 7;
                     const int row = rowB[n];
                     const int kb = kc * 128 + c * 16;
@@ -151,16 +178,7 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
                     const uint8_t* src = ok ? a.b_codes + (size_t)row * K2 + kb : a.b_codes;
                     cp_async_16(Bs + n * 128 + ((c ^ (n & 7)) << 4), src, ok ? 16u : 0u);
                 }
-                for (int idx = lane; idx < 256; idx += 32) {             // weight scales: 128 rows x 2 groups
-                    const int row = idx >> 1, g = idx & 1;
-                    const int kb = kc * 8 + g * 4;
-                    const bool ok = kb < K32;
-                    const int grow = MODE == 1 ? (row < 64 ? mt * 64 + row : a.F + mt * 64 + (row - 64))
-                                               : mt * 128 + row;
-                    const uint8_t* src = ok ? sfa + (size_t)grow * K32 + kb : sfa;
-                    cp_async_4(SFs + g * 512 + (row & 31) * 16 + (row >> 5) * 4, src, ok ? 4u : 0u);
-                }
-                for (int idx = lane; idx < BN * 2; idx += 32) {          // activation scales
+                for (int idx = lane; idx < N * 2; idx += 32) {           // scales into the atoms
                     const int n = idx >> 1, g = idx & 1;
                     const int row = rowB[n];
                     const int kb = kc * 8 + g * 4;
@@ -223,8 +241,9 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
     } else {
         // ------------------------------------------------------------ epilogue (warps 0..3)
         float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
-        uint32_t j = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
+        uint32_t j = 0, jc = 0;
+        bool ok_run = true;
+        for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x, ++j) {
             const int4 w = a.work[item / a.m_tiles];
             const int mt = item % a.m_tiles;
             const int pos0 = w.y, nv = w.z;
@@ -234,47 +253,55 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
             tc_fence_after();
             const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16) + b * BN;
             if (MODE == 1) {
-                if (!warp_wait(xr, (j & 1) ^ 1, abort_flag)) break;
-                for (int c0 = 0; c0 < BN && c0 < nv; c0 += 16) {
+                // rows 0-63: gate f0..f0+63 (warps 0, 1); rows 64-127: up (warps 2, 3)
+                for (int c0 = 0; c0 < nv; c0 += 16, ++jc) {
                     uint32_t v[16];
                     tc_ld_x16(trow + c0, v);
                     tc_wait_ld();
-                    float* dst = xch + (warp * 32 + lane) * (BN + 1) + c0;
+                    if (warp >= 2) {
+                        if (!warp_wait(uread, (jc & 1) ^ 1, abort_flag)) { ok_run = false; break; }
+                        float* dst = xch + ((warp - 2) * 32 + lane) * C::XCH_STRIDE;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) dst[i] = __uint_as_float(v[i]);
+                        for (int i = 0; i < 16; ++i) dst[i] = __uint_as_float(v[i]);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(uready);
+                    } else {
+                        if (!warp_wait(uready, jc & 1, abort_flag)) { ok_run = false; break; }
+                        const float* src = xch + (warp * 32 + lane) * C::XCH_STRIDE;
+                        const int f0 = mt * 64 + warp * 32;          // this warp's 32 features = one block
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (c0 + i >= nv) break;           // warp-uniform
+                            const float g = __uint_as_float(v[i]);
+                            const float h = g / (1.0f + expf(-g)) * src[i];
+                            float amax = fabsf(h);
+#pragma unroll
+                            for (int off = 16; off > 0; off >>= 1)
+                                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+                            const int X = mx_shared_exp(amax);
+                            const uint32_t code = e2m1_code(h, exp2_int(-X));
+                            const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+                            const uint32_t byte = (code | (hi << 4)) & 0xFFu;
+                            const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
+                            const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
+                            const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 6);
+                            const size_t pos = (size_t)(pos0 + c0 + i);
+                            if ((lane & 7) == 0)
+                                *reinterpret_cast<uint32_t*>(a.hq + pos * (a.F / 2) + f0 / 2 + (lane >> 3) * 4) =
+                                    byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                            if (lane == 0) a.hs[pos * (a.F / 32) + f0 / 32] = (uint8_t)(X + 127);
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(uread);
+                    }
                 }
+                if (!ok_run) break;
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) { mbar_arrive(&acce[b]); mbar_arrive(xw); }
-                if (!warp_wait(xw, j & 1, abort_flag)) break;
-                for (int uu = warp; uu < nv * 2; uu += 4) {
-                    const int n = uu >> 1, bb = uu & 1;
-                    const int fl = bb * 32 + lane;
-                    const float g = xch[fl * (BN + 1) + n];
-                    const float up = xch[(64 + fl) * (BN + 1) + n];
-                    const float h = g / (1.0f + expf(-g)) * up;
-                    float amax = fabsf(h);
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-                    const int X = mx_shared_exp(amax);
-                    const uint32_t code = e2m1_code(h, exp2_int(-X));
-                    const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, code, 1);
-                    const uint32_t byte = (code | (hi << 4)) & 0xFFu;
-                    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
-                    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
-                    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 6);
-                    const size_t pos = (size_t)(pos0 + n);
-                    const int f0 = mt * 64 + bb * 32;
-                    if ((lane & 7) == 0)
-                        *reinterpret_cast<uint32_t*>(a.hq + pos * (a.F / 2) + f0 / 2 + (lane >> 3) * 4) =
-                            byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-                    if (lane == 0) a.hs[pos * (a.F / 32) + f0 / 32] = (uint8_t)(X + 127);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xr);
+                if (lane == 0) mbar_arrive(&acce[b]);
             } else {
                 const int dr = mt * 128 + warp * 32 + lane;
-                for (int c0 = 0; c0 < BN && c0 < nv; c0 += 16) {
+                for (int c0 = 0; c0 < nv; c0 += 16) {
                     uint32_t v[16];
                     tc_ld_x16(trow + c0, v);
                     tc_wait_ld();
@@ -344,7 +371,7 @@ cudaError_t launch_one(const CUtensorMap& map, const GemmArgs& g, long max_items
     if (occ == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 192, C::SMEM);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::THREADS, C::SMEM);
         if (e != cudaSuccess) return e;
         if (occ < 1) return cudaErrorInvalidConfiguration;
         const int tmem_fit = 512 / C::TMEM_COLS;
@@ -355,7 +382,7 @@ cudaError_t launch_one(const CUtensorMap& map, const GemmArgs& g, long max_items
     long grid = (long)occ * moe_sm_count();
     if (grid > max_items) grid = max_items;
     moe_prof_begin(MODE == 1 ? MK_GEMM_GATE_UP : MK_GEMM_DOWN, s);
-    kern<<<(unsigned)grid, 192, C::SMEM, s>>>(map, g);
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM, s>>>(map, g);
     moe_prof_end(MODE == 1 ? MK_GEMM_GATE_UP : MK_GEMM_DOWN, s);
     moe_count_launches(1);
     return cudaGetLastError();
@@ -364,10 +391,9 @@ cudaError_t launch_one(const CUtensorMap& map, const GemmArgs& g, long max_items
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& map, const GemmArgs& g, long max_items, int bn, cudaStream_t s) {
     switch (bn) {
-        case 16: return launch_one<MODE, 16, 4>(map, g, max_items, s);
-        case 32: return launch_one<MODE, 32, 4>(map, g, max_items, s);
-        case 64: return MODE == 1 ? launch_one<MODE, 64, 3>(map, g, max_items, s)
-                                  : launch_one<MODE, 64, 4>(map, g, max_items, s);
+        case 16: return launch_one<MODE, 16, 8>(map, g, max_items, s);
+        case 32: return launch_one<MODE, 32, 8>(map, g, max_items, s);
+        case 64: return launch_one<MODE, 64, 6>(map, g, max_items, s);
         default: return launch_one<MODE, 128, 4>(map, g, max_items, s);
     }
 }

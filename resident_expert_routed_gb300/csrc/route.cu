@@ -102,15 +102,25 @@ __global__ void __launch_bounds__(256) route_select(const float* __restrict__ pa
     float lg[VPL];
     int slot[VPL];
 #pragma unroll
+    for (int i = 0; i < VPL; ++i) lg[i] = 0.0f;
+    // K slices summed in slice order (deterministic); each slice issues VPL independent loads
+    for (int z = 0; z < splits; ++z) {
+        const float* pz = partial + ((size_t)z * T + t) * E;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) lg[i] += pz[e];
+        }
+    }
+#pragma unroll
     for (int i = 0; i < VPL; ++i) {
-        int e = lane + 32 * i;
-        lg[i] = NEG;
+        const int e = lane + 32 * i;
         slot[i] = -1;
         if (e < E) {
-            float acc = 0.0f;
-            for (int z = 0; z < splits; ++z) acc += partial[((size_t)z * T + t) * E + e];
-            lg[i] = acc + (bias ? bias[e] : 0.0f);
+            lg[i] += bias ? bias[e] : 0.0f;
             slot[i] = slot_of[e];
+        } else {
+            lg[i] = NEG;
         }
     }
     // softmax over all E: max, then sum of exp(l - max)

@@ -156,15 +156,40 @@ def expert_weights(seed: int, layer: int, expert: int, d: int, ffn: int) -> dict
     )
 
 
+def pack_scales(scales: np.ndarray, gate_up: bool, ffn: int = 0) -> np.ndarray:
+    """Scale bytes [R, K/32] in the arena's tile-atom order (the layout the arena record uses).
+
+    Rows are taken in 128-row tiles (gate/up: 64 gate rows f0..f0+63 then the 64
+    matching up rows ffn+f0..; down: 128 consecutive rows), and each tile's
+    scales in 512-byte atoms of 4 K-blocks: byte (r % 32) * 16 + (r // 32) * 4 + k
+    for tile row r and K-block 4a + k of atom a. Tiles, then atoms, are stored in order.
+    """
+    R, Kb = scales.shape
+    if gate_up:
+        g = np.arange(ffn // 64)[:, None]
+        r = np.arange(128)[None, :]
+        rows = np.where(r < 64, 64 * g + r, ffn + 64 * g + (r - 64))
+    else:
+        rows = np.arange(R).reshape(-1, 128)
+    t = scales[rows]                                   # [tiles, 128, Kb]
+    t = t.reshape(t.shape[0], 4, 32, Kb // 4, 4)       # r = 32 j + r0 ; kb = 4 a + k
+    return np.ascontiguousarray(t.transpose(0, 3, 2, 1, 4)).reshape(-1)
+
+
 def expert_slot_bytes(seed: int, layer: int, expert: int, d: int, ffn: int) -> np.ndarray:
-    """One whole slot record (uint8 [slot_bytes]) holding expert (layer, expert)."""
+    """One whole slot record (uint8 [slot_bytes]) holding expert (layer, expert).
+
+    Codes are stored in their logical row-major layout; scales in the tile-atom
+    order of ``pack_scales``.
+    """
     rec = slot_record(d, ffn)
     w = expert_weights(seed, layer, expert, d, ffn)
     out = np.zeros(rec["slot_bytes"], dtype=np.uint8)
     out[rec["off_gu_codes"]:rec["off_gu_codes"] + rec["gu_codes_bytes"]] = w["gu_codes"].ravel()
-    out[rec["off_gu_scales"]:rec["off_gu_scales"] + rec["gu_scales_bytes"]] = w["gu_scales"].ravel()
+    out[rec["off_gu_scales"]:rec["off_gu_scales"] + rec["gu_scales_bytes"]] = \
+        pack_scales(w["gu_scales"], True, ffn)
     out[rec["off_dn_codes"]:rec["off_dn_codes"] + rec["dn_codes_bytes"]] = w["dn_codes"].ravel()
-    out[rec["off_dn_scales"]:rec["off_dn_scales"] + rec["dn_scales_bytes"]] = w["dn_scales"].ravel()
+    out[rec["off_dn_scales"]:rec["off_dn_scales"] + rec["dn_scales_bytes"]] = pack_scales(w["dn_scales"], False)
     return out
 
 

@@ -6,6 +6,8 @@
 // its flat id layer * E + expert.
 //   codes byte j  = byte (j % 8) of hash(j / 8)            (uniform nibbles)
 //   scale byte j  = 121 + ((hash(j / 32) >> 2 * (j % 32)) & 3)   (2^U, U in -6..-3)
+// where j is the row-major index; codes are stored row-major, scales at their
+// position in the arena's tile-atom order.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -30,8 +32,28 @@ struct Region {
     int64_t off;
     int64_t bytes;
     uint32_t tid;
-    int scales;
+    int scales;       // 0: codes; 1: scales of a gate/up matrix; 2: scales of a down matrix
+    int kb;           // scale bytes per row (K / 32)
+    int ffn;
 };
+
+// Position of logical scale byte (row, k-block) in the arena's tile-atom order:
+// 128-row tiles (gate/up: 64 gate rows f0.. then the 64 up rows ffn+f0..),
+// 512-byte atoms of 4 k-blocks, byte (r % 32) * 16 + (r / 32) * 4 + kb % 4.
+__device__ inline int64_t packed_scale_offset(const Region& r, int64_t row, int kb) {
+    int64_t tile, tr;
+    if (r.scales == 1) {
+        const bool up = row >= r.ffn;
+        const int64_t f = up ? row - r.ffn : row;
+        tile = f / 64;
+        tr = (up ? 64 : 0) + f % 64;
+    } else {
+        tile = row / 128;
+        tr = row % 128;
+    }
+    const int64_t atoms_per_tile = r.kb / 4;
+    return (tile * atoms_per_tile + kb / 4) * 512 + (tr % 32) * 16 + (tr / 32) * 4 + kb % 4;
+}
 
 __global__ void fill_slots(uint8_t* arena, int64_t slot_bytes, Region r0, Region r1, Region r2, Region r3,
                            const int32_t* slots, const int32_t* flats, int slot_begin, int n, int E, uint64_t seed) {
@@ -53,18 +75,15 @@ __global__ void fill_slots(uint8_t* arena, int64_t slot_bytes, Region r0, Region
             for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < words; w += (int64_t)gridDim.x * blockDim.x)
                 dst[w] = hash_at(base, (uint64_t)w);
         } else {
-            const int64_t groups = r.bytes / 32;                 // one hash -> 32 scale bytes
+            uint8_t* dstb = rec + r.off;
+            const int64_t groups = r.bytes / 32;                 // one hash -> 32 logical scale bytes
             for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += (int64_t)gridDim.x * blockDim.x) {
                 const uint64_t h = hash_at(base, (uint64_t)g);
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    uint64_t word = 0;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int j = w * 8 + i;
-                        word |= (uint64_t)(121u + (uint32_t)((h >> (2 * j)) & 3u)) << (8 * i);
-                    }
-                    dst[g * 4 + w] = word;
+                for (int j = 0; j < 32; ++j) {
+                    const int64_t idx = g * 32 + j;              // logical row-major index
+                    const int64_t row = idx / r.kb;
+                    const int kb = (int)(idx % r.kb);
+                    dstb[packed_scale_offset(r, row, kb)] = (uint8_t)(121u + (uint32_t)((h >> (2 * j)) & 3u));
                 }
             }
         }
@@ -83,10 +102,10 @@ int synth_fill_slots(void* arena_base, int64_t slot_bytes, int64_t off_gu_codes,
                      int64_t off_dn_codes, int64_t off_dn_scales, int d, int ffn, const int32_t* slots,
                      const int32_t* flats, int slot_begin, int n, int E, uint64_t seed, void* stream) {
     if (n <= 0) return 0;
-    Region r0{off_gu_codes, (int64_t)2 * ffn * d / 2, 4, 0};
-    Region r1{off_gu_scales, (int64_t)2 * ffn * d / 32, 5, 1};
-    Region r2{off_dn_codes, (int64_t)d * ffn / 2, 6, 0};
-    Region r3{off_dn_scales, (int64_t)d * ffn / 32, 7, 1};
+    Region r0{off_gu_codes, (int64_t)2 * ffn * d / 2, 4, 0, 0, ffn};
+    Region r1{off_gu_scales, (int64_t)2 * ffn * d / 32, 5, 1, d / 32, ffn};
+    Region r2{off_dn_codes, (int64_t)d * ffn / 2, 6, 0, 0, ffn};
+    Region r3{off_dn_scales, (int64_t)d * ffn / 32, 7, 2, ffn / 32, ffn};
     dim3 grid(64, n);
     fill_slots<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint8_t*>(arena_base), slot_bytes,
                                                                     r0, r1, r2, r3, slots, flats, slot_begin, n, E,
