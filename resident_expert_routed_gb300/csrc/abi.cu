@@ -48,27 +48,32 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int bn_for(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128; }
 
 // Workspace of the FFN, carved in this order (every piece 256-byte aligned).
+// Positions are slot-sorted with every slot's segment padded to a multiple of
+// the tile height bn, so at most work_max tiles and pad_max = work_max * bn rows.
 struct FfnCarve {
-    size_t rank, pair_of_pos, offsets, tile_off, work, n_work, xq, xs, hq, hs, Y, total;
-    int work_max;
+    size_t pos_of_pair, pair_of_pos, seg, tile_off, work, n_work, xp, xsp, hq, hsp, Y, total;
+    int work_max, pad_max, bn;
 };
 
 FfnCarve ffn_carve(int T, int k, int d, int F, int S) {
     FfnCarve c{};
+    c.bn = bn_for(T);
     const size_t P = (size_t)T * k;
-    c.work_max = (int)((P < (size_t)S ? P : (size_t)S) + P / 16 + 1);
+    const size_t U = P < (size_t)S ? P : (size_t)S;
+    c.work_max = (int)(U + (P + c.bn - 1) / c.bn);
+    c.pad_max = c.work_max * c.bn;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
-    c.rank = take(P * 4);
-    c.pair_of_pos = take(P * 4);
-    c.offsets = take(((size_t)S + 1) * 4);
+    c.pos_of_pair = take(P * 4);
+    c.pair_of_pos = take((size_t)c.pad_max * 4);
+    c.seg = take((size_t)S * 4);
     c.tile_off = take((size_t)S * 4);
     c.work = take((size_t)c.work_max * 16);
     c.n_work = take(4);
-    c.xq = take((size_t)T * d / 2);
-    c.xs = take((size_t)T * d / 32);
-    c.hq = take(P * F / 2);
-    c.hs = take(P * F / 32);
+    c.xp = take((size_t)c.pad_max * d / 2);
+    c.xsp = take((size_t)c.work_max * (d / 128) * 512);
+    c.hq = take((size_t)c.pad_max * F / 2);
+    c.hsp = take((size_t)c.work_max * (F / 128) * 512);
     c.Y = take(P * d * 4);
     c.total = o;
     return c;
@@ -82,7 +87,7 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 
 // ------------------------------------------------------------------ optional per-launch event timing
 const char* const kKernelNames[MK_COUNT] = {"router_logits_partial", "route_select", "demand_accumulate",
-                                            "hot_miss_select", "ffn_plan_quant", "ffn_gemm_gate_up",
+                                            "hot_miss_select", "ffn_plan", "ffn_pack", "ffn_gemm_gate_up",
                                             "ffn_gemm_down", "ffn_combine", "arena_replan", "ring_install"};
 struct ProfRec {
     int kind;
@@ -278,20 +283,21 @@ moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot
     a.sel_w = sel_w;
     a.arena = arena;
     a.T = T; a.k = k; a.d = d; a.F = F; a.S = S;
-    a.bn = bn_for(T);
+    a.bn = c.bn;
     a.out = out;
-    a.rank = reinterpret_cast<int32_t*>(w + c.rank);
+    a.pos_of_pair = reinterpret_cast<int32_t*>(w + c.pos_of_pair);
     a.pair_of_pos = reinterpret_cast<int32_t*>(w + c.pair_of_pos);
-    a.offsets = reinterpret_cast<int32_t*>(w + c.offsets);
+    a.seg = reinterpret_cast<int32_t*>(w + c.seg);
     a.tile_off = reinterpret_cast<int32_t*>(w + c.tile_off);
     a.work = reinterpret_cast<int4*>(w + c.work);
     a.n_work = reinterpret_cast<int32_t*>(w + c.n_work);
-    a.xq = w + c.xq;
-    a.xs = w + c.xs;
+    a.xp = w + c.xp;
+    a.xsp = w + c.xsp;
     a.hq = w + c.hq;
-    a.hs = w + c.hs;
+    a.hsp = w + c.hsp;
     a.Y = reinterpret_cast<float*>(w + c.Y);
     a.work_max = c.work_max;
+    a.pad_max = c.pad_max;
     a.err = err;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_ffn_plan(a, s);

@@ -64,6 +64,15 @@ MOE_DEV uint32_t e2m1_code(float v, float inv_scale) {
     return e2m1_mag_code(fabsf(v * inv_scale)) | (v < 0.0f ? 8u : 0u);
 }
 
+// Byte of the scale of (operand row `pos`, K-block `kb`) in an activation
+// operand laid out for the tensor cores: rows are grouped in tiles of `bn`
+// (a slot's rows always start a tile), each tile's scales stored as 512-byte
+// atoms of four K-blocks, row r of the tile at (r % 32) * 16 + (r / 32) * 4.
+MOE_DEV size_t operand_scale_offset(int pos, int kb, int bn, int K) {
+    const int tile = pos / bn, r = pos % bn;
+    return ((size_t)tile * (K / 128) + (kb >> 2)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3);
+}
+
 MOE_DEV void record_error(uint32_t* err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }
@@ -135,6 +144,13 @@ MOE_DEV void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, 
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
         ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+MOE_DEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
 }
 
@@ -265,10 +281,19 @@ struct FfnLaunch {
     const uint16_t* x; const int32_t* sel_slot; const float* sel_w; const moe_arena* arena;
     int T, k, d, F, S, bn;
     float* out;
-    // workspace
-    int32_t* rank; int32_t* pair_of_pos; int32_t* offsets; int32_t* tile_off; int4* work; int32_t* n_work;
-    uint8_t* xq; uint8_t* xs; uint8_t* hq; uint8_t* hs; float* Y;
-    int work_max;
+    // workspace: positions are slot-sorted and padded so that every slot starts a tile of bn rows
+    int32_t* pos_of_pair;   // [T*k]
+    int32_t* pair_of_pos;   // [pad_max]
+    int32_t* seg;           // [S]  first position of each slot
+    int32_t* tile_off;      // [S]  first work entry of each slot
+    int4* work;             // [work_max] (slot, first position, rows)
+    int32_t* n_work;
+    uint8_t* xp;            // [pad_max, d/2]   gate/up activation operand (MXFP4 codes)
+    uint8_t* xsp;           // [work_max * d/128 * 512] its scales, tile atoms
+    uint8_t* hq;            // [pad_max, F/2]   down activation operand
+    uint8_t* hsp;           // [work_max * F/128 * 512]
+    float* Y;               // [T*k, d] one fp32 row per pick
+    int work_max, pad_max;
     uint32_t* err;
 };
 cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s);
@@ -287,7 +312,7 @@ int moe_sm_count();
 
 // Kernel kinds for the optional per-launch event timing (abi.cu).
 enum MoeKernelKind {
-    MK_ROUTER_LOGITS = 0, MK_ROUTE_SELECT, MK_DEMAND, MK_HOT_MISS, MK_PLAN_QUANT, MK_GEMM_GATE_UP,
+    MK_ROUTER_LOGITS = 0, MK_ROUTE_SELECT, MK_DEMAND, MK_HOT_MISS, MK_PLAN, MK_PACK, MK_GEMM_GATE_UP,
     MK_GEMM_DOWN, MK_COMBINE, MK_REPLAN, MK_RING, MK_COUNT
 };
 void moe_prof_begin(int kind, cudaStream_t s);

@@ -4,34 +4,35 @@
 // TideLM README: the experts are "native MXFP4" (profile table) and live in
 // one arena of slots shared by all layers (item 1); the picks of a step are
 // routed only to resident slots (item 2). One launch per GEMM covers every
-// used slot: the work list from ffn_plan names (slot, first row, rows) groups.
+// used slot: the work list from ffn_plan names (slot, first row, rows) tiles.
 //
 //   gate/up (MODE 1): for 64 ffn features f0..f0+63 of one slot, D = [Wg; Wu]
-//       rows (64 gate + 64 up = M 128) x the group's activation rows (N), K = d;
+//       rows (64 gate + 64 up = M 128) x the tile's activation rows (N), K = d;
 //       epilogue: h = silu(g) * u, re-quantised to MXFP4 in blocks of 32
-//       features (OCP MX v1.0 rule) into the hq workspace.
+//       features (OCP MX v1.0 rule) into the down GEMM's activation operand.
 //   down (MODE 2): for 128 output rows d0..d0+127, D = Wd rows x hq rows,
-//       K = ffn; epilogue: fp32 rows Y[pair] (combined later in pick order).
+//       K = ffn; epilogue: fp32 rows Y[pick] (combined later in pick order).
 //
 // The weight tile is the MMA's A operand (M = 128) and the few routed rows the
-// B operand (N = 16..128), so a decode-sized group still streams whole weight
-// tiles at full width. Per CTA (persistent over work items, 224 threads):
-//   warp 4     TMA: per stage, two 64-row boxes of weight codes (128-byte
-//              swizzle) and one 1-D bulk copy of the stage's weight scales,
-//              which the arena keeps in the tensor cores' scale-atom order;
-//              it never waits on anything but a free stage;
-//   warp 6     gather: cp.async of the routed activation rows (named by
-//              index, swizzled by hand) and of their scales into 32x16-byte
-//              atoms; signals a stage once its copies have landed;
+// B operand (N = 16..128), so a decode-sized tile still streams whole weight
+// tiles at full width. Every operand arrives by TMA / bulk copy issued by one
+// thread, so a stage costs one DRAM round trip and nothing else:
+//   warp 4     lane 0, per stage of 256 K: two 64-row boxes of weight codes
+//              (128-byte swizzle), one box of activation rows (its height the
+//              tile's row count rounded up), and two 1-D bulk copies of scale
+//              atoms (weights: from the arena, which keeps scales in the
+//              tensor cores' atom order; activations: from the workspace,
+//              written in that order by ffn_pack / the gate/up epilogue);
 //   warp 5     TMEM allocator; lane 0 issues tcgen05.cp (scales -> TMEM) and
 //              tcgen05.mma, and commits to the stage / accumulator barriers;
 //   warps 0-3  epilogue: tcgen05.ld of their 32-lane quadrant of the
 //              double-buffered accumulator, then the per-mode epilogue (the
 //              up-projection rows reach the gate rows' warps through a small
 //              shared-memory exchange, 16 columns at a time).
-// Every wait is bounded (MOE_WAIT_LIMIT_NS); on expiry the CTA raises its
-// abort flag, every role leaves its loop, TMEM is freed and the device error
-// word gets MOE_DEV_TIMEOUT.
+// The grid is persistent (one CTA per SM) over the flattened (tile, 128-row
+// weight block) items. Every wait is bounded (MOE_WAIT_LIMIT_NS); on expiry
+// the CTA raises its abort flag, every role leaves its loop, TMEM is freed and
+// the device error word gets MOE_DEV_TIMEOUT.
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -40,29 +41,32 @@
 
 namespace {
 
+struct GemmMaps {
+    CUtensorMap a;        // weight codes: (row bytes, rows, slots), box 128 B x 64 rows x 1
+    CUtensorMap b[4];     // activation codes: (row bytes, positions), box 128 B x {16, 32, 64, 128} rows
+};
+
 struct GemmArgs {
     const uint8_t* arena;
     int64_t slot_bytes;
-    int64_t off_scales;          // this GEMM's weight scales within a slot
+    int64_t off_scales;          // this GEMM's weight scales within a slot (tile-atom order)
     int K;                       // reduction length: d (gate/up) or ffn (down)
     int m_tiles;
     int F;                       // ffn
     int d;                       // hidden size
-    int k;                       // picks per token
     const int4* work;
     const int32_t* n_work;
     const int32_t* pair_of_pos;
-    const uint8_t* b_codes;      // gate/up: xq [T, d/2];  down: hq [P, ffn/2]
-    const uint8_t* b_scales;     // gate/up: xs [T, d/32]; down: hs [P, ffn/32]
-    uint8_t* hq;
-    uint8_t* hs;
-    float* Y;
+    const uint8_t* b_scales;     // activation scale atoms (xsp or hsp)
+    uint8_t* hq;                 // gate/up output: down activation codes [pad_max, F/2]
+    uint8_t* hsp;                // gate/up output: down activation scale atoms
+    float* Y;                    // down output [T*k, d]
     uint32_t* err;
 };
 
 template <int MODE, int BN, int NS>
 struct Cfg {
-    static constexpr int THREADS = 224;           // warps 0-3 epilogue, 4 TMA, 5 MMA, 6 gather
+    static constexpr int THREADS = 192;           // warps 0-3 epilogue, 4 TMA, 5 MMA
     static constexpr int A_BYTES = 128 * 128;     // 128 rows x 128 B = 256 e2m1 along K
     static constexpr int B_BYTES = BN * 128;
     static constexpr int SF_BYTES = 2048;         // A atom 0, A atom 1, B atom 0, B atom 1 (512 B each)
@@ -72,23 +76,20 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + NS * A_BYTES;
     static constexpr int OFF_SF = OFF_B + NS * B_BYTES;
     static constexpr int OFF_XCH = OFF_SF + NS * SF_BYTES;
-    static constexpr int OFF_ROWB = OFF_XCH + XCH_BYTES;
-    static constexpr int OFF_BAR = (OFF_ROWB + BN * 4 + 7) / 8 * 8;
+    static constexpr int OFF_BAR = (OFF_XCH + XCH_BYTES + 7) / 8 * 8;
     static constexpr int N_BARS = 2 * NS + 6;
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
     static constexpr int TMEM_USED = 2 * BN + 16 * NS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
-    static constexpr int LAG = 2;                 // cp.async groups the gather warp keeps in flight
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "BN");
-    static_assert(NS > LAG, "stages");
+    static_assert(BN == 16 || BN == 32 || BN == 64 || BN == 128, "BN");
     static_assert(TMEM_USED <= 512, "TMEM");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 template <int MODE, int BN, int NS>
-__global__ void __launch_bounds__(224, 1) ffn_gemm_kernel(const __grid_constant__ CUtensorMap tmap, const GemmArgs a) {
+__global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     using C = Cfg<MODE, BN, NS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -100,17 +101,17 @@ __global__ void __launch_bounds__(224, 1) ffn_gemm_kernel(const __grid_constant_
     uint64_t* uread = uready + 1;      // gate/up exchange: up values consumed (warps 0, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-    int32_t* rowB = reinterpret_cast<int32_t*>(smem + C::OFF_ROWB);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1 + 32); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(&accf[b], 1); mbar_init(&acce[b], 4); }
         mbar_init(uready, 2);
         mbar_init(uread, 2);
         *abort_flag = 0;
         fence_barrier_init();
-        prefetch_tmap(&tmap);
+        prefetch_tmap(&maps.a);
+        for (int i = 0; i < 4; ++i) prefetch_tmap(&maps.b[i]);
     }
     if (warp == 5) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
     tc_fence_before();
@@ -120,18 +121,25 @@ __global__ void __launch_bounds__(224, 1) ffn_gemm_kernel(const __grid_constant_
 
     const int n_items = *a.n_work * a.m_tiles;
     const int nk = (a.K + 255) / 256;
+    const int atoms_per_tile = a.K / 128;
 
     if (warp == 4) {
-        // ------------------------------------------------------------ TMA: weight codes + packed weight scales
+        // ------------------------------------------------------------ TMA producer (one thread)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok_run = true;
+            int4 w_next = blockIdx.x < n_items ? a.work[blockIdx.x / a.m_tiles] : make_int4(0, 0, 0, 0);
             for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x) {
-                const int4 w = a.work[item / a.m_tiles];
+                const int4 w = w_next;
+                const int nxt = item + gridDim.x;          // fetch the next entry while this item streams
+                if (nxt < n_items) w_next = a.work[nxt / a.m_tiles];
                 const int mt = item % a.m_tiles;
-                const int slot = w.x;
+                const int slot = w.x, pos0 = w.y, nv = w.z;
+                const int hb = nv <= 16 ? 0 : nv <= 32 ? 1 : nv <= 64 ? 2 : 3;   // activation box height
+                const uint32_t b_bytes = (16u << hb) * 128u;
                 const uint8_t* sfa = a.arena + (size_t)slot * a.slot_bytes + a.off_scales +
-                                     (size_t)mt * (a.K / 128) * 512;
+                                     (size_t)mt * atoms_per_tile * 512;
+                const uint8_t* sfb = a.b_scales + (size_t)(pos0 / BN) * atoms_per_tile * 512;
                 const int yA0 = MODE == 1 ? mt * 64 : mt * 128;
                 const int yA1 = MODE == 1 ? a.F + mt * 64 : mt * 128 + 64;
                 for (int kc = 0; kc < nk; ++kc, ++it) {
@@ -139,64 +147,18 @@ __global__ void __launch_bounds__(224, 1) ffn_gemm_kernel(const __grid_constant_
                     const uint32_t r = it / NS;
                     if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
                     uint8_t* As = smem + C::OFF_A + s * C::A_BYTES;
+                    uint8_t* Bs = smem + C::OFF_B + s * C::B_BYTES;
                     uint8_t* SFs = smem + C::OFF_SF + s * C::SF_BYTES;
                     const uint32_t sf_bytes = (a.K - kc * 256 >= 256) ? 1024u : 512u;
-                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + sf_bytes);
-                    tma_load_3d(As, &tmap, &full[s], kc * 128, yA0, slot);
-                    tma_load_3d(As + 64 * 128, &tmap, &full[s], kc * 128, yA1, slot);
+                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + b_bytes + 2 * sf_bytes);
+                    tma_load_3d(As, &maps.a, &full[s], kc * 128, yA0, slot);
+                    tma_load_3d(As + 64 * 128, &maps.a, &full[s], kc * 128, yA1, slot);
+                    tma_load_2d(Bs, &maps.b[hb], &full[s], kc * 128, pos0);
                     bulk_load(SFs, sfa + (size_t)kc * 1024, sf_bytes, &full[s]);
+                    bulk_load(SFs + 1024, sfb + (size_t)kc * 1024, sf_bytes, &full[s]);
                 }
             }
         }
-    } else if (warp == 6) {
-        // ------------------------------------------------------------ gather: routed activation rows + scales
-        const int K2 = a.K / 2, K32 = a.K / 32;
-        uint32_t it = 0;
-        bool ok_run = true;
-        for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x) {
-            const int4 w = a.work[item / a.m_tiles];
-            const int pos0 = w.y, nv = w.z;
-            const int N = (nv + 15) & ~15;
-            __syncwarp();
-            for (int n = lane; n < N; n += 32) {
-                int r = -1;
-                if (n < nv) r = MODE == 1 ? a.pair_of_pos[pos0 + n] / a.k : pos0 + n;
-                rowB[n] = r;
-            }
-            __syncwarp();
-            for (int kc = 0; kc < nk; ++kc, ++it) {
-                const int s = (int)(it % NS);
-                const uint32_t r = it / NS;
-                if (!warp_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
-                uint8_t* Bs = smem + C::OFF_B + s * C::B_BYTES;
-                uint8_t* SFs = smem + C::OFF_SF + s * C::SF_BYTES;
-                for (int idx = lane; idx < N * 8; idx += 32) {           // 16-byte chunks, 128-byte swizzle
-                    const int n = idx >> 3, c = idx & 7;
-                    const int row = rowB[n];
-                    const int kb = kc * 128 + c * 16;
-                    const bool ok = row >= 0 && kb < K2;
-                    const uint8_t* src = ok ? a.b_codes + (size_t)row * K2 + kb : a.b_codes;
-                    cp_async_16(Bs + n * 128 + ((c ^ (n & 7)) << 4), src, ok ? 16u : 0u);
-                }
-                for (int idx = lane; idx < N * 2; idx += 32) {           // scales into the atoms
-                    const int n = idx >> 1, g = idx & 1;
-                    const int row = rowB[n];
-                    const int kb = kc * 8 + g * 4;
-                    const bool ok = row >= 0 && kb < K32;
-                    const uint8_t* src = ok ? a.b_scales + (size_t)row * K32 + kb : a.b_scales;
-                    cp_async_4(SFs + 1024 + g * 512 + (n & 31) * 16 + (n >> 5) * 4, src, ok ? 4u : 0u);
-                }
-                cp_async_commit();
-                if (it >= (uint32_t)C::LAG) {
-                    cp_async_wait<C::LAG>();
-                    fence_proxy_async_smem();
-                    mbar_arrive(&full[(it - C::LAG) % NS]);
-                }
-            }
-        }
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        for (uint32_t j = it > (uint32_t)C::LAG ? it - C::LAG : 0u; j < it; ++j) mbar_arrive(&full[j % NS]);
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -271,7 +233,7 @@ __global__ void __launch_bounds__(224, 1) ffn_gemm_kernel(const __grid_constant_
                         const int f0 = mt * 64 + warp * 32;          // this warp's 32 features = one block
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            if (c0 + i >= nv) break;           // warp-uniform
+                            if (c0 + i >= nv) break;                 // warp-uniform
                             const float g = __uint_as_float(v[i]);
                             const float h = g / (1.0f + expf(-g)) * src[i];
                             float amax = fabsf(h);
@@ -285,11 +247,11 @@ __global__ void __launch_bounds__(224, 1) ffn_gemm_kernel(const __grid_constant_
                             const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
                             const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
                             const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 6);
-                            const size_t pos = (size_t)(pos0 + c0 + i);
+                            const int pos = pos0 + c0 + i;
                             if ((lane & 7) == 0)
-                                *reinterpret_cast<uint32_t*>(a.hq + pos * (a.F / 2) + f0 / 2 + (lane >> 3) * 4) =
+                                *reinterpret_cast<uint32_t*>(a.hq + (size_t)pos * (a.F / 2) + f0 / 2 + (lane >> 3) * 4) =
                                     byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-                            if (lane == 0) a.hs[pos * (a.F / 32) + f0 / 32] = (uint8_t)(X + 127);
+                            if (lane == 0) a.hsp[operand_scale_offset(pos, f0 / 32, BN, a.F)] = (uint8_t)(X + 127);
                         }
                         __syncwarp();
                         if (lane == 0) mbar_arrive(uread);
@@ -344,24 +306,40 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 3-D view of one weight region of every slot: (row bytes, rows, slots); box
-// 128 bytes x 64 rows x 1 slot, 128-byte swizzle.
-cudaError_t make_weight_map(CUtensorMap* m, const uint8_t* base, uint64_t row_bytes, uint64_t rows, uint64_t slots,
-                            uint64_t slot_bytes) {
+cudaError_t encode(CUtensorMap* m, const uint8_t* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                   const cuuint32_t* box) {
     auto enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
-    cuuint64_t dims[3] = {row_bytes, rows, slots};
-    cuuint64_t strides[2] = {row_bytes, slot_bytes};
-    cuuint32_t box[3] = {128, 64, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dims, strides, box, estr,
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<uint8_t*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Weight codes of every slot: (row bytes, rows, slots); box 128 bytes x 64 rows x 1 slot.
+cudaError_t make_weight_map(CUtensorMap* m, const uint8_t* base, uint64_t row_bytes, uint64_t rows, uint64_t slots,
+                            uint64_t slot_bytes) {
+    cuuint64_t dims[3] = {row_bytes, rows, slots};
+    cuuint64_t strides[2] = {row_bytes, slot_bytes};
+    cuuint32_t box[3] = {128, 64, 1};
+    return encode(m, base, 3, dims, strides, box);
+}
+
+// Activation operand rows: (row bytes, positions); boxes of 16, 32, 64 and 128 rows.
+cudaError_t make_act_maps(CUtensorMap* m, const uint8_t* base, uint64_t row_bytes, uint64_t rows) {
+    for (int i = 0; i < 4; ++i) {
+        cuuint64_t dims[2] = {row_bytes, rows};
+        cuuint64_t strides[1] = {row_bytes};
+        cuuint32_t box[2] = {128, (cuuint32_t)(16 << i)};
+        cudaError_t e = encode(&m[i], base, 2, dims, strides, box);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 template <int MODE, int BN, int NS>
-cudaError_t launch_one(const CUtensorMap& map, const GemmArgs& g, long max_items, cudaStream_t s) {
+cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& g, long max_items, cudaStream_t s) {
     using C = Cfg<MODE, BN, NS>;
     auto kern = ffn_gemm_kernel<MODE, BN, NS>;
     static int occ_cache[64] = {};
@@ -382,19 +360,19 @@ cudaError_t launch_one(const CUtensorMap& map, const GemmArgs& g, long max_items
     long grid = (long)occ * moe_sm_count();
     if (grid > max_items) grid = max_items;
     moe_prof_begin(MODE == 1 ? MK_GEMM_GATE_UP : MK_GEMM_DOWN, s);
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM, s>>>(map, g);
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM, s>>>(maps, g);
     moe_prof_end(MODE == 1 ? MK_GEMM_GATE_UP : MK_GEMM_DOWN, s);
     moe_count_launches(1);
     return cudaGetLastError();
 }
 
 template <int MODE>
-cudaError_t launch_mode(const CUtensorMap& map, const GemmArgs& g, long max_items, int bn, cudaStream_t s) {
+cudaError_t launch_mode(const GemmMaps& maps, const GemmArgs& g, long max_items, int bn, cudaStream_t s) {
     switch (bn) {
-        case 16: return launch_one<MODE, 16, 8>(map, g, max_items, s);
-        case 32: return launch_one<MODE, 32, 8>(map, g, max_items, s);
-        case 64: return launch_one<MODE, 64, 6>(map, g, max_items, s);
-        default: return launch_one<MODE, 128, 4>(map, g, max_items, s);
+        case 16: return launch_one<MODE, 16, 10>(maps, g, max_items, s);
+        case 32: return launch_one<MODE, 32, 9>(maps, g, max_items, s);
+        case 64: return launch_one<MODE, 64, 8>(maps, g, max_items, s);
+        default: return launch_one<MODE, 128, 6>(maps, g, max_items, s);
     }
 }
 
@@ -403,12 +381,14 @@ cudaError_t launch_mode(const CUtensorMap& map, const GemmArgs& g, long max_item
 cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches) {
     const moe_arena& ar = *a.arena;
     const uint8_t* base = static_cast<const uint8_t*>(ar.base);
-    CUtensorMap map_gu, map_dn;
-    cudaError_t e = make_weight_map(&map_gu, base + ar.off_gu_codes, (uint64_t)a.d / 2, (uint64_t)2 * a.F,
+    GemmMaps m1, m2;
+    cudaError_t e = make_weight_map(&m1.a, base + ar.off_gu_codes, (uint64_t)a.d / 2, (uint64_t)2 * a.F,
                                     (uint64_t)ar.n_slots, (uint64_t)ar.slot_bytes);
-    if (e != cudaSuccess) return e;
-    e = make_weight_map(&map_dn, base + ar.off_dn_codes, (uint64_t)a.F / 2, (uint64_t)a.d, (uint64_t)ar.n_slots,
-                        (uint64_t)ar.slot_bytes);
+    if (e == cudaSuccess) e = make_act_maps(m1.b, a.xp, (uint64_t)a.d / 2, (uint64_t)a.pad_max);
+    if (e == cudaSuccess)
+        e = make_weight_map(&m2.a, base + ar.off_dn_codes, (uint64_t)a.F / 2, (uint64_t)a.d, (uint64_t)ar.n_slots,
+                            (uint64_t)ar.slot_bytes);
+    if (e == cudaSuccess) e = make_act_maps(m2.b, a.hq, (uint64_t)a.F / 2, (uint64_t)a.pad_max);
     if (e != cudaSuccess) return e;
 
     GemmArgs g{};
@@ -416,7 +396,6 @@ cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches
     g.slot_bytes = ar.slot_bytes;
     g.F = a.F;
     g.d = a.d;
-    g.k = a.k;
     g.work = a.work;
     g.n_work = a.n_work;
     g.pair_of_pos = a.pair_of_pos;
@@ -426,21 +405,19 @@ cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches
     g1.off_scales = ar.off_gu_scales;
     g1.K = a.d;
     g1.m_tiles = a.F / 64;
-    g1.b_codes = a.xq;
-    g1.b_scales = a.xs;
+    g1.b_scales = a.xsp;
     g1.hq = a.hq;
-    g1.hs = a.hs;
-    e = launch_mode<1>(map_gu, g1, (long)a.work_max * g1.m_tiles, a.bn, s);
+    g1.hsp = a.hsp;
+    e = launch_mode<1>(m1, g1, (long)a.work_max * g1.m_tiles, a.bn, s);
     if (e != cudaSuccess) return e;
 
     GemmArgs g2 = g;       // down
     g2.off_scales = ar.off_dn_scales;
     g2.K = a.F;
     g2.m_tiles = a.d / 128;
-    g2.b_codes = a.hq;
-    g2.b_scales = a.hs;
+    g2.b_scales = a.hsp;
     g2.Y = a.Y;
-    e = launch_mode<2>(map_dn, g2, (long)a.work_max * g2.m_tiles, a.bn, s);
+    e = launch_mode<2>(m2, g2, (long)a.work_max * g2.m_tiles, a.bn, s);
     if (n_launches) *n_launches = 2;
     return e;
 }

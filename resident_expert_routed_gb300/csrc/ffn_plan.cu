@@ -1,22 +1,21 @@
-// Grouping of the routed picks by arena slot, activation quantisation, and the
-// weighted combine of the expert outputs.
+// Grouping of the routed picks by arena slot, activation quantisation into
+// the tensor cores' operand layout, and the weighted combine of the outputs.
 //
 // TideLM README items 1-2 route each token to resident slots of one shared
 // arena; the expert FFN then runs per slot over the rows routed to it. The
-// rows are named by index rather than copied per expert (the colibri cluster
-// page's v2 wire format: "each expert naming its rows by index"), and the
 // combine adds a token's expert outputs in its own pick order, so the result
-// does not depend on how the work was split (same page: replies added in the
-// local loop's per-row expert order).
+// does not depend on how the work was split (colibri cluster page: replies
+// are added in the local loop's per-row expert order).
 //
-// ffn_plan_quant (one launch):
-//   block 0      counts picks per slot (shared-memory atomics), scans the
-//                counts, gives every pick a position in slot-sorted order and
-//                writes the GEMM work list: (slot, first position, rows) per
-//                group of at most BN rows of one slot;
-//   blocks 1..   quantise each token row of x to MXFP4 once (OCP MX v1.0:
-//                exponent floor(log2 amax) - 2, round to nearest even,
-//                saturate at 6; two codes per byte, even element low).
+// ffn_plan (one CTA): counts picks per slot (shared-memory atomics), gives
+//   each slot a segment of positions padded to a multiple of the tile height
+//   BN, gives every pick a position in its slot's segment, and writes the GEMM
+//   work list: (slot, first position, rows) per tile of at most BN rows.
+// ffn_pack: for every pick, quantises its token row of x to MXFP4 (OCP MX
+//   v1.0: exponent floor(log2 amax) - 2, round to nearest even, saturate at
+//   6; two codes per byte, even element low) straight into row `position` of
+//   the gate/up GEMM's activation operand, and its scales into the tile's
+//   scale atoms, so the GEMM fetches both with plain TMA / bulk copies.
 // ffn_combine: out[t] = sum_j sel_w[t,j] * Y[t*k + j], j in order.
 #include "common.cuh"
 
@@ -24,10 +23,13 @@ namespace {
 
 constexpr int PLAN_THREADS = 1024;
 
-__device__ void plan_block(const int32_t* __restrict__ sel_slot, int P, int S, int bn, int32_t* __restrict__ rank,
-                           int32_t* __restrict__ pair_of_pos, int32_t* __restrict__ offsets,
-                           int32_t* __restrict__ tile_off, int4* __restrict__ work, int32_t* __restrict__ n_work,
-                           uint32_t* err, int32_t* cnt) {
+__global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restrict__ sel_slot, int P, int S, int bn,
+                                                         int32_t* __restrict__ pos_of_pair,
+                                                         int32_t* __restrict__ pair_of_pos,
+                                                         int32_t* __restrict__ seg, int32_t* __restrict__ tile_off,
+                                                         int4* __restrict__ work, int32_t* __restrict__ n_work,
+                                                         uint32_t* err) {
+    extern __shared__ int32_t cnt[];
     __shared__ unsigned long long part[PLAN_THREADS];
     const int tid = threadIdx.x;
     for (int i = tid; i < S; i += PLAN_THREADS) cnt[i] = 0;
@@ -35,17 +37,18 @@ __device__ void plan_block(const int32_t* __restrict__ sel_slot, int P, int S, i
     for (int p = tid; p < P; p += PLAN_THREADS) {
         int s = sel_slot[p];
         if (s >= S) { record_error(err, MOE_DEV_BAD_SLOT); s = -1; }
-        rank[p] = s >= 0 ? atomicAdd(&cnt[s], 1) : -1;
+        pos_of_pair[p] = s >= 0 ? atomicAdd(&cnt[s], 1) : -1;          // rank within the slot for now
     }
     __syncthreads();
-    // exclusive scan of (rows, tiles) per slot; each thread owns a contiguous chunk
+    // exclusive scan of (padded rows, tiles) per slot; each thread owns a contiguous chunk
     const int chunk = (S + PLAN_THREADS - 1) / PLAN_THREADS;
     const int b0 = tid * chunk, b1 = min(S, b0 + chunk);
+    auto packed = [bn](int c) {
+        const unsigned long long tiles = (unsigned long long)((c + bn - 1) / bn);
+        return (tiles * bn) | (tiles << 32);
+    };
     unsigned long long local = 0;
-    for (int i = b0; i < b1; ++i) {
-        const unsigned long long c = (unsigned long long)cnt[i];
-        local += c | ((c + bn - 1) / bn << 32);
-    }
+    for (int i = b0; i < b1; ++i) local += packed(cnt[i]);
     part[tid] = local;
     __syncthreads();
     for (int off = 1; off < PLAN_THREADS; off <<= 1) {      // Hillis-Steele inclusive scan
@@ -56,37 +59,39 @@ __device__ void plan_block(const int32_t* __restrict__ sel_slot, int P, int S, i
     }
     unsigned long long run = tid > 0 ? part[tid - 1] : 0ull;
     for (int i = b0; i < b1; ++i) {
-        const unsigned long long c = (unsigned long long)cnt[i];
-        offsets[i] = (int32_t)(run & 0xFFFFFFFFull);
+        seg[i] = (int32_t)(run & 0xFFFFFFFFull);
         tile_off[i] = (int32_t)(run >> 32);
-        run += c | ((c + bn - 1) / bn << 32);
+        run += packed(cnt[i]);
     }
-    if (tid == PLAN_THREADS - 1) {
-        offsets[S] = (int32_t)(part[tid] & 0xFFFFFFFFull);
-        *n_work = (int32_t)(part[tid] >> 32);
-    }
+    if (tid == PLAN_THREADS - 1) *n_work = (int32_t)(part[tid] >> 32);
     __syncthreads();
     for (int p = tid; p < P; p += PLAN_THREADS) {
-        int s = sel_slot[p];
+        const int s = sel_slot[p];
         if (s < 0 || s >= S) continue;
-        pair_of_pos[offsets[s] + rank[p]] = p;
+        const int pos = seg[s] + pos_of_pair[p];
+        pos_of_pair[p] = pos;
+        pair_of_pos[pos] = p;
     }
     for (int i = tid; i < S; i += PLAN_THREADS) {
         const int c = cnt[i];
         const int nt = (c + bn - 1) / bn;
-        for (int q = 0; q < nt; ++q)
-            work[tile_off[i] + q] = make_int4(i, offsets[i] + q * bn, min(bn, c - q * bn), 0);
+        for (int q = 0; q < nt; ++q) work[tile_off[i] + q] = make_int4(i, seg[i] + q * bn, min(bn, c - q * bn), 0);
     }
 }
 
-// One thread per (token, 32-element block): 64 bytes of bf16 in, 16 bytes of
-// codes and one scale byte out.
-__device__ void quant_rows(const uint16_t* __restrict__ x, int T, int d, uint8_t* __restrict__ xq,
-                           uint8_t* __restrict__ xs, int block_rank, int n_blocks) {
+// One thread per (pick, 32-element block): 64 bytes of bf16 in, 16 bytes of
+// codes to the pick's operand row and one scale byte to its tile's atom.
+__global__ void __launch_bounds__(256) ffn_pack(const uint16_t* __restrict__ x, const int32_t* __restrict__ pos_of_pair,
+                                                int P, int k, int d, int bn, uint8_t* __restrict__ xp,
+                                                uint8_t* __restrict__ xsp) {
     const int nb = d / 32;
-    const long total = (long)T * nb;
-    for (long i = (long)block_rank * blockDim.x + threadIdx.x; i < total; i += (long)n_blocks * blockDim.x) {
-        const long t = i / nb, b = i % nb;
+    const long total = (long)P * nb;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+        const long p = i / nb;
+        const int b = (int)(i % nb);
+        const int pos = pos_of_pair[p];
+        if (pos < 0) continue;
+        const long t = p / k;
         const uint4* src = reinterpret_cast<const uint4*>(x + t * d + b * 32);
         uint4 v[4];
 #pragma unroll
@@ -106,21 +111,8 @@ __device__ void quant_rows(const uint16_t* __restrict__ x, int T, int d, uint8_t
             for (int r = 0; r < 8; ++r) word |= e2m1_code(f[q * 8 + r], inv) << (4 * r);
             w[q] = word;
         }
-        *reinterpret_cast<uint4*>(xq + t * (d / 2) + b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-        xs[t * nb + b] = (uint8_t)(X + 127);
-    }
-}
-
-__global__ void __launch_bounds__(PLAN_THREADS) ffn_plan_quant(const int32_t* sel_slot, int P, int S, int bn,
-                                                               int32_t* rank, int32_t* pair_of_pos,
-                                                               int32_t* offsets, int32_t* tile_off, int4* work,
-                                                               int32_t* n_work, uint32_t* err, const uint16_t* x,
-                                                               int T, int d, uint8_t* xq, uint8_t* xs) {
-    extern __shared__ int32_t cnt[];
-    if (blockIdx.x == 0) {
-        plan_block(sel_slot, P, S, bn, rank, pair_of_pos, offsets, tile_off, work, n_work, err, cnt);
-    } else {
-        quant_rows(x, T, d, xq, xs, blockIdx.x - 1, gridDim.x - 1);
+        *reinterpret_cast<uint4*>(xp + (size_t)pos * (d / 2) + b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        xsp[operand_scale_offset(pos, b, bn, d)] = (uint8_t)(X + 127);
     }
 }
 
@@ -148,24 +140,28 @@ __global__ void __launch_bounds__(256) ffn_combine(const float* __restrict__ Y, 
 
 cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
     const int P = a.T * a.k;
-    const long qthreads = (long)a.T * (a.d / 32);
-    int qblocks = (int)((qthreads + PLAN_THREADS - 1) / PLAN_THREADS);
-    if (qblocks > 4 * moe_sm_count()) qblocks = 4 * moe_sm_count();
     const size_t smem = (size_t)a.S * sizeof(int32_t);
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_plan_quant, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 4);
+        cudaError_t e = cudaFuncSetAttribute(ffn_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 4);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    moe_prof_begin(MK_PLAN_QUANT, s);
-    ffn_plan_quant<<<1 + qblocks, PLAN_THREADS, smem, s>>>(a.sel_slot, P, a.S, a.bn, a.rank, a.pair_of_pos, a.offsets,
-                                                           a.tile_off, a.work, a.n_work, a.err, a.x, a.T, a.d, a.xq,
-                                                           a.xs);
-    moe_prof_end(MK_PLAN_QUANT, s);
-    moe_count_launches(1);
+    moe_prof_begin(MK_PLAN, s);
+    ffn_plan<<<1, PLAN_THREADS, smem, s>>>(a.sel_slot, P, a.S, a.bn, a.pos_of_pair, a.pair_of_pos, a.seg, a.tile_off,
+                                           a.work, a.n_work, a.err);
+    moe_prof_end(MK_PLAN, s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long tasks = (long)P * (a.d / 32);
+    long blocks = (tasks + 255) / 256;
+    if (blocks > 8L * moe_sm_count()) blocks = 8L * moe_sm_count();
+    moe_prof_begin(MK_PACK, s);
+    ffn_pack<<<(unsigned)blocks, 256, 0, s>>>(a.x, a.pos_of_pair, P, a.k, a.d, a.bn, a.xp, a.xsp);
+    moe_prof_end(MK_PACK, s);
+    moe_count_launches(2);
     return cudaGetLastError();
 }
 
