@@ -63,20 +63,25 @@ typedef enum {
  * Passed by HOST pointer; `base` is a device pointer to n_slots records of
  * slot_bytes each. Slots [0, n_main) form the main arena and the rest the
  * hot-read ring (README item 3); the FFN treats them alike.
- * One slot record holds one expert in MXFP4 (two e2m1 codes per byte, the
- * even element in the LOW nibble, K contiguous; one e8m0 byte per 32 K):
- *   off_gu_codes   [2*ffn, d/2]   row-major; gate rows 0..ffn-1, then up rows ffn..2ffn-1
- *   off_gu_scales  2*ffn*d/32 bytes, tile-atom order (below)
- *   off_dn_codes   [d, ffn/2]     row-major
+ * One slot record holds one expert in MXFP4 (e2m1 codes, two per byte with
+ * the even element in the LOW nibble; one e8m0 scale byte per 32 along K).
+ * Logically the expert is W_gu [2*ffn, d] (gate rows 0..ffn-1, then up rows
+ * ffn..2ffn-1) and W_dn [d, ffn]. The record stores them in the order the
+ * tensor cores consume them, so that every pipeline stage is one contiguous
+ * copy:
+ *   off_gu_codes   (ffn/64) * ceil(d/256) * 16384 bytes, tile-major code blocks
+ *   off_gu_scales  2*ffn*d/32 bytes, tile-atom order
+ *   off_dn_codes   (d/128) * ceil(ffn/256) * 16384 bytes, tile-major code blocks
  *   off_dn_scales  d*ffn/32 bytes, tile-atom order
- * Tile-atom order of a scale matrix S[row, kb] (kb = K-block of 32): rows are
- * grouped in 128-row tiles -- for gate/up, tile g is gate rows 64g..64g+63
- * followed by up rows ffn+64g..ffn+64g+63; for down, rows 128g..128g+127 --
- * and each tile's scales are stored as consecutive 512-byte atoms of four
- * K-blocks: S[row, 4a + k] of tile row r sits at byte
- *   (g * (K/128) + a) * 512 + (r % 32) * 16 + (r / 32) * 4 + k.
- * (This is the order in which the tensor cores take block scales, so a stage
- * of scales is one contiguous copy.)
+ * Tiles: rows are grouped in tiles of 128 -- for W_gu, tile g is gate rows
+ * 64g..64g+63 followed by up rows ffn+64g..ffn+64g+63; for W_dn, rows
+ * 128g..128g+127. Tile row r is the r-th row of that list.
+ * Tile-major code blocks: for tile g and chunk c of 256 elements along K
+ * (128 bytes; zero past the row end), a 16 KB block of 128 rows x 128 bytes
+ * at byte (g * ceil(K/256) + c) * 16384; within it, the 16-byte piece q of
+ * tile row r is stored at r * 128 + (q ^ (r % 8)) * 16 (the 128-byte swizzle).
+ * Tile-atom scales: scale S[row, 4a + k] (K-block 4a + k) of tile row r is at
+ * byte (g * (K/128) + a) * 512 + (r % 32) * 16 + (r / 32) * 4 + k.
  * Requirements: base and every offset 256-byte aligned, slot_bytes a multiple
  * of 256, d and ffn multiples of 128.
  */

@@ -265,8 +265,8 @@ moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot
     if (b % 256 || arena->off_gu_codes % 256 || arena->off_gu_scales % 256 || arena->off_dn_codes % 256 ||
         arena->off_dn_scales % 256)
         return MOE_EINVAL;
-    const int64_t guc = (int64_t)2 * F * d / 2, gus = (int64_t)2 * F * d / 32;
-    const int64_t dnc = (int64_t)d * F / 2, dns = (int64_t)d * F / 32;
+    const int64_t guc = (int64_t)(F / 64) * ((d + 255) / 256) * 16384, gus = (int64_t)2 * F * d / 32;
+    const int64_t dnc = (int64_t)(d / 128) * ((F + 255) / 256) * 16384, dns = (int64_t)d * F / 32;
     auto inside = [&](int64_t off, int64_t len) { return off >= 0 && off + len <= arena->slot_bytes; };
     if (!inside(arena->off_gu_codes, guc) || !inside(arena->off_gu_scales, gus) || !inside(arena->off_dn_codes, dnc) ||
         !inside(arena->off_dn_scales, dns))

@@ -17,12 +17,14 @@
 // B operand (N = 16..128), so a decode-sized tile still streams whole weight
 // tiles at full width. Every operand arrives by TMA / bulk copy issued by one
 // thread, so a stage costs one DRAM round trip and nothing else:
-//   warp 4     lane 0, per stage of 256 K: two 64-row boxes of weight codes
-//              (128-byte swizzle), one box of activation rows (its height the
-//              tile's row count rounded up), and two 1-D bulk copies of scale
-//              atoms (weights: from the arena, which keeps scales in the
-//              tensor cores' atom order; activations: from the workspace,
-//              written in that order by ffn_pack / the gate/up epilogue);
+//   warp 4     lane 0, per stage of 512 K: one 32 KB bulk copy of two weight
+//              code blocks (the arena keeps codes in tile-major blocks, already
+//              in the 128-byte swizzle, so a stage is one contiguous DRAM
+//              stream), two TMA boxes of activation rows (their height the
+//              tile's row count rounded up), and two 1-D bulk copies of scale atoms
+//              (weights: from the arena, which keeps scales in the tensor
+//              cores' atom order; activations: from the workspace, written in
+//              that order by ffn_pack / the gate/up epilogue);
 //   warp 5     TMEM allocator; lane 0 issues tcgen05.cp (scales -> TMEM) and
 //              tcgen05.mma, and commits to the stage / accumulator barriers;
 //   warps 0-3  epilogue: tcgen05.ld of their 32-lane quadrant of the
@@ -42,13 +44,13 @@
 namespace {
 
 struct GemmMaps {
-    CUtensorMap a;        // weight codes: (row bytes, rows, slots), box 128 B x 64 rows x 1
     CUtensorMap b[4];     // activation codes: (row bytes, positions), box 128 B x {16, 32, 64, 128} rows
 };
 
 struct GemmArgs {
     const uint8_t* arena;
     int64_t slot_bytes;
+    int64_t off_codes;           // this GEMM's weight codes within a slot (tile-major 16 KB blocks)
     int64_t off_scales;          // this GEMM's weight scales within a slot (tile-atom order)
     int K;                       // reduction length: d (gate/up) or ffn (down)
     int m_tiles;
@@ -64,12 +66,20 @@ struct GemmArgs {
     uint32_t* err;
 };
 
-template <int MODE, int BN, int NS>
+// One pipeline stage covers KCH chunks of 256 elements along K: KCH 16 KB
+// weight-code blocks (contiguous in the arena), KCH activation boxes and the
+// matching scale atoms (2 per chunk per operand, contiguous). Bigger stages
+// amortise the per-stage barrier round trip.
+template <int MODE, int BN, int NS, int KCH>
 struct Cfg {
     static constexpr int THREADS = 192;           // warps 0-3 epilogue, 4 TMA, 5 MMA
-    static constexpr int A_BYTES = 128 * 128;     // 128 rows x 128 B = 256 e2m1 along K
-    static constexpr int B_BYTES = BN * 128;
-    static constexpr int SF_BYTES = 2048;         // A atom 0, A atom 1, B atom 0, B atom 1 (512 B each)
+    static constexpr int BLK = 128 * 128;         // one 16 KB code block: 128 rows x 256 e2m1
+    static constexpr int A_BYTES = KCH * BLK;
+    static constexpr int B_CHUNK = BN * 128;
+    static constexpr int B_BYTES = KCH * B_CHUNK;
+    static constexpr int SF_HALF = KCH * 1024;    // weight atoms, then activation atoms
+    static constexpr int SF_BYTES = 2 * SF_HALF;
+    static constexpr int SF_COLS = 16 * KCH;      // TMEM columns of one stage's scales
     static constexpr int XCH_STRIDE = 17;         // floats per exchange row (16 columns + pad)
     static constexpr int XCH_BYTES = MODE == 1 ? 64 * XCH_STRIDE * 4 : 0;
     static constexpr int OFF_A = 0;
@@ -80,17 +90,18 @@ struct Cfg {
     static constexpr int N_BARS = 2 * NS + 6;
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
-    static constexpr int TMEM_USED = 2 * BN + 16 * NS;
+    static constexpr int TMEM_USED = 2 * BN + SF_COLS * NS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
     static_assert(BN == 16 || BN == 32 || BN == 64 || BN == 128, "BN");
+    static_assert(KCH == 1 || KCH == 2, "KCH");
     static_assert(TMEM_USED <= 512, "TMEM");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-template <int MODE, int BN, int NS>
+template <int MODE, int BN, int NS, int KCH>
 __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
-    using C = Cfg<MODE, BN, NS>;
+    using C = Cfg<MODE, BN, NS, KCH>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -110,7 +121,6 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
         mbar_init(uread, 2);
         *abort_flag = 0;
         fence_barrier_init();
-        prefetch_tmap(&maps.a);
         for (int i = 0; i < 4; ++i) prefetch_tmap(&maps.b[i]);
     }
     if (warp == 5) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
@@ -120,8 +130,9 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
     const uint32_t tmem = *tmem_slot;
 
     const int n_items = *a.n_work * a.m_tiles;
-    const int nk = (a.K + 255) / 256;
-    const int atoms_per_tile = a.K / 128;
+    const int nc = (a.K + 255) / 256;                 // 256-element chunks along K
+    const int nst = (nc + KCH - 1) / KCH;             // pipeline stages per item
+    const int atoms = a.K / 128;                      // scale atoms per 128-row tile
 
     if (warp == 4) {
         // ------------------------------------------------------------ TMA producer (one thread)
@@ -137,25 +148,28 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
                 const int slot = w.x, pos0 = w.y, nv = w.z;
                 const int hb = nv <= 16 ? 0 : nv <= 32 ? 1 : nv <= 64 ? 2 : 3;   // activation box height
                 const uint32_t b_bytes = (16u << hb) * 128u;
-                const uint8_t* sfa = a.arena + (size_t)slot * a.slot_bytes + a.off_scales +
-                                     (size_t)mt * atoms_per_tile * 512;
-                const uint8_t* sfb = a.b_scales + (size_t)(pos0 / BN) * atoms_per_tile * 512;
-                const int yA0 = MODE == 1 ? mt * 64 : mt * 128;
-                const int yA1 = MODE == 1 ? a.F + mt * 64 : mt * 128 + 64;
-                for (int kc = 0; kc < nk; ++kc, ++it) {
+                const uint8_t* rec = a.arena + (size_t)slot * a.slot_bytes;
+                const uint8_t* codes = rec + a.off_codes + (size_t)mt * nc * C::BLK;
+                const uint8_t* sfa = rec + a.off_scales + (size_t)mt * atoms * 512;
+                const uint8_t* sfb = a.b_scales + (size_t)(pos0 / BN) * atoms * 512;
+                for (int st = 0; st < nst; ++st, ++it) {
                     const int s = (int)(it % NS);
                     const uint32_t r = it / NS;
                     if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
                     uint8_t* As = smem + C::OFF_A + s * C::A_BYTES;
                     uint8_t* Bs = smem + C::OFF_B + s * C::B_BYTES;
                     uint8_t* SFs = smem + C::OFF_SF + s * C::SF_BYTES;
-                    const uint32_t sf_bytes = (a.K - kc * 256 >= 256) ? 1024u : 512u;
-                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + b_bytes + 2 * sf_bytes);
-                    tma_load_3d(As, &maps.a, &full[s], kc * 128, yA0, slot);
-                    tma_load_3d(As + 64 * 128, &maps.a, &full[s], kc * 128, yA1, slot);
-                    tma_load_2d(Bs, &maps.b[hb], &full[s], kc * 128, pos0);
-                    bulk_load(SFs, sfa + (size_t)kc * 1024, sf_bytes, &full[s]);
-                    bulk_load(SFs + 1024, sfb + (size_t)kc * 1024, sf_bytes, &full[s]);
+                    const int c0 = st * KCH;
+                    const int chunks = nc - c0 < KCH ? nc - c0 : KCH;
+                    const int at0 = 2 * c0;
+                    const int ats = atoms - at0 < 2 * KCH ? atoms - at0 : 2 * KCH;
+                    const uint32_t sf_bytes = (uint32_t)ats * 512u;
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)chunks * (C::BLK + b_bytes) + 2 * sf_bytes);
+                    bulk_load(As, codes + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK, &full[s]);
+                    for (int q = 0; q < chunks; ++q)
+                        tma_load_2d(Bs + q * C::B_CHUNK, &maps.b[hb], &full[s], (c0 + q) * 128, pos0);
+                    bulk_load(SFs, sfa + (size_t)at0 * 512, sf_bytes, &full[s]);
+                    bulk_load(SFs + C::SF_HALF, sfb + (size_t)at0 * 512, sf_bytes, &full[s]);
                 }
             }
         }
@@ -172,28 +186,28 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
                 if (!mbar_wait(&acce[b], (u & 1) ^ 1, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t dt = tmem + b * BN;
-                for (int kc = 0; kc < nk; ++kc, ++it) {
+                for (int st = 0; st < nst; ++st, ++it) {
                     const int s = (int)(it % NS);
                     const uint32_t r = it / NS;
                     if (!mbar_wait(&full[s], r & 1, abort_flag)) { ok_run = false; break; }
                     tc_fence_after();
-                    const int rem = (a.K - kc * 256) / 64;
-                    const int ksteps = rem < 4 ? rem : 4;
-                    const uint32_t sfc = tmem + 2 * BN + s * 16;
+                    const int rem = (a.K - st * 256 * KCH) / 64;
+                    const int ksteps = rem < 4 * KCH ? rem : 4 * KCH;      // MMAs of K = 64
+                    const int ats = (ksteps + 1) / 2;                        // scale atoms used (2 MMAs each)
+                    const uint32_t sfc = tmem + 2 * BN + s * C::SF_COLS;
                     const uint32_t sfs = smem_u32(smem + C::OFF_SF + s * C::SF_BYTES);
-                    tc_cp_sf_atom(sfc + 0, smem_desc_sf(sfs));
-                    tc_cp_sf_atom(sfc + 8, smem_desc_sf(sfs + 1024));
-                    if (ksteps > 2) {
-                        tc_cp_sf_atom(sfc + 4, smem_desc_sf(sfs + 512));
-                        tc_cp_sf_atom(sfc + 12, smem_desc_sf(sfs + 1536));
+                    for (int q = 0; q < ats; ++q) {
+                        tc_cp_sf_atom(sfc + 4 * q, smem_desc_sf(sfs + 512 * q));
+                        tc_cp_sf_atom(sfc + 8 * KCH + 4 * q, smem_desc_sf(sfs + C::SF_HALF + 512 * q));
                     }
                     const uint32_t as = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
                     const uint32_t bs = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
                     for (int kk = 0; kk < ksteps; ++kk) {
+                        const int q = kk >> 2, kq = kk & 3;
                         const int sfid = (kk & 1) * 2;
-                        tc_mma_mxf4(dt, smem_desc_sw128(as + kk * 32), smem_desc_sw128(bs + kk * 32),
-                                    idesc_mxf4(N, sfid, sfid), sfc + (kk >> 1) * 4, sfc + 8 + (kk >> 1) * 4,
-                                    (kc | kk) != 0 ? 1u : 0u);
+                        tc_mma_mxf4(dt, smem_desc_sw128(as + q * C::BLK + kq * 32),
+                                    smem_desc_sw128(bs + q * C::B_CHUNK + kq * 32), idesc_mxf4(N, sfid, sfid),
+                                    sfc + (kk >> 1) * 4, sfc + 8 * KCH + (kk >> 1) * 4, (st | kk) != 0 ? 1u : 0u);
                     }
                     tc_commit(&empty[s]);
                 }
@@ -317,15 +331,6 @@ cudaError_t encode(CUtensorMap* m, const uint8_t* base, int rank, const cuuint64
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Weight codes of every slot: (row bytes, rows, slots); box 128 bytes x 64 rows x 1 slot.
-cudaError_t make_weight_map(CUtensorMap* m, const uint8_t* base, uint64_t row_bytes, uint64_t rows, uint64_t slots,
-                            uint64_t slot_bytes) {
-    cuuint64_t dims[3] = {row_bytes, rows, slots};
-    cuuint64_t strides[2] = {row_bytes, slot_bytes};
-    cuuint32_t box[3] = {128, 64, 1};
-    return encode(m, base, 3, dims, strides, box);
-}
-
 // Activation operand rows: (row bytes, positions); boxes of 16, 32, 64 and 128 rows.
 cudaError_t make_act_maps(CUtensorMap* m, const uint8_t* base, uint64_t row_bytes, uint64_t rows) {
     for (int i = 0; i < 4; ++i) {
@@ -338,10 +343,10 @@ cudaError_t make_act_maps(CUtensorMap* m, const uint8_t* base, uint64_t row_byte
     return cudaSuccess;
 }
 
-template <int MODE, int BN, int NS>
+template <int MODE, int BN, int NS, int KCH>
 cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& g, long max_items, cudaStream_t s) {
-    using C = Cfg<MODE, BN, NS>;
-    auto kern = ffn_gemm_kernel<MODE, BN, NS>;
+    using C = Cfg<MODE, BN, NS, KCH>;
+    auto kern = ffn_gemm_kernel<MODE, BN, NS, KCH>;
     static int occ_cache[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -369,10 +374,10 @@ cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& g, long max_items, 
 template <int MODE>
 cudaError_t launch_mode(const GemmMaps& maps, const GemmArgs& g, long max_items, int bn, cudaStream_t s) {
     switch (bn) {
-        case 16: return launch_one<MODE, 16, 10>(maps, g, max_items, s);
-        case 32: return launch_one<MODE, 32, 9>(maps, g, max_items, s);
-        case 64: return launch_one<MODE, 64, 8>(maps, g, max_items, s);
-        default: return launch_one<MODE, 128, 6>(maps, g, max_items, s);
+        case 16: return launch_one<MODE, 16, 5, 2>(maps, g, max_items, s);
+        case 32: return launch_one<MODE, 32, 4, 2>(maps, g, max_items, s);
+        case 64: return launch_one<MODE, 64, 4, 2>(maps, g, max_items, s);
+        default: return launch_one<MODE, 128, 3, 2>(maps, g, max_items, s);
     }
 }
 
@@ -382,12 +387,7 @@ cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches
     const moe_arena& ar = *a.arena;
     const uint8_t* base = static_cast<const uint8_t*>(ar.base);
     GemmMaps m1, m2;
-    cudaError_t e = make_weight_map(&m1.a, base + ar.off_gu_codes, (uint64_t)a.d / 2, (uint64_t)2 * a.F,
-                                    (uint64_t)ar.n_slots, (uint64_t)ar.slot_bytes);
-    if (e == cudaSuccess) e = make_act_maps(m1.b, a.xp, (uint64_t)a.d / 2, (uint64_t)a.pad_max);
-    if (e == cudaSuccess)
-        e = make_weight_map(&m2.a, base + ar.off_dn_codes, (uint64_t)a.F / 2, (uint64_t)a.d, (uint64_t)ar.n_slots,
-                            (uint64_t)ar.slot_bytes);
+    cudaError_t e = make_act_maps(m1.b, a.xp, (uint64_t)a.d / 2, (uint64_t)a.pad_max);
     if (e == cudaSuccess) e = make_act_maps(m2.b, a.hq, (uint64_t)a.F / 2, (uint64_t)a.pad_max);
     if (e != cudaSuccess) return e;
 
@@ -402,6 +402,7 @@ cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches
     g.err = a.err;
 
     GemmArgs g1 = g;       // gate/up + SwiGLU
+    g1.off_codes = ar.off_gu_codes;
     g1.off_scales = ar.off_gu_scales;
     g1.K = a.d;
     g1.m_tiles = a.F / 64;
@@ -412,6 +413,7 @@ cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches
     if (e != cudaSuccess) return e;
 
     GemmArgs g2 = g;       // down
+    g2.off_codes = ar.off_dn_codes;
     g2.off_scales = ar.off_dn_scales;
     g2.K = a.F;
     g2.m_tiles = a.d / 128;

@@ -6,8 +6,8 @@
 // its flat id layer * E + expert.
 //   codes byte j  = byte (j % 8) of hash(j / 8)            (uniform nibbles)
 //   scale byte j  = 121 + ((hash(j / 32) >> 2 * (j % 32)) & 3)   (2^U, U in -6..-3)
-// where j is the row-major index; codes are stored row-major, scales at their
-// position in the arena's tile-atom order.
+// where j is the row-major index; codes are stored in tile-major 16 KB blocks
+// and scales in tile-atom order (the arena record layout).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -30,27 +30,45 @@ __device__ inline uint64_t hash_at(uint64_t base, uint64_t idx) { return mix(bas
 
 struct Region {
     int64_t off;
-    int64_t bytes;
+    int64_t bytes;    // logical bytes (rows x bytes per row)
     uint32_t tid;
-    int scales;       // 0: codes; 1: scales of a gate/up matrix; 2: scales of a down matrix
-    int kb;           // scale bytes per row (K / 32)
+    int scales;       // codes: 0; scales: 1 (gate/up matrix) or 2 (down matrix)
+    int kb;           // bytes per row: K / 2 for codes, K / 32 for scales
     int ffn;
+    int gate_up;      // codes: 1 for the gate/up matrix
 };
+
+// Tile (128 rows) and tile row of a logical row: gate/up tiles are 64 gate rows
+// followed by the matching 64 up rows; down tiles are 128 consecutive rows.
+__device__ inline void tile_of(int64_t row, bool gate_up, int ffn, int64_t* tile, int64_t* tr) {
+    if (gate_up) {
+        const bool up = row >= ffn;
+        const int64_t f = up ? row - ffn : row;
+        *tile = f / 64;
+        *tr = (up ? 64 : 0) + f % 64;
+    } else {
+        *tile = row / 128;
+        *tr = row % 128;
+    }
+}
+
+// Position of logical code byte `col` of `row` in the tile-major block order:
+// 16 KB blocks of 128 rows x 128 bytes per (tile, chunk of 128 bytes along the
+// row), 16-byte piece c of tile row r at piece c ^ (r % 8).
+__device__ inline int64_t packed_code_offset(const Region& r, int64_t row, int64_t col) {
+    int64_t tile, tr;
+    tile_of(row, r.gate_up != 0, r.ffn, &tile, &tr);
+    const int64_t nkc = (r.kb + 127) / 128;
+    const int64_t kc = col / 128, piece = (col % 128) / 16;
+    return (tile * nkc + kc) * 16384 + tr * 128 + ((piece ^ (tr & 7)) * 16) + col % 16;
+}
 
 // Position of logical scale byte (row, k-block) in the arena's tile-atom order:
 // 128-row tiles (gate/up: 64 gate rows f0.. then the 64 up rows ffn+f0..),
 // 512-byte atoms of 4 k-blocks, byte (r % 32) * 16 + (r / 32) * 4 + kb % 4.
 __device__ inline int64_t packed_scale_offset(const Region& r, int64_t row, int kb) {
     int64_t tile, tr;
-    if (r.scales == 1) {
-        const bool up = row >= r.ffn;
-        const int64_t f = up ? row - r.ffn : row;
-        tile = f / 64;
-        tr = (up ? 64 : 0) + f % 64;
-    } else {
-        tile = row / 128;
-        tr = row % 128;
-    }
+    tile_of(row, r.scales == 1, r.ffn, &tile, &tr);
     const int64_t atoms_per_tile = r.kb / 4;
     return (tile * atoms_per_tile + kb / 4) * 512 + (tr % 32) * 16 + (tr / 32) * 4 + kb % 4;
 }
@@ -69,11 +87,12 @@ __global__ void fill_slots(uint8_t* arena, int64_t slot_bytes, Region r0, Region
     for (int q = 0; q < 4; ++q) {
         const Region r = rs[q];
         const uint64_t base = stream_base(seed, r.tid, layer, expert);
-        uint64_t* dst = reinterpret_cast<uint64_t*>(rec + r.off);
         if (!r.scales) {
-            const int64_t words = r.bytes / 8;
-            for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < words; w += (int64_t)gridDim.x * blockDim.x)
-                dst[w] = hash_at(base, (uint64_t)w);
+            const int64_t words = r.bytes / 8;              // 8 logical bytes stay within one 16-byte piece
+            for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < words; w += (int64_t)gridDim.x * blockDim.x) {
+                const int64_t row = (w * 8) / r.kb, col = (w * 8) % r.kb;
+                *reinterpret_cast<uint64_t*>(rec + r.off + packed_code_offset(r, row, col)) = hash_at(base, (uint64_t)w);
+            }
         } else {
             uint8_t* dstb = rec + r.off;
             const int64_t groups = r.bytes / 32;                 // one hash -> 32 logical scale bytes
@@ -102,10 +121,10 @@ int synth_fill_slots(void* arena_base, int64_t slot_bytes, int64_t off_gu_codes,
                      int64_t off_dn_codes, int64_t off_dn_scales, int d, int ffn, const int32_t* slots,
                      const int32_t* flats, int slot_begin, int n, int E, uint64_t seed, void* stream) {
     if (n <= 0) return 0;
-    Region r0{off_gu_codes, (int64_t)2 * ffn * d / 2, 4, 0, 0, ffn};
-    Region r1{off_gu_scales, (int64_t)2 * ffn * d / 32, 5, 1, d / 32, ffn};
-    Region r2{off_dn_codes, (int64_t)d * ffn / 2, 6, 0, 0, ffn};
-    Region r3{off_dn_scales, (int64_t)d * ffn / 32, 7, 2, ffn / 32, ffn};
+    Region r0{off_gu_codes, (int64_t)2 * ffn * d / 2, 4, 0, d / 2, ffn, 1};
+    Region r1{off_gu_scales, (int64_t)2 * ffn * d / 32, 5, 1, d / 32, ffn, 0};
+    Region r2{off_dn_codes, (int64_t)d * ffn / 2, 6, 0, ffn / 2, ffn, 0};
+    Region r3{off_dn_scales, (int64_t)d * ffn / 32, 7, 2, ffn / 32, ffn, 0};
     dim3 grid(64, n);
     fill_slots<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint8_t*>(arena_base), slot_bytes,
                                                                     r0, r1, r2, r3, slots, flats, slot_begin, n, E,

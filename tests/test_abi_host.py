@@ -81,8 +81,11 @@ def test_route_rejects_bad_arguments():
 
 
 def _arena(**kw):
-    a = dict(base=0x100000, slot_bytes=52224, n_slots=16, d=256, ffn=128, reserved=0,
-             off_gu_codes=0, off_gu_scales=32768, off_dn_codes=34816, off_dn_scales=51200)
+    import synth
+    rec = synth.slot_record(256, 128)
+    a = dict(base=0x100000, slot_bytes=rec["slot_bytes"], n_slots=16, d=256, ffn=128, reserved=0,
+             off_gu_codes=rec["off_gu_codes"], off_gu_scales=rec["off_gu_scales"],
+             off_dn_codes=rec["off_dn_codes"], off_dn_scales=rec["off_dn_scales"])
     a.update(kw)
     return moe.MoeArena(ctypes.c_void_p(a["base"]), a["slot_bytes"], a["n_slots"], a["d"], a["ffn"], 0,
                         a["off_gu_codes"], a["off_gu_scales"], a["off_dn_codes"], a["off_dn_scales"])
@@ -92,9 +95,9 @@ def _arena(**kw):
     (dict(d=200), moe.MOE_EINVAL),                  # d % 128
     (dict(ffn=96), moe.MOE_EINVAL),                 # ffn % 128
     (dict(base=0x100010), moe.MOE_EINVAL),          # arena base not 256-aligned
-    (dict(off_dn_scales=51300), moe.MOE_EINVAL),    # offset not 256-aligned
-    (dict(off_dn_scales=52224), moe.MOE_EINVAL),    # region past the end of the slot
-    (dict(slot_bytes=52000), moe.MOE_EINVAL),       # slot size not a multiple of 256
+    (dict(off_dn_scales=67584 + 100), moe.MOE_EINVAL),   # offset not 256-aligned
+    (dict(off_dn_scales=68608), moe.MOE_EINVAL),         # region past the end of the slot
+    (dict(slot_bytes=68600), moe.MOE_EINVAL),            # slot size not a multiple of 256
     (dict(n_slots=20000), moe.MOE_EUNSUPPORTED),    # beyond the per-call slot limit
     (dict(), moe.MOE_ENOMEM),                       # valid arena, workspace too small
 ])
