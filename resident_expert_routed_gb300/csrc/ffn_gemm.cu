@@ -6,31 +6,30 @@
 // routed only to resident slots (item 2). One launch per GEMM covers every
 // used slot: the work list from ffn_plan names (slot, first row, rows) tiles.
 //
-//   gate/up (MODE 1): for 64 ffn features f0..f0+63 of one slot, D = [Wg; Wu]
-//       rows (64 gate + 64 up = M 128) x the tile's activation rows (N), K = d;
-//       epilogue: h = silu(g) * u, re-quantised to MXFP4 in blocks of 32
-//       features (OCP MX v1.0 rule) into the down GEMM's activation operand.
+//   gate/up (MODE 1): for 128 ffn features f0..f0+127 of one slot, two MMAs
+//       per K step, D_g = Wg[f0..] x A and D_u = Wu[f0..] x A (M 128 each, N =
+//       the tile's activation rows, K = d) into two TMEM accumulators; the
+//       epilogue thread of TMEM lane f holds g and u of feature f0 + f, forms
+//       h = silu(g) * u and re-quantises it to MXFP4 in blocks of 32 features
+//       (one warp = one block; OCP MX v1.0 rule) into the down GEMM's operand.
 //   down (MODE 2): for 128 output rows d0..d0+127, D = Wd rows x hq rows,
 //       K = ffn; epilogue: fp32 rows Y[pick] (combined later in pick order).
 //
-// The weight tile is the MMA's A operand (M = 128) and the few routed rows the
-// B operand (N = 16..128), so a decode-sized tile still streams whole weight
-// tiles at full width. Every operand arrives by TMA / bulk copy issued by one
-// thread, so a stage costs one DRAM round trip and nothing else:
-//   warp 4     lane 0, per stage of 512 K: one 32 KB bulk copy of two weight
-//              code blocks (the arena keeps codes in tile-major blocks, already
-//              in the 128-byte swizzle, so a stage is one contiguous DRAM
-//              stream), two TMA boxes of activation rows (their height the
-//              tile's row count rounded up), and two 1-D bulk copies of scale atoms
-//              (weights: from the arena, which keeps scales in the tensor
-//              cores' atom order; activations: from the workspace, written in
-//              that order by ffn_pack / the gate/up epilogue);
+// The weight tiles are the MMA's A operand (M = 128) and the few routed rows
+// the B operand (N = 16..128), so a decode-sized tile still streams whole
+// weight tiles at full width. Every operand arrives by bulk copy / TMA issued
+// by one thread, so a stage costs one DRAM round trip and nothing else:
+//   warp 4     lane 0, per stage: 32 KB of weight codes as contiguous bulk
+//              copies (the arena keeps codes in tile-major 16 KB blocks, already
+//              in the 128-byte swizzle), TMA boxes of activation rows (their
+//              height the tile's row count rounded up), and 1-D bulk copies of
+//              scale atoms (weights: from the arena, which keeps scales in the
+//              tensor cores' atom order; activations: from the workspace,
+//              written in that order by ffn_pack / the gate/up epilogue);
 //   warp 5     TMEM allocator; lane 0 issues tcgen05.cp (scales -> TMEM) and
 //              tcgen05.mma, and commits to the stage / accumulator barriers;
 //   warps 0-3  epilogue: tcgen05.ld of their 32-lane quadrant of the
-//              double-buffered accumulator, then the per-mode epilogue (the
-//              up-projection rows reach the gate rows' warps through a small
-//              shared-memory exchange, 16 columns at a time).
+//              (double-buffered) accumulators, then the per-mode epilogue.
 // The grid is persistent (one CTA per SM) over the flattened (tile, 128-row
 // weight block) items. Every wait is bounded (MOE_WAIT_LIMIT_NS); on expiry
 // the CTA raises its abort flag, every role leaves its loop, TMEM is freed and
@@ -66,59 +65,56 @@ struct GemmArgs {
     uint32_t* err;
 };
 
-// One pipeline stage covers KCH chunks of 256 elements along K: KCH 16 KB
-// weight-code blocks (contiguous in the arena), KCH activation boxes and the
-// matching scale atoms (2 per chunk per operand, contiguous). Bigger stages
-// amortise the per-stage barrier round trip.
-template <int MODE, int BN, int NS, int KCH>
+// Per pipeline stage: KCH chunks of 256 elements along K. The gate/up GEMM
+// loads, per chunk, one 16 KB code block of the gate tile and one of the up
+// tile (rows f0..f0+127 and ffn+f0..ffn+f0+127) and accumulates them into two
+// TMEM accumulators, so that each epilogue thread holds g and u of the same
+// feature; the down GEMM loads one tile. Stages carry 32 KB of weights.
+template <int MODE, int BN, int NS, int KCH, int NBUF>
 struct Cfg {
     static constexpr int THREADS = 192;           // warps 0-3 epilogue, 4 TMA, 5 MMA
+    static constexpr int NMAT = MODE == 1 ? 2 : 1;
     static constexpr int BLK = 128 * 128;         // one 16 KB code block: 128 rows x 256 e2m1
-    static constexpr int A_BYTES = KCH * BLK;
+    static constexpr int A_BYTES = NMAT * KCH * BLK;
     static constexpr int B_CHUNK = BN * 128;
     static constexpr int B_BYTES = KCH * B_CHUNK;
-    static constexpr int SF_HALF = KCH * 1024;    // weight atoms, then activation atoms
-    static constexpr int SF_BYTES = 2 * SF_HALF;
-    static constexpr int SF_COLS = 16 * KCH;      // TMEM columns of one stage's scales
-    static constexpr int XCH_STRIDE = 17;         // floats per exchange row (16 columns + pad)
-    static constexpr int XCH_BYTES = MODE == 1 ? 64 * XCH_STRIDE * 4 : 0;
+    static constexpr int SFA_MAT = KCH * 1024;    // weight atoms of one matrix (2 per chunk)
+    static constexpr int SF_BYTES = (NMAT + 1) * SFA_MAT;
+    static constexpr int SF_COLS = (NMAT + 1) * 8 * KCH;   // TMEM columns of one stage's scales
+    static constexpr int ACC_COLS = NMAT * BN;    // one accumulator buffer (gate, then up)
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + NS * A_BYTES;
     static constexpr int OFF_SF = OFF_B + NS * B_BYTES;
-    static constexpr int OFF_XCH = OFF_SF + NS * SF_BYTES;
-    static constexpr int OFF_BAR = (OFF_XCH + XCH_BYTES + 7) / 8 * 8;
-    static constexpr int N_BARS = 2 * NS + 6;
+    static constexpr int OFF_BAR = OFF_SF + NS * SF_BYTES;
+    static constexpr int N_BARS = 2 * NS + 2 * NBUF;
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
-    static constexpr int TMEM_USED = 2 * BN + SF_COLS * NS;
+    static constexpr int TMEM_USED = NBUF * ACC_COLS + SF_COLS * NS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
     static_assert(BN == 16 || BN == 32 || BN == 64 || BN == 128, "BN");
     static_assert(KCH == 1 || KCH == 2, "KCH");
+    static_assert(NBUF == 1 || NBUF == 2, "NBUF");
     static_assert(TMEM_USED <= 512, "TMEM");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-template <int MODE, int BN, int NS, int KCH>
+template <int MODE, int BN, int NS, int KCH, int NBUF>
 __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
-    using C = Cfg<MODE, BN, NS, KCH>;
+    using C = Cfg<MODE, BN, NS, KCH, NBUF>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* empty = full + NS;
     uint64_t* accf = empty + NS;
-    uint64_t* acce = accf + 2;
-    uint64_t* uready = acce + 2;       // gate/up exchange: up values written (warps 2, 3)
-    uint64_t* uread = uready + 1;      // gate/up exchange: up values consumed (warps 0, 1)
+    uint64_t* acce = accf + NBUF;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int b = 0; b < 2; ++b) { mbar_init(&accf[b], 1); mbar_init(&acce[b], 4); }
-        mbar_init(uready, 2);
-        mbar_init(uread, 2);
+        for (int b = 0; b < NBUF; ++b) { mbar_init(&accf[b], 1); mbar_init(&acce[b], 4); }
         *abort_flag = 0;
         fence_barrier_init();
         for (int i = 0; i < 4; ++i) prefetch_tmap(&maps.b[i]);
@@ -149,8 +145,12 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
                 const int hb = nv <= 16 ? 0 : nv <= 32 ? 1 : nv <= 64 ? 2 : 3;   // activation box height
                 const uint32_t b_bytes = (16u << hb) * 128u;
                 const uint8_t* rec = a.arena + (size_t)slot * a.slot_bytes;
-                const uint8_t* codes = rec + a.off_codes + (size_t)mt * nc * C::BLK;
-                const uint8_t* sfa = rec + a.off_scales + (size_t)mt * atoms * 512;
+                // weight tiles: gate mt and up F/128 + mt, or down mt
+                const int tile0 = mt, tile1 = a.F / 128 + mt;
+                const uint8_t* codes0 = rec + a.off_codes + (size_t)tile0 * nc * C::BLK;
+                const uint8_t* codes1 = rec + a.off_codes + (size_t)tile1 * nc * C::BLK;
+                const uint8_t* sfa0 = rec + a.off_scales + (size_t)tile0 * atoms * 512;
+                const uint8_t* sfa1 = rec + a.off_scales + (size_t)tile1 * atoms * 512;
                 const uint8_t* sfb = a.b_scales + (size_t)(pos0 / BN) * atoms * 512;
                 for (int st = 0; st < nst; ++st, ++it) {
                     const int s = (int)(it % NS);
@@ -164,12 +164,18 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
                     const int at0 = 2 * c0;
                     const int ats = atoms - at0 < 2 * KCH ? atoms - at0 : 2 * KCH;
                     const uint32_t sf_bytes = (uint32_t)ats * 512u;
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)chunks * (C::BLK + b_bytes) + 2 * sf_bytes);
-                    bulk_load(As, codes + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK, &full[s]);
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)chunks * (C::NMAT * C::BLK + b_bytes) +
+                                                        (C::NMAT + 1) * sf_bytes);
+                    bulk_load(As, codes0 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK, &full[s]);
+                    bulk_load(SFs, sfa0 + (size_t)at0 * 512, sf_bytes, &full[s]);
+                    if (C::NMAT == 2) {
+                        bulk_load(As + KCH * C::BLK, codes1 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK,
+                                  &full[s]);
+                        bulk_load(SFs + C::SFA_MAT, sfa1 + (size_t)at0 * 512, sf_bytes, &full[s]);
+                    }
                     for (int q = 0; q < chunks; ++q)
                         tma_load_2d(Bs + q * C::B_CHUNK, &maps.b[hb], &full[s], (c0 + q) * 128, pos0);
-                    bulk_load(SFs, sfa + (size_t)at0 * 512, sf_bytes, &full[s]);
-                    bulk_load(SFs + C::SF_HALF, sfb + (size_t)at0 * 512, sf_bytes, &full[s]);
+                    bulk_load(SFs + C::NMAT * C::SFA_MAT, sfb + (size_t)at0 * 512, sf_bytes, &full[s]);
                 }
             }
         }
@@ -181,11 +187,11 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
             for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x, ++j) {
                 const int nv = a.work[item / a.m_tiles].z;
                 const int N = (nv + 15) & ~15;
-                const int b = j & 1;
-                const uint32_t u = j >> 1;
+                const int b = (int)(j % NBUF);
+                const uint32_t u = j / NBUF;
                 if (!mbar_wait(&acce[b], (u & 1) ^ 1, abort_flag)) break;
                 tc_fence_after();
-                const uint32_t dt = tmem + b * BN;
+                const uint32_t dt = tmem + b * C::ACC_COLS;
                 for (int st = 0; st < nst; ++st, ++it) {
                     const int s = (int)(it % NS);
                     const uint32_t r = it / NS;
@@ -194,20 +200,22 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
                     const int rem = (a.K - st * 256 * KCH) / 64;
                     const int ksteps = rem < 4 * KCH ? rem : 4 * KCH;      // MMAs of K = 64
                     const int ats = (ksteps + 1) / 2;                        // scale atoms used (2 MMAs each)
-                    const uint32_t sfc = tmem + 2 * BN + s * C::SF_COLS;
+                    const uint32_t sfc = tmem + NBUF * C::ACC_COLS + s * C::SF_COLS;
                     const uint32_t sfs = smem_u32(smem + C::OFF_SF + s * C::SF_BYTES);
-                    for (int q = 0; q < ats; ++q) {
-                        tc_cp_sf_atom(sfc + 4 * q, smem_desc_sf(sfs + 512 * q));
-                        tc_cp_sf_atom(sfc + 8 * KCH + 4 * q, smem_desc_sf(sfs + C::SF_HALF + 512 * q));
-                    }
+                    for (int m = 0; m <= C::NMAT; ++m)                       // weight atoms, then activation atoms
+                        for (int q = 0; q < ats; ++q)
+                            tc_cp_sf_atom(sfc + 8 * KCH * m + 4 * q, smem_desc_sf(sfs + C::SFA_MAT * m + 512 * q));
                     const uint32_t as = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
                     const uint32_t bs = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
+                    const uint32_t sfb = sfc + 8 * KCH * C::NMAT;
                     for (int kk = 0; kk < ksteps; ++kk) {
                         const int q = kk >> 2, kq = kk & 3;
-                        const int sfid = (kk & 1) * 2;
-                        tc_mma_mxf4(dt, smem_desc_sw128(as + q * C::BLK + kq * 32),
-                                    smem_desc_sw128(bs + q * C::B_CHUNK + kq * 32), idesc_mxf4(N, sfid, sfid),
-                                    sfc + (kk >> 1) * 4, sfc + 8 * KCH + (kk >> 1) * 4, (st | kk) != 0 ? 1u : 0u);
+                        const uint32_t idesc = idesc_mxf4(N, (kk & 1) * 2, (kk & 1) * 2);
+                        const uint64_t bdesc = smem_desc_sw128(bs + q * C::B_CHUNK + kq * 32);
+                        const uint32_t acc = (st | kk) != 0 ? 1u : 0u;
+                        for (int m = 0; m < C::NMAT; ++m)
+                            tc_mma_mxf4(dt + m * BN, smem_desc_sw128(as + (m * KCH + q) * C::BLK + kq * 32), bdesc,
+                                        idesc, sfc + 8 * KCH * m + (kk >> 1) * 4, sfb + (kk >> 1) * 4, acc);
                     }
                     tc_commit(&empty[s]);
                 }
@@ -216,65 +224,47 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 0..3)
-        float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
-        uint32_t j = 0, jc = 0;
-        bool ok_run = true;
-        for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x, ++j) {
+        uint32_t j = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
             const int4 w = a.work[item / a.m_tiles];
             const int mt = item % a.m_tiles;
             const int pos0 = w.y, nv = w.z;
-            const int b = j & 1;
-            const uint32_t u = j >> 1;
+            const int b = (int)(j % NBUF);
+            const uint32_t u = j / NBUF;
             if (!warp_wait(&accf[b], u & 1, abort_flag)) break;
             tc_fence_after();
-            const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16) + b * BN;
+            const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16) + b * C::ACC_COLS;
             if (MODE == 1) {
-                // rows 0-63: gate f0..f0+63 (warps 0, 1); rows 64-127: up (warps 2, 3)
-                for (int c0 = 0; c0 < nv; c0 += 16, ++jc) {
-                    uint32_t v[16];
-                    tc_ld_x16(trow + c0, v);
+                // lane of warp q holds gate and up of feature f0 + 32 q + lane: one 32-block per warp
+                const int fb = mt * 128 + warp * 32;
+                for (int c0 = 0; c0 < nv; c0 += 16) {
+                    uint32_t vg[16], vu[16];
+                    tc_ld_x16(trow + c0, vg);
+                    tc_ld_x16(trow + BN + c0, vu);
                     tc_wait_ld();
-                    if (warp >= 2) {
-                        if (!warp_wait(uread, (jc & 1) ^ 1, abort_flag)) { ok_run = false; break; }
-                        float* dst = xch + ((warp - 2) * 32 + lane) * C::XCH_STRIDE;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) dst[i] = __uint_as_float(v[i]);
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(uready);
-                    } else {
-                        if (!warp_wait(uready, jc & 1, abort_flag)) { ok_run = false; break; }
-                        const float* src = xch + (warp * 32 + lane) * C::XCH_STRIDE;
-                        const int f0 = mt * 64 + warp * 32;          // this warp's 32 features = one block
+                    for (int i = 0; i < 16; ++i) {
+                        if (c0 + i >= nv) break;                 // warp-uniform
+                        const float g = __uint_as_float(vg[i]);
+                        const float h = g / (1.0f + expf(-g)) * __uint_as_float(vu[i]);
+                        float amax = fabsf(h);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (c0 + i >= nv) break;                 // warp-uniform
-                            const float g = __uint_as_float(v[i]);
-                            const float h = g / (1.0f + expf(-g)) * src[i];
-                            float amax = fabsf(h);
-#pragma unroll
-                            for (int off = 16; off > 0; off >>= 1)
-                                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-                            const int X = mx_shared_exp(amax);
-                            const uint32_t code = e2m1_code(h, exp2_int(-X));
-                            const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, code, 1);
-                            const uint32_t byte = (code | (hi << 4)) & 0xFFu;
-                            const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
-                            const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
-                            const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 6);
-                            const int pos = pos0 + c0 + i;
-                            if ((lane & 7) == 0)
-                                *reinterpret_cast<uint32_t*>(a.hq + (size_t)pos * (a.F / 2) + f0 / 2 + (lane >> 3) * 4) =
-                                    byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-                            if (lane == 0) a.hsp[operand_scale_offset(pos, f0 / 32, BN, a.F)] = (uint8_t)(X + 127);
-                        }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(uread);
+                        for (int off = 16; off > 0; off >>= 1)
+                            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+                        const int X = mx_shared_exp(amax);
+                        const uint32_t code = e2m1_code(h, exp2_int(-X));
+                        const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+                        const uint32_t byte = (code | (hi << 4)) & 0xFFu;
+                        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
+                        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
+                        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 6);
+                        const int pos = pos0 + c0 + i;
+                        if ((lane & 7) == 0)
+                            *reinterpret_cast<uint32_t*>(a.hq + (size_t)pos * (a.F / 2) + fb / 2 + (lane >> 3) * 4) =
+                                byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                        if (lane == 0) a.hsp[operand_scale_offset(pos, fb / 32, BN, a.F)] = (uint8_t)(X + 127);
                     }
                 }
-                if (!ok_run) break;
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acce[b]);
             } else {
                 const int dr = mt * 128 + warp * 32 + lane;
                 for (int c0 = 0; c0 < nv; c0 += 16) {
@@ -288,10 +278,10 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
                         if (c0 + i < nv) a.Y[(size_t)pp * a.d + dr] = __uint_as_float(v[i]);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acce[b]);
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);
         }
     }
 
@@ -343,10 +333,10 @@ cudaError_t make_act_maps(CUtensorMap* m, const uint8_t* base, uint64_t row_byte
     return cudaSuccess;
 }
 
-template <int MODE, int BN, int NS, int KCH>
+template <int MODE, int BN, int NS, int KCH, int NBUF>
 cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& g, long max_items, cudaStream_t s) {
-    using C = Cfg<MODE, BN, NS, KCH>;
-    auto kern = ffn_gemm_kernel<MODE, BN, NS, KCH>;
+    using C = Cfg<MODE, BN, NS, KCH, NBUF>;
+    auto kern = ffn_gemm_kernel<MODE, BN, NS, KCH, NBUF>;
     static int occ_cache[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -373,11 +363,19 @@ cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& g, long max_items, 
 
 template <int MODE>
 cudaError_t launch_mode(const GemmMaps& maps, const GemmArgs& g, long max_items, int bn, cudaStream_t s) {
-    switch (bn) {
-        case 16: return launch_one<MODE, 16, 5, 2>(maps, g, max_items, s);
-        case 32: return launch_one<MODE, 32, 4, 2>(maps, g, max_items, s);
-        case 64: return launch_one<MODE, 64, 4, 2>(maps, g, max_items, s);
-        default: return launch_one<MODE, 128, 3, 2>(maps, g, max_items, s);
+    if constexpr (MODE == 1) {   // gate + up tiles per stage: 32 KB of weights at KCH = 1
+        switch (bn) {
+            case 16: return launch_one<MODE, 16, 5, 1, 2>(maps, g, max_items, s);
+            case 32: return launch_one<MODE, 32, 5, 1, 2>(maps, g, max_items, s);
+            case 64: return launch_one<MODE, 64, 5, 1, 2>(maps, g, max_items, s);
+            default: return launch_one<MODE, 128, 4, 1, 1>(maps, g, max_items, s);
+        }
+    }
+    else switch (bn) {      // one tile per stage: 32 KB of weights at KCH = 2
+        case 16: return launch_one<MODE, 16, 5, 2, 2>(maps, g, max_items, s);
+        case 32: return launch_one<MODE, 32, 5, 2, 2>(maps, g, max_items, s);
+        case 64: return launch_one<MODE, 64, 4, 2, 2>(maps, g, max_items, s);
+        default: return launch_one<MODE, 128, 3, 2, 2>(maps, g, max_items, s);
     }
 }
 
@@ -405,7 +403,7 @@ cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches
     g1.off_codes = ar.off_gu_codes;
     g1.off_scales = ar.off_gu_scales;
     g1.K = a.d;
-    g1.m_tiles = a.F / 64;
+    g1.m_tiles = a.F / 128;
     g1.b_scales = a.xsp;
     g1.hq = a.hq;
     g1.hsp = a.hsp;

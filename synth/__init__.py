@@ -116,7 +116,7 @@ def slot_record(d: int, ffn: int) -> dict:
     """
     def al(x, a=256):
         return (x + a - 1) // a * a
-    gu_c = (ffn // 64) * ((d + 255) // 256) * 16384      # tile-major code blocks (pack_codes)
+    gu_c = (2 * ffn // 128) * ((d + 255) // 256) * 16384   # tile-major code blocks (pack_codes)
     gu_s = 2 * ffn * d // 32
     dn_c = (d // 128) * ((ffn + 255) // 256) * 16384
     dn_s = d * ffn // 32
@@ -156,19 +156,15 @@ def expert_weights(seed: int, layer: int, expert: int, d: int, ffn: int) -> dict
     )
 
 
-def _tile_rows(R: int, gate_up: bool, ffn: int) -> np.ndarray:
-    """[tiles, 128] logical row of each tile row (gate/up: 64 gate rows then the matching 64 up rows)."""
-    if gate_up:
-        g = np.arange(ffn // 64)[:, None]
-        r = np.arange(128)[None, :]
-        return np.where(r < 64, 64 * g + r, ffn + 64 * g + (r - 64))
+def _tile_rows(R: int) -> np.ndarray:
+    """[tiles, 128] logical row of each tile row: tile g holds rows 128g..128g+127."""
     return np.arange(R).reshape(-1, 128)
 
 
-def pack_codes(codes: np.ndarray, gate_up: bool, ffn: int = 0) -> np.ndarray:
+def pack_codes(codes: np.ndarray) -> np.ndarray:
     """Code bytes [R, K/2] in the arena's tile-major block order.
 
-    For each 128-row tile (rows as in ``pack_scales``) and each chunk of 256
+    For each tile of 128 consecutive rows and each chunk of 256
     elements along K (128 bytes, zero-padded past the row end), one 16 KB block
     of 128 rows x 128 bytes; 16-byte piece c of tile row r is stored at piece
     c ^ (r % 8) of that row (the 128-byte swizzle). Blocks are stored tile by
@@ -176,7 +172,7 @@ def pack_codes(codes: np.ndarray, gate_up: bool, ffn: int = 0) -> np.ndarray:
     """
     R, Kh = codes.shape
     nkc = (Kh + 127) // 128
-    rows = _tile_rows(R, gate_up, ffn)
+    rows = _tile_rows(R)
     tiles = rows.shape[0]
     t = np.zeros((tiles, 128, nkc * 128), np.uint8)
     t[:, :, :Kh] = codes[rows]
@@ -189,16 +185,15 @@ def pack_codes(codes: np.ndarray, gate_up: bool, ffn: int = 0) -> np.ndarray:
     return np.ascontiguousarray(out.transpose(0, 2, 1, 3, 4)).reshape(-1)
 
 
-def pack_scales(scales: np.ndarray, gate_up: bool, ffn: int = 0) -> np.ndarray:
+def pack_scales(scales: np.ndarray) -> np.ndarray:
     """Scale bytes [R, K/32] in the arena's tile-atom order (the layout the arena record uses).
 
-    Rows are taken in 128-row tiles (gate/up: 64 gate rows f0..f0+63 then the 64
-    matching up rows ffn+f0..; down: 128 consecutive rows), and each tile's
-    scales in 512-byte atoms of 4 K-blocks: byte (r % 32) * 16 + (r // 32) * 4 + k
-    for tile row r and K-block 4a + k of atom a. Tiles, then atoms, are stored in order.
+    Rows are taken in tiles of 128 consecutive rows, and each tile's scales in
+    512-byte atoms of 4 K-blocks: byte (r % 32) * 16 + (r // 32) * 4 + k for
+    tile row r and K-block 4a + k of atom a. Tiles, then atoms, are stored in order.
     """
     R, Kb = scales.shape
-    rows = _tile_rows(R, gate_up, ffn)
+    rows = _tile_rows(R)
     t = scales[rows]                                   # [tiles, 128, Kb]
     t = t.reshape(t.shape[0], 4, 32, Kb // 4, 4)       # r = 32 j + r0 ; kb = 4 a + k
     return np.ascontiguousarray(t.transpose(0, 3, 2, 1, 4)).reshape(-1)
@@ -213,11 +208,11 @@ def expert_slot_bytes(seed: int, layer: int, expert: int, d: int, ffn: int) -> n
     rec = slot_record(d, ffn)
     w = expert_weights(seed, layer, expert, d, ffn)
     out = np.zeros(rec["slot_bytes"], dtype=np.uint8)
-    out[rec["off_gu_codes"]:rec["off_gu_codes"] + rec["gu_codes_bytes"]] = pack_codes(w["gu_codes"], True, ffn)
+    out[rec["off_gu_codes"]:rec["off_gu_codes"] + rec["gu_codes_bytes"]] = pack_codes(w["gu_codes"])
     out[rec["off_gu_scales"]:rec["off_gu_scales"] + rec["gu_scales_bytes"]] = \
-        pack_scales(w["gu_scales"], True, ffn)
-    out[rec["off_dn_codes"]:rec["off_dn_codes"] + rec["dn_codes_bytes"]] = pack_codes(w["dn_codes"], False)
-    out[rec["off_dn_scales"]:rec["off_dn_scales"] + rec["dn_scales_bytes"]] = pack_scales(w["dn_scales"], False)
+        pack_scales(w["gu_scales"])
+    out[rec["off_dn_codes"]:rec["off_dn_codes"] + rec["dn_codes_bytes"]] = pack_codes(w["dn_codes"])
+    out[rec["off_dn_scales"]:rec["off_dn_scales"] + rec["dn_scales_bytes"]] = pack_scales(w["dn_scales"])
     return out
 
 

@@ -38,18 +38,10 @@ struct Region {
     int gate_up;      // codes: 1 for the gate/up matrix
 };
 
-// Tile (128 rows) and tile row of a logical row: gate/up tiles are 64 gate rows
-// followed by the matching 64 up rows; down tiles are 128 consecutive rows.
-__device__ inline void tile_of(int64_t row, bool gate_up, int ffn, int64_t* tile, int64_t* tr) {
-    if (gate_up) {
-        const bool up = row >= ffn;
-        const int64_t f = up ? row - ffn : row;
-        *tile = f / 64;
-        *tr = (up ? 64 : 0) + f % 64;
-    } else {
-        *tile = row / 128;
-        *tr = row % 128;
-    }
+// Tile (128 consecutive rows) and tile row of a logical row.
+__device__ inline void tile_of(int64_t row, int64_t* tile, int64_t* tr) {
+    *tile = row / 128;
+    *tr = row % 128;
 }
 
 // Position of logical code byte `col` of `row` in the tile-major block order:
@@ -57,18 +49,17 @@ __device__ inline void tile_of(int64_t row, bool gate_up, int ffn, int64_t* tile
 // row), 16-byte piece c of tile row r at piece c ^ (r % 8).
 __device__ inline int64_t packed_code_offset(const Region& r, int64_t row, int64_t col) {
     int64_t tile, tr;
-    tile_of(row, r.gate_up != 0, r.ffn, &tile, &tr);
+    tile_of(row, &tile, &tr);
     const int64_t nkc = (r.kb + 127) / 128;
     const int64_t kc = col / 128, piece = (col % 128) / 16;
     return (tile * nkc + kc) * 16384 + tr * 128 + ((piece ^ (tr & 7)) * 16) + col % 16;
 }
 
 // Position of logical scale byte (row, k-block) in the arena's tile-atom order:
-// 128-row tiles (gate/up: 64 gate rows f0.. then the 64 up rows ffn+f0..),
-// 512-byte atoms of 4 k-blocks, byte (r % 32) * 16 + (r / 32) * 4 + kb % 4.
+// 128-row tiles, 512-byte atoms of 4 k-blocks, byte (r % 32) * 16 + (r / 32) * 4 + kb % 4.
 __device__ inline int64_t packed_scale_offset(const Region& r, int64_t row, int kb) {
     int64_t tile, tr;
-    tile_of(row, r.scales == 1, r.ffn, &tile, &tr);
+    tile_of(row, &tile, &tr);
     const int64_t atoms_per_tile = r.kb / 4;
     return (tile * atoms_per_tile + kb / 4) * 512 + (tr % 32) * 16 + (tr / 32) * 4 + kb % 4;
 }
