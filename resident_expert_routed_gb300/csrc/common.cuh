@@ -73,6 +73,35 @@ MOE_DEV size_t operand_scale_offset(int pos, int kb, int bn, int K) {
     return ((size_t)tile * (K / 128) + (kb >> 2)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3);
 }
 
+// Inclusive prefix sum of one 64-bit value per thread across the whole block
+// (blockDim.x a multiple of 32, at most 1024). `scratch` is shared memory of
+// 32 values; *total receives the block's sum. Contains __syncthreads().
+MOE_DEV unsigned long long block_inclusive_scan_u64(unsigned long long v, unsigned long long* scratch,
+                                                    unsigned long long* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long o = __shfl_up_sync(0xFFFFFFFFu, v, off);
+        if (lane >= off) v += o;
+    }
+    __syncthreads();                       // scratch may still be read by a previous call
+    if (lane == 31) scratch[wid] = v;
+    __syncthreads();
+    if (wid == 0) {
+        unsigned long long s = lane < nw ? scratch[lane] : 0ull;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned long long o = __shfl_up_sync(0xFFFFFFFFu, s, off);
+            if (lane >= off) s += o;
+        }
+        scratch[lane] = s;
+    }
+    __syncthreads();
+    if (wid > 0) v += scratch[wid - 1];
+    *total = scratch[nw - 1];
+    return v;
+}
+
 MOE_DEV void record_error(uint32_t* err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }

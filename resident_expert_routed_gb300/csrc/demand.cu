@@ -47,14 +47,45 @@ __device__ __forceinline__ unsigned long long miss_key(const float* M, int f, fl
     return ((unsigned long long)__float_as_uint(m) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)f);
 }
 
+constexpr int MAX_CAND = 2048;
+
 __global__ void __launch_bounds__(1024) hot_miss_select(float* __restrict__ M, int n, float thr, int cap,
                                                         int32_t* __restrict__ out_flat,
                                                         float* __restrict__ out_share, int32_t* __restrict__ n_out) {
     __shared__ unsigned long long wbest[32];
     __shared__ unsigned long long picked;
     __shared__ int count;
-    if (threadIdx.x == 0) { picked = ~0ull; count = 0; }
+    __shared__ int n_cand;
+    __shared__ unsigned long long cand[MAX_CAND];
+    if (threadIdx.x == 0) { picked = ~0ull; count = 0; n_cand = 0; }
     __syncthreads();
+    // usual case: few shares pass the threshold; rank them directly by their keys (all distinct)
+    for (int f = threadIdx.x; f < n; f += blockDim.x) {
+        const unsigned long long key = miss_key(M, f, thr);
+        if (key) {
+            const int i = atomicAdd(&n_cand, 1);
+            if (i < MAX_CAND) cand[i] = key;
+        }
+    }
+    __syncthreads();
+    const int C = n_cand;
+    if (C <= MAX_CAND) {
+        for (int i = threadIdx.x; i < C; i += blockDim.x) {
+            const unsigned long long key = cand[i];
+            int rank = 0;
+            for (int q = 0; q < C; ++q) rank += cand[q] > key;
+            if (rank < cap) {
+                out_flat[rank] = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+                out_share[rank] = __uint_as_float((uint32_t)(key >> 32));
+            }
+        }
+        if (threadIdx.x == 0) count = C < cap ? C : cap;
+        __syncthreads();
+        if (threadIdx.x == 0) *n_out = count;
+        for (int f = threadIdx.x; f < n; f += blockDim.x) M[f] = 0.0f;
+        return;
+    }
+    // many candidates: `cap` block-wide arg-max rounds, each below the previous pick
     for (int j = 0; j < cap; ++j) {
         const unsigned long long prev = picked;
         unsigned long long best = 0ull;

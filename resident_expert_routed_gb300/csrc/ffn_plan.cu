@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restri
                                                          int4* __restrict__ work, int32_t* __restrict__ n_work,
                                                          uint32_t* err) {
     extern __shared__ int32_t cnt[];
-    __shared__ unsigned long long part[PLAN_THREADS];
+    __shared__ unsigned long long scan_scratch[32];
     const int tid = threadIdx.x;
     for (int i = tid; i < S; i += PLAN_THREADS) cnt[i] = 0;
     __syncthreads();
@@ -49,21 +49,15 @@ __global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restri
     };
     unsigned long long local = 0;
     for (int i = b0; i < b1; ++i) local += packed(cnt[i]);
-    part[tid] = local;
-    __syncthreads();
-    for (int off = 1; off < PLAN_THREADS; off <<= 1) {      // Hillis-Steele inclusive scan
-        unsigned long long v = tid >= off ? part[tid - off] : 0ull;
-        __syncthreads();
-        part[tid] += v;
-        __syncthreads();
-    }
-    unsigned long long run = tid > 0 ? part[tid - 1] : 0ull;
+    unsigned long long total = 0;
+    const unsigned long long incl = block_inclusive_scan_u64(local, scan_scratch, &total);
+    unsigned long long run = incl - local;
     for (int i = b0; i < b1; ++i) {
         seg[i] = (int32_t)(run & 0xFFFFFFFFull);
         tile_off[i] = (int32_t)(run >> 32);
         run += packed(cnt[i]);
     }
-    if (tid == PLAN_THREADS - 1) *n_work = (int32_t)(part[tid] >> 32);
+    if (tid == 0) *n_work = (int32_t)(total >> 32);
     __syncthreads();
     for (int p = tid; p < P; p += PLAN_THREADS) {
         const int s = sel_slot[p];

@@ -30,26 +30,31 @@ __global__ void __launch_bounds__(256) router_logits_partial(const uint16_t* __r
     const int kbeg = blockIdx.z * kslice, kend = kbeg + kslice;
     float acc[4][4] = {};
     const int lr = tid >> 2, lc = (tid & 3) * 8;   // loader: row, 8 consecutive k
+    const int tl = t0 + lr, el = e0 + lr;
+    // registers hold the next K tile while the current one is multiplied
+    uint4 xv = make_uint4(0, 0, 0, 0);
+    float4 wa = make_float4(0, 0, 0, 0), wb = wa;
+    auto fetch = [&](int k0) {
+        xv = make_uint4(0, 0, 0, 0);
+        wa = make_float4(0, 0, 0, 0);
+        wb = wa;
+        if (tl < T) xv = *reinterpret_cast<const uint4*>(x + (size_t)tl * d + k0 + lc);
+        if (el < E) {
+            wa = *reinterpret_cast<const float4*>(W + (size_t)el * d + k0 + lc);
+            wb = *reinterpret_cast<const float4*>(W + (size_t)el * d + k0 + lc + 4);
+        }
+    };
+    fetch(kbeg);
     for (int k0 = kbeg; k0 < kend; k0 += BK) {
-        {   // x tile: 64 tokens x 32 bf16 -> xs[k][t]
-            int t = t0 + lr;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (t < T) v = *reinterpret_cast<const uint4*>(x + (size_t)t * d + k0 + lc);
-            const uint16_t* h = reinterpret_cast<const uint16_t*>(&v);
+        {   // x tile: 64 tokens x 32 bf16 -> xs[k][t]; W tile: 64 experts x 32 fp32 -> ws[k][e]
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(&xv);
 #pragma unroll
             for (int i = 0; i < 8; ++i) xs[lc + i][lr] = bf16_bits_to_float(h[i]);
-        }
-        {   // W tile: 64 experts x 32 fp32 -> ws[k][e]
-            int e = e0 + lr;
-            float4 a = make_float4(0, 0, 0, 0), b = a;
-            if (e < E) {
-                a = *reinterpret_cast<const float4*>(W + (size_t)e * d + k0 + lc);
-                b = *reinterpret_cast<const float4*>(W + (size_t)e * d + k0 + lc + 4);
-            }
-            ws[lc + 0][lr] = a.x; ws[lc + 1][lr] = a.y; ws[lc + 2][lr] = a.z; ws[lc + 3][lr] = a.w;
-            ws[lc + 4][lr] = b.x; ws[lc + 5][lr] = b.y; ws[lc + 6][lr] = b.z; ws[lc + 7][lr] = b.w;
+            ws[lc + 0][lr] = wa.x; ws[lc + 1][lr] = wa.y; ws[lc + 2][lr] = wa.z; ws[lc + 3][lr] = wa.w;
+            ws[lc + 4][lr] = wb.x; ws[lc + 5][lr] = wb.y; ws[lc + 6][lr] = wb.z; ws[lc + 7][lr] = wb.w;
         }
         __syncthreads();
+        if (k0 + BK < kend) fetch(k0 + BK);
 #pragma unroll 8
         for (int kk = 0; kk < BK; ++kk) {
             float a[4], b[4];
@@ -103,9 +108,27 @@ __global__ void __launch_bounds__(256) route_select(const float* __restrict__ pa
     int slot[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) lg[i] = 0.0f;
-    // K slices summed in slice order (deterministic); each slice issues VPL independent loads
-    for (int z = 0; z < splits; ++z) {
-        const float* pz = partial + ((size_t)z * T + t) * E;
+    // K slices summed in slice order (deterministic); U slices' loads are issued together
+    constexpr int U = VPL >= 16 ? 1 : 64 / (VPL * 2);
+    int zs = 0;
+    for (; zs + U <= splits; zs += U) {
+        float v[U][VPL];
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const float* pz = partial + ((size_t)(zs + q) * T + t) * E;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                const int e = lane + 32 * i;
+                v[q][i] = e < E ? pz[e] : 0.0f;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < U; ++q)
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) lg[i] += v[q][i];
+    }
+    for (; zs < splits; ++zs) {
+        const float* pz = partial + ((size_t)zs * T + t) * E;
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
             const int e = lane + 32 * i;

@@ -143,6 +143,25 @@ def test_demand_and_heavy_miss_parity():
         assert not Mi.any()                                       # reset for the next step
 
 
+@pytest.mark.parametrize("L,E,cap,frac", [(12, 256, 16, 0.9), (60, 256, 16, 0.05), (2, 16, 0, 0.5)])
+def test_heavy_miss_candidate_counts(L, E, cap, frac):
+    # few candidates (ranked directly) and more than 2048 (block-wide rounds): same list as the oracle
+    rng = np.random.default_rng(L * E + cap)
+    M = np.where(rng.random((L, E)) < frac, rng.random((L, E)).astype(np.float32), 0).astype(np.float32)
+    M[0, :4] = M[0, 4]                         # ties: the lower flat index first
+    Mi = torch.from_numpy(M).cuda()
+    flat = torch.full((max(cap, 1),), -7, dtype=torch.int32, device="cuda")
+    share = torch.zeros(max(cap, 1), dtype=torch.float32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_hot_miss_select(Mi, 0.01, cap, flat, share, n)
+    torch.cuda.synchronize()
+    ids_ref, sh_ref = oracle.hot_miss_select(M.astype(np.float64), 0.01, cap)
+    assert int(n.item()) == len(ids_ref)
+    assert list(flat.cpu().numpy()[:len(ids_ref)]) == list(ids_ref)
+    assert np.array_equal(share.cpu().numpy()[:len(ids_ref)], sh_ref.astype(np.float32))
+    assert not Mi.any()
+
+
 def test_heavy_miss_hand_worked_on_gpu():
     import json, os
     g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")))["heavy_miss"]
