@@ -122,6 +122,29 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
                               void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * moe_route_resident without a caller workspace (the paper has no counterpart:
+ * this exists for callers of this library that cannot allocate device memory
+ * when they route -- e.g. a serving loop whose memory budget was fixed at
+ * start-up, or a plug-in whose host framework owns every allocation -- since
+ * cudaMalloc can also synchronise the device). Same arguments, results and
+ * limits as moe_route_resident, minus the workspace; it allocates nothing.
+ * The split-K partial logits live in one fixed device array of 4 MiB
+ * (2^20 fp32) inside the library, held by every GPU that loads the library
+ * until the process exits; a call whose partials would not fit
+ * (splits * T * E > 2^20, e.g. T above 128 for E = 256) returns
+ * MOE_EUNSUPPORTED. Every call on a device shares that array: calls whose
+ * work overlaps on the GPU (different streams without ordering) race and
+ * corrupt each other's results. Each call writes every element it reads, so
+ * nothing needs clearing between calls. The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.
+ */
+moe_status moe_route_resident_noalloc(const void* hidden_bf16, const float* w_router, const float* bias,
+                                      const int32_t* slot_of, int T, int d, int E, int k,
+                                      int32_t* want_e, float* want_s,
+                                      int32_t* sel_e, int32_t* sel_slot, float* sel_w, void* stream);
+
+/*
  * Demand accumulation (README item 1: every wanted pick, resident or not,
  * recorded per (layer, expert) weighted by its routing score; item 2: the
  * demand of a substituted pick still counts) and the miss share (item 3: a

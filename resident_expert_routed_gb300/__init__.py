@@ -27,7 +27,7 @@ MOE_OK, MOE_EINVAL, MOE_ECUDA, MOE_ENOMEM, MOE_ETIMEOUT, MOE_EDEVICE, MOE_EUNSUP
 MOE_DEV_BAD_SLOT, MOE_DEV_NAN_SCALE, MOE_DEV_TIMEOUT, MOE_DEV_BAD_TABLE, MOE_DEV_RESIDENT = 0x1, 0x2, 0x4, 0x8, 0x10
 
 # Every symbol the header declares (checked by the CPU test suite).
-EXPORTS = ("moe_route_resident", "moe_demand_accumulate", "moe_hot_miss_select", "moe_expert_ffn_mxfp4",
+EXPORTS = ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accumulate", "moe_hot_miss_select", "moe_expert_ffn_mxfp4",
            "moe_arena_replan", "moe_ring_install", "moe_workspace_bytes", "moe_replan_workspace_bytes",
            "moe_device_status", "moe_status_str", "moe_kernel_launches", "moe_profile_enable",
            "moe_profile_kernel_count", "moe_profile_read", "moe_profile_reset")
@@ -60,6 +60,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         raise ImportError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
     L = ctypes.CDLL(path)
     L.moe_route_resident.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_route_resident_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]
     L.moe_demand_accumulate.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]
     L.moe_hot_miss_select.argtypes = [_P, _I, _I, _F, _I, _P, _P, _P, _P]
     L.moe_expert_ffn_mxfp4.argtypes = [_P, _P, _P, ctypes.POINTER(MoeArena), _I, _I, _P, _P, _SZ, _P]
@@ -81,7 +82,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                    ctypes.POINTER(ctypes.c_double)]
     L.moe_profile_reset.restype = None
     L.moe_profile_reset.argtypes = []
-    for name in ("moe_route_resident", "moe_demand_accumulate", "moe_hot_miss_select", "moe_expert_ffn_mxfp4",
+    for name in ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accumulate", "moe_hot_miss_select",
+                 "moe_expert_ffn_mxfp4",
                  "moe_arena_replan", "moe_ring_install", "moe_device_status", "moe_profile_enable",
                  "moe_profile_read"):
         L[name].restype = _I
@@ -145,6 +147,21 @@ def moe_route_resident(hidden_bf16, w_router, bias, slot_of, k, want_e, want_s, 
         _ptr(hidden_bf16), _ptr(w_router), _ptr(bias), _ptr(slot_of), T, d, E, k, _ptr(want_e), _ptr(want_s),
         _ptr(sel_e), _ptr(sel_slot), _ptr(sel_w), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def moe_route_resident_noalloc(hidden_bf16, w_router, bias, slot_of, k, want_e, want_s, sel_e, sel_slot, sel_w,
+                               stream=None) -> None:
+    """moe_route_resident for callers that cannot allocate device memory: no workspace argument.
+
+    The partial logits go to a fixed 4 MiB array inside the library (shared by
+    all calls on a device, so calls must not overlap on the GPU); sizes whose
+    partials do not fit raise MoeError with MOE_EUNSUPPORTED.
+    """
+    T, d = hidden_bf16.shape
+    E = w_router.shape[0]
+    _check("moe_route_resident_noalloc", load().moe_route_resident_noalloc(
+        _ptr(hidden_bf16), _ptr(w_router), _ptr(bias), _ptr(slot_of), T, d, E, k, _ptr(want_e), _ptr(want_s),
+        _ptr(sel_e), _ptr(sel_slot), _ptr(sel_w), _stream(stream)))
 
 
 def moe_demand_accumulate(want_e, want_s, slot_of, layer, demand, miss_max, stream=None) -> None:

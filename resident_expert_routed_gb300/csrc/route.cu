@@ -13,6 +13,8 @@
 //                          warp-shuffle arg-max rounds.
 // The K split keeps >= ~256 CTAs streaming W_r at decode sizes; the partials
 // are small and stay in L2.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace {
@@ -228,4 +230,64 @@ cudaError_t launch_route(const RouteLaunch& a, cudaStream_t s) {
     moe_prof_end(MK_ROUTE_SELECT, s);
     moe_count_launches(2);
     return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ routing without a caller workspace
+//
+// Some callers cannot allocate device memory at the point where they route:
+// code running under an allocator that must not grow (a serving loop that
+// fixed its memory budget at start-up, a plug-in whose host framework owns all
+// allocations), or code that may not synchronise the device, which a cudaMalloc
+// can do. For them the split-K partial logits live in this fixed array instead
+// of a caller-provided workspace. It is part of the library's image, so every
+// GPU that loads the library holds its 4 MiB until the process exits.
+namespace {
+
+constexpr size_t kNoAllocPartials = size_t(1) << 20;          // fp32 partial logits: 4 MiB
+static __device__ __align__(256) float g_route_partials[kNoAllocPartials];
+
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[64] = {};
+
+// Device address of the array for the current device, looked up once per device.
+cudaError_t noalloc_partials(float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_route_partials);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_route_resident_noalloc(const void* hidden_bf16, const float* w_router, const float* bias,
+                                                 const int32_t* slot_of, int T, int d, int E, int k,
+                                                 int32_t* want_e, float* want_s, int32_t* sel_e, int32_t* sel_slot,
+                                                 float* sel_w, void* stream) {
+    if (!hidden_bf16 || !w_router || !slot_of || !want_e || !want_s || !sel_e || !sel_slot || !sel_w)
+        return MOE_EINVAL;
+    if (T < 1 || d < 32 || d % 32 || E < 1 || k < 1 || k > 32 || k > E) return MOE_EINVAL;
+    if (E > 1024) return MOE_EUNSUPPORTED;
+    const int splits = route_splits(T, E, d);
+    if ((size_t)splits * T * E > kNoAllocPartials) return MOE_EUNSUPPORTED;   // beyond the fixed array
+    float* partials = nullptr;
+    if (noalloc_partials(&partials) != cudaSuccess) return MOE_ECUDA;
+    RouteLaunch a{};
+    a.x = static_cast<const uint16_t*>(hidden_bf16);
+    a.w = w_router;
+    a.bias = bias;
+    a.slot_of = slot_of;
+    a.T = T; a.d = d; a.E = E; a.k = k;
+    a.splits = splits;
+    a.want_e = want_e; a.want_s = want_s; a.sel_e = sel_e; a.sel_slot = sel_slot; a.sel_w = sel_w;
+    a.partial = partials;      // every element read below is written earlier in the same call
+    return launch_route(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
