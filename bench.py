@@ -153,6 +153,19 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) for r in rows if num(r[3]) is not None), default=None)}
 
 
+def measured_traffic(kernel_json: str):
+    """DRAM bytes per launch from the committed ncu capture, or None if the kernel source changed since."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", kernel_json)
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p))
+    src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+    if hashlib.sha256(src).hexdigest()[:16] != rec["source_sha256_prefix"]:
+        return None
+    return rec["dram_bytes_read"] + rec["dram_bytes_write"]
+
+
 def flush_l2(scratch):
     scratch.add_(1)
 
@@ -364,7 +377,8 @@ def run_ours(args, rank, ws, local):
     u_mean = float(np.mean(slots_used))
     achieved = u_mean * gate_up_bytes / (gu[1] / gu[0] / 1000.0) / 1e9
     roofline = {"bound": "hbm", "kernel": "ffn_gemm_gate_up", "achieved": achieved, "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                "traffic": measured_traffic("ffn_gemm_gate_up_decode_T64.json"),
                 "peak_source": f"{pk['source']} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                 if pk["source"] == "measured" else "fallback 6800 GB/s",
                 "algorithmic_bytes_per_launch": u_mean * gate_up_bytes,
