@@ -1,0 +1,199 @@
+"""Multi-step GPU runs against the oracle: the hot-read ring and the shared arena.
+
+GLM-like layer: between steps, 64 seeded non-resident experts are installed
+in the ring slots (FIFO) and their bytes written; routing and the FFN are then
+checked against the oracle on that step's table (README item 3: ring slots on
+top of the budget, routable from the step after).
+
+Full decode step: 60 layers share one arena of 10,000 main + 64 ring slots;
+each step routes 2 tokens through all layers, records demand, takes the
+step's heavy-miss list and installs it in the ring; after the steps the arena
+is re-planned from the demand history (README item 1). Every layer's routing,
+the heavy-miss lists, the demand table, sampled FFN outputs and the re-plan
+are checked; the oracle always sees the table the GPU used (a snapshot), so
+near-ties cannot cascade across steps.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.cases import ffn_within_tolerance, hidden_dev, near_tie_tokens, to_dev
+
+pytestmark = pytest.mark.gpu
+
+moe = pytest.importorskip("resident_expert_routed_gb300")
+from resident_expert_routed_gb300.layer import LayerBuffers, layer_step, step_end  # noqa: E402
+
+
+def _arena(cfg, n_slots, owner):
+    rec = synth.slot_record(cfg.d, cfg.ffn)
+    buf = torch.zeros(n_slots * rec["slot_bytes"], dtype=torch.uint8, device="cuda")
+    synth.fill_slots_device(buf, cfg.d, cfg.ffn, cfg.seed, cfg.E, to_dev(owner.astype(np.int32)))
+    return moe.Arena(buf, rec["slot_bytes"], n_slots, cfg.d, cfg.ffn, rec["off_gu_codes"], rec["off_gu_scales"],
+                     rec["off_dn_codes"], rec["off_dn_scales"])
+
+
+def _fill(arena, cfg, slots, flats):
+    synth.fill_slots_device(arena.buf, cfg.d, cfg.ffn, cfg.seed, cfg.E, to_dev(np.asarray(flats, np.int32)),
+                            slots=to_dev(np.asarray(slots, np.int32)))
+
+
+def _check_routing(ref, buf, slot_of, k, E):
+    """Routing of one layer call against the oracle (near-tie tokens excluded)."""
+    sel = buf.sel_e.cpu().numpy()
+    want = buf.want_e.cpu().numpy()
+    slot = buf.sel_slot.cpu().numpy()
+    tie_s = near_tie_tokens(ref["scores"], slot_of >= 0, k)
+    tie_w = near_tie_tokens(ref["scores"], np.ones(E, bool), k)
+    for t in range(sel.shape[0]):
+        if not tie_w[t]:
+            assert set(want[t]) == set(ref["want_e"][t])
+        if not tie_s[t]:
+            assert set(sel[t]) == set(ref["sel_e"][t])
+        assert np.array_equal(slot[t], np.where(sel[t] >= 0, slot_of[np.maximum(sel[t], 0)], -1))
+    return sel, slot
+
+
+def _oracle_ffn(cfg, x, sel_slot, sel_w, owner):
+    used = sorted({int(s) for s in sel_slot.ravel() if s >= 0})
+    idx = {s: i for i, s in enumerate(used)}
+    sel_u = np.vectorize(lambda s: idx.get(int(s), -1))(sel_slot).astype(np.int32)
+    ex = [synth.expert_weights(cfg.seed, int(owner[s]) // cfg.E, int(owner[s]) % cfg.E, cfg.d, cfg.ffn) for s in used]
+    return oracle.ffn(x, sel_u, sel_w.astype(np.float64), ex, cfg.d, cfg.ffn)
+
+
+def test_glm_layer_with_ring_refills():
+    cfg, T, steps = synth.GLM, 16, 3
+    W = synth.router_weights(cfg.seed, cfg.E, cfg.d)
+    b = synth.router_bias(cfg.seed, cfg.E, cfg.sigma)
+    res = synth.resident_set(cfg, b)
+    n_slots = cfg.resident + cfg.n_ring
+    slot_of = synth.slot_table(cfg, res, cfg.resident)
+    owner = np.full(n_slots, -1, np.int32)
+    owner[slot_of[res]] = res
+    b = synth.drifted_bias(cfg, b)                        # the tide moved: misses happen
+    arena = _arena(cfg, n_slots, owner)
+    buf = LayerBuffers(T, cfg.k, cfg.E, cfg.d, cfg.ffn, n_slots)
+    so_d, ow_d = to_dev(slot_of), to_dev(owner)
+    Wd, bd = to_dev(W), to_dev(b)
+    demand = torch.zeros((1, cfg.E), dtype=torch.int64, device="cuda")
+    miss = torch.zeros((1, cfg.E), dtype=torch.float32, device="cuda")
+    ring_ptr = 0
+    for step in range(steps):
+        if step > 0:                                      # refill the ring between steps
+            cand = synth.ring_candidates(cfg, step, slot_of, cfg.n_ring)
+            slots = []
+            for f in cand:
+                rs = cfg.resident + ring_ptr % cfg.n_ring
+                ring_ptr += 1
+                moe.moe_ring_install(so_d, ow_d, rs, int(f))
+                assert oracle.ring_install(slot_of, owner, rs, int(f)) == 0
+                slots.append(rs)
+            _fill(arena, cfg, slots, cand)
+            torch.cuda.synchronize()
+            assert np.array_equal(so_d.cpu().numpy(), slot_of) and np.array_equal(ow_d.cpu().numpy(), owner)
+            assert moe.moe_device_status() == (moe.MOE_OK, 0)
+        x = synth.hidden_bf16(cfg.seed, T, cfg.d, stream=200 + step)
+        out = layer_step(hidden_dev(x), Wd, bd, so_d, arena, demand, miss, 0, buf)
+        step_end(miss, buf)
+        torch.cuda.synchronize()
+        ref = oracle.route(x, W, b, slot_of, cfg.k)
+        sel, sel_slot = _check_routing(ref, buf, slot_of, cfg.k, cfg.E)
+        if step > 0:
+            assert (sel_slot >= cfg.resident).any()       # ring experts are routed to
+        rows = np.arange(0, T, 5)
+        exp = _oracle_ffn(cfg, x[rows], sel_slot[rows], buf.sel_w.cpu().numpy()[rows], owner)
+        ok, fro, mx = ffn_within_tolerance(out.cpu().numpy()[rows].astype(np.float64), exp)
+        assert ok, (step, fro, mx)
+    del arena
+
+
+def test_full_decode_step_shared_arena_replan():
+    cfg, T, steps = synth.FULL, 2, 6
+    L, E = cfg.L, cfg.E
+    n_slots = cfg.n_main + cfg.n_ring
+    slot_of, owner = synth.full_initial_arena(cfg)
+    Ws = [synth.router_weights(cfg.seed, E, cfg.d, layer) for layer in range(L)]
+    bs = [synth.router_bias(cfg.seed, E, cfg.sigma, layer) for layer in range(L)]
+    arena = _arena(cfg, n_slots, owner)
+    W_d = to_dev(np.stack(Ws))
+    b_d = to_dev(np.stack(bs))
+    so_d, ow_d = to_dev(slot_of), to_dev(owner)
+    demand = torch.zeros((L, E), dtype=torch.int64, device="cuda")
+    miss = torch.zeros((L, E), dtype=torch.float32, device="cuda")
+    buf = LayerBuffers(T, cfg.k, E, cfg.d, cfg.ffn, n_slots)
+    Dref = np.zeros((L, E))
+    adds = np.zeros((L, E))
+    ring_ptr = 0
+    ffn_samples = {(0, 0), (2, 31), (5, 59)}
+    for step in range(steps):
+        Mref = np.zeros((L, E))
+        for layer in range(L):
+            x = synth.hidden_bf16(cfg.seed, T, cfg.d, stream=step * L + layer)
+            so_l = slot_of[layer * E:(layer + 1) * E]
+            out = layer_step(hidden_dev(x), W_d[layer], b_d[layer], so_d[layer * E:(layer + 1) * E], arena, demand,
+                             miss, layer, buf)
+            torch.cuda.synchronize()
+            ref = oracle.route(x, Ws[layer], bs[layer], so_l, cfg.k)
+            sel, sel_slot = _check_routing(ref, buf, so_l, cfg.k, E)
+            want = buf.want_e.cpu().numpy()
+            ws = np.take_along_axis(ref["scores"], want.astype(np.int64), axis=1)
+            oracle.demand(want, ws, so_l, layer, Dref, Mref)
+            np.add.at(adds[layer], want.ravel(), 1)
+            if (step, layer) in ffn_samples:
+                exp = _oracle_ffn(cfg, x, sel_slot, buf.sel_w.cpu().numpy(), owner)
+                ok, fro, mx = ffn_within_tolerance(out.cpu().numpy().astype(np.float64), exp)
+                assert ok, (step, layer, fro, mx)
+        flat, share, n = step_end(miss, buf)
+        torch.cuda.synchronize()
+        got = list(flat.cpu().numpy()[:int(n.item())])
+        ids_ref, _ = oracle.hot_miss_select(Mref, 0.2, 16)
+        cand = np.sort(Mref.ravel()[Mref.ravel() >= 0.2])[::-1]
+        if not (len(cand) > 16 and abs(cand[15] - cand[16]) <= 1e-5 * cand[15]) and \
+                not np.any(np.abs(Mref - 0.2) <= 2e-6):
+            assert got == list(ids_ref), (step, got, list(ids_ref))
+        slots = []
+        for f in got:                                     # the step's heavy misses go into the ring
+            rs = cfg.n_main + ring_ptr % cfg.n_ring
+            ring_ptr += 1
+            moe.moe_ring_install(so_d, ow_d, rs, int(f))
+            assert oracle.ring_install(slot_of, owner, rs, int(f)) == 0
+            slots.append(rs)
+        if slots:
+            _fill(arena, cfg, slots, got)
+        torch.cuda.synchronize()
+        assert np.array_equal(so_d.cpu().numpy(), slot_of)
+    assert ring_ptr > 0                                   # the drift-free random arena misses heavily
+    Dg = demand.cpu().numpy().astype(np.float64) / 2.0 ** 40
+    assert np.all(np.abs(Dg - Dref) <= 1e-5 * Dref + adds * 2.0 ** -41 + 1e-15)
+
+    # re-plan the shared arena from the GPU's demand table; the oracle re-plans the same table
+    so_ref, ow_ref, loads_ref = oracle.replan(Dg * 2.0 ** 40, cfg.n_main, slot_of, owner)
+    loads = torch.full((cfg.n_main,), -1, dtype=torch.int32, device="cuda")
+    nl = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(moe.moe_replan_workspace_bytes(L, E), dtype=torch.uint8, device="cuda")
+    moe.moe_arena_replan(demand, cfg.n_main, so_d, ow_d, loads, nl, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == (moe.MOE_OK, 0)
+    assert np.array_equal(ow_d.cpu().numpy(), ow_ref) and np.array_equal(so_d.cpu().numpy(), so_ref)
+    n_loads = int(nl.item())
+    assert n_loads == len(loads_ref) > 0
+    assert np.array_equal(loads.cpu().numpy()[:n_loads], loads_ref)
+    _fill(arena, cfg, loads_ref, ow_ref[loads_ref])       # refill the slots given to newcomers
+
+    # one more step on the re-planned arena: routing and FFN of a layer that gained experts
+    layer = int(ow_ref[loads_ref[0]]) // E
+    x = synth.hidden_bf16(cfg.seed, T, cfg.d, stream=steps * L + layer)
+    so_l = so_ref[layer * E:(layer + 1) * E]
+    out = layer_step(hidden_dev(x), W_d[layer], b_d[layer], so_d[layer * E:(layer + 1) * E], arena, demand, miss,
+                     layer, buf)
+    torch.cuda.synchronize()
+    ref = oracle.route(x, Ws[layer], bs[layer], so_l, cfg.k)
+    sel, sel_slot = _check_routing(ref, buf, so_l, cfg.k, E)
+    exp = _oracle_ffn(cfg, x, sel_slot, buf.sel_w.cpu().numpy(), ow_ref)
+    ok, fro, mx = ffn_within_tolerance(out.cpu().numpy().astype(np.float64), exp)
+    assert ok, (fro, mx)
+    del arena
+    torch.cuda.empty_cache()
