@@ -6,6 +6,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp4.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -52,17 +53,22 @@ MOE_DEV int mx_shared_exp(float amax) {
     return X < -127 ? -127 : (X > 127 ? 127 : X);
 }
 
-// Round |a| to the e2m1 grid {0,.5,1,1.5,2,3,4,6}: nearest, ties to the even
-// code, saturating at 6. Midpoints between codes c and c+1 round up when c is
-// odd (>=) and down when c is even (>).
-MOE_DEV uint32_t e2m1_mag_code(float a) {
-    return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) + (uint32_t)(a >= 1.75f) +
-           (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
+// Two values (already divided by their block scale) to one byte of e2m1 codes,
+// the first in the low nibble: round to nearest, ties to the even code,
+// saturating at +-6 (CUDA's fp4 conversion; it agrees value for value with
+// the OCP rule the oracle spells out, only the sign bit of a zero may differ).
+MOE_DEV uint32_t e2m1x2(float lo, float hi) {
+    return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(lo, hi), __NV_E2M1, cudaRoundNearest);
 }
 
-MOE_DEV uint32_t e2m1_code(float v, float inv_scale) {
-    return e2m1_mag_code(fabsf(v * inv_scale)) | (v < 0.0f ? 8u : 0u);
+// Eight values to one 32-bit word of e2m1 codes (element 0 in the lowest nibble).
+MOE_DEV uint32_t e2m1x8(const float* v, float inv_scale) {
+    return e2m1x2(v[0] * inv_scale, v[1] * inv_scale) | (e2m1x2(v[2] * inv_scale, v[3] * inv_scale) << 8) |
+           (e2m1x2(v[4] * inv_scale, v[5] * inv_scale) << 16) | (e2m1x2(v[6] * inv_scale, v[7] * inv_scale) << 24);
 }
+
+// SwiGLU product silu(g) * u with the fast exponential and division intrinsics.
+MOE_DEV float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 // Byte of the scale of (operand row `pos`, K-block `kb`) in an activation
 // operand laid out for the tensor cores: rows are grouped in tiles of `bn`

@@ -61,7 +61,7 @@ struct GemmArgs {
     const uint8_t* b_scales;     // activation scale atoms (xsp or hsp)
     uint8_t* hq;                 // gate/up output: down activation codes [pad_max, F/2]
     uint8_t* hsp;                // gate/up output: down activation scale atoms
-    float* Y;                    // down output [T*k, d]
+    float* Y;                    // down output [T*k, d] (per-pick rows)
     uint32_t* err;
 };
 
@@ -245,16 +245,15 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         if (c0 + i >= nv) break;                 // warp-uniform
-                        const float g = __uint_as_float(vg[i]);
-                        const float h = g / (1.0f + expf(-g)) * __uint_as_float(vu[i]);
+                        const float h = silu_mul(__uint_as_float(vg[i]), __uint_as_float(vu[i]));
                         float amax = fabsf(h);
 #pragma unroll
                         for (int off = 16; off > 0; off >>= 1)
                             amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
                         const int X = mx_shared_exp(amax);
-                        const uint32_t code = e2m1_code(h, exp2_int(-X));
-                        const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, code, 1);
-                        const uint32_t byte = (code | (hi << 4)) & 0xFFu;
+                        const float hs = h * exp2_int(-X);
+                        const float hs_hi = __shfl_down_sync(0xFFFFFFFFu, hs, 1);
+                        const uint32_t byte = e2m1x2(hs, hs_hi);      // valid on even lanes
                         const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
                         const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
                         const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 6);
@@ -282,6 +281,192 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce[b]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag) record_error(a.err, MOE_DEV_TIMEOUT);
+}
+
+// Gate/up for tiles of up to 128 routed rows (large batches), in the
+// token-major orientation: D[row, 0..255] = A[row] x [Wg tile; Wu tile]^T,
+// M = 128 routed rows, N = 256 (gate features f0..f0+127, then up), K = d.
+// The epilogue thread of TMEM lane r holds the 128 gate and 128 up values of
+// its row, so h = silu(g) * u and its MXFP4 blocks of 32 features are formed
+// in registers, with no shuffles. One accumulator buffer (256 columns).
+template <int NS>
+struct CfgTok {
+    static constexpr int THREADS = 192;
+    static constexpr int BLK = 128 * 128;
+    static constexpr int A_BYTES = BLK;                 // 128 activation rows x 256 e2m1
+    static constexpr int B_BYTES = 2 * BLK;             // gate block, up block (256 rows)
+    static constexpr int SF_BYTES = 3 * 1024;           // activation atoms, gate atoms, up atoms
+    static constexpr int SF_COLS = 24;                  // activation 8, weights 16 (per k-group: gate 4 | up 4)
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + NS * A_BYTES;
+    static constexpr int OFF_SF = OFF_B + NS * B_BYTES;
+    static constexpr int OFF_BAR = OFF_SF + NS * SF_BYTES;
+    static constexpr int N_BARS = 2 * NS + 2;
+    static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+    static constexpr int SMEM = OFF_MISC + 16 + 1024;
+    static constexpr int TMEM_USED = 256 + SF_COLS * NS;
+    static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(TMEM_USED <= 512, "TMEM");
+};
+
+template <int NS>
+__global__ void __launch_bounds__(192, 1) ffn_gate_up_tokens_kernel(const __grid_constant__ GemmMaps maps,
+                                                                    const GemmArgs a) {
+    using C = CfgTok<NS>;
+    constexpr int BN = 128;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* empty = full + NS;
+    uint64_t* accf = empty + NS;
+    uint64_t* acce = accf + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        mbar_init(accf, 1);
+        mbar_init(acce, 4);
+        *abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&maps.b[3]);
+    }
+    if (warp == 5) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_items = *a.n_work * a.m_tiles;
+    const int nc = (a.K + 255) / 256;
+    const int atoms = a.K / 128;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ TMA producer (one thread)
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok_run = true;
+            int4 w_next = blockIdx.x < n_items ? a.work[blockIdx.x / a.m_tiles] : make_int4(0, 0, 0, 0);
+            for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x) {
+                const int4 w = w_next;
+                const int nxt = item + gridDim.x;
+                if (nxt < n_items) w_next = a.work[nxt / a.m_tiles];
+                const int mt = item % a.m_tiles;
+                const int slot = w.x, pos0 = w.y;
+                const uint8_t* rec = a.arena + (size_t)slot * a.slot_bytes;
+                const int tg = mt, tu = a.F / 128 + mt;               // gate tile, up tile
+                const uint8_t* cg = rec + a.off_codes + (size_t)tg * nc * C::BLK;
+                const uint8_t* cu = rec + a.off_codes + (size_t)tu * nc * C::BLK;
+                const uint8_t* sg = rec + a.off_scales + (size_t)tg * atoms * 512;
+                const uint8_t* su = rec + a.off_scales + (size_t)tu * atoms * 512;
+                const uint8_t* sa = a.b_scales + (size_t)(pos0 / BN) * atoms * 512;
+                for (int kc = 0; kc < nc; ++kc, ++it) {
+                    const int s = (int)(it % NS);
+                    const uint32_t r = it / NS;
+                    if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
+                    uint8_t* As = smem + C::OFF_A + s * C::A_BYTES;
+                    uint8_t* Bs = smem + C::OFF_B + s * C::B_BYTES;
+                    uint8_t* SFs = smem + C::OFF_SF + s * C::SF_BYTES;
+                    const int at0 = 2 * kc;
+                    const int ats = atoms - at0 < 2 ? atoms - at0 : 2;
+                    const uint32_t sf_bytes = (uint32_t)ats * 512u;
+                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES + 3 * sf_bytes);
+                    tma_load_2d(As, &maps.b[3], &full[s], kc * 128, pos0);
+                    bulk_load(Bs, cg + (size_t)kc * C::BLK, C::BLK, &full[s]);
+                    bulk_load(Bs + C::BLK, cu + (size_t)kc * C::BLK, C::BLK, &full[s]);
+                    bulk_load(SFs, sa + (size_t)at0 * 512, sf_bytes, &full[s]);
+                    bulk_load(SFs + 1024, sg + (size_t)at0 * 512, sf_bytes, &full[s]);
+                    bulk_load(SFs + 2048, su + (size_t)at0 * 512, sf_bytes, &full[s]);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, j = 0;
+            bool ok_run = true;
+            for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x, ++j) {
+                if (!mbar_wait(acce, (j & 1) ^ 1, abort_flag)) break;
+                tc_fence_after();
+                for (int kc = 0; kc < nc; ++kc, ++it) {
+                    const int s = (int)(it % NS);
+                    const uint32_t r = it / NS;
+                    if (!mbar_wait(&full[s], r & 1, abort_flag)) { ok_run = false; break; }
+                    tc_fence_after();
+                    const int rem = (a.K - kc * 256) / 64;
+                    const int ksteps = rem < 4 ? rem : 4;
+                    const int ats = (ksteps + 1) / 2;
+                    const uint32_t sfc = tmem + 256 + s * C::SF_COLS;
+                    const uint32_t sfs = smem_u32(smem + C::OFF_SF + s * C::SF_BYTES);
+                    for (int q = 0; q < ats; ++q) {
+                        tc_cp_sf_atom(sfc + 4 * q, smem_desc_sf(sfs + 512 * q));               // activations
+                        tc_cp_sf_atom(sfc + 8 + 8 * q, smem_desc_sf(sfs + 1024 + 512 * q));    // gate rows 0..127
+                        tc_cp_sf_atom(sfc + 12 + 8 * q, smem_desc_sf(sfs + 2048 + 512 * q));   // up rows 128..255
+                    }
+                    const uint32_t as = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
+                    const uint32_t bs = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
+                    for (int kk = 0; kk < ksteps; ++kk)
+                        tc_mma_mxf4(tmem, smem_desc_sw128(as + kk * 32), smem_desc_sw128(bs + kk * 32),
+                                    idesc_mxf4(256, (kk & 1) * 2, (kk & 1) * 2), sfc + (kk >> 1) * 4,
+                                    sfc + 8 + (kk >> 1) * 8, (kc | kk) != 0 ? 1u : 0u);
+                    tc_commit(&empty[s]);
+                }
+                if (ok_run) tc_commit(accf);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue: lane = routed row
+        uint32_t j = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
+            const int4 w = a.work[item / a.m_tiles];
+            const int mt = item % a.m_tiles;
+            const int pos0 = w.y, nv = w.z;
+            if (!warp_wait(accf, j & 1, abort_flag)) break;
+            tc_fence_after();
+            const int row = warp * 32 + lane;
+            const int pos = pos0 + row;
+            const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+            for (int fb = 0; fb < 4; ++fb) {                        // 4 blocks of 32 features
+                uint32_t g0[16], g1[16], u0[16], u1[16];
+                tc_ld_x16(trow + 32 * fb, g0);
+                tc_ld_x16(trow + 32 * fb + 16, g1);
+                tc_ld_x16(trow + 128 + 32 * fb, u0);
+                tc_ld_x16(trow + 128 + 32 * fb + 16, u1);
+                tc_wait_ld();
+                float h[32];
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    h[i] = silu_mul(__uint_as_float(i < 16 ? g0[i] : g1[i - 16]),
+                                    __uint_as_float(i < 16 ? u0[i] : u1[i - 16]));
+                    amax = fmaxf(amax, fabsf(h[i]));
+                }
+                const int X = mx_shared_exp(amax);
+                const float inv = exp2_int(-X);
+                uint32_t wd[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) wd[q] = e2m1x8(h + q * 8, inv);
+                if (row < nv) {
+                    const int f = mt * 128 + 32 * fb;
+                    *reinterpret_cast<uint4*>(a.hq + (size_t)pos * (a.F / 2) + f / 2) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                    a.hsp[operand_scale_offset(pos, f / 32, BN, a.F)] = (uint8_t)(X + 127);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce);
         }
     }
 
@@ -361,6 +546,28 @@ cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& g, long max_items, 
     return cudaGetLastError();
 }
 
+template <int NS>
+cudaError_t launch_tokens(const GemmMaps& maps, const GemmArgs& g, long max_items, cudaStream_t s) {
+    using C = CfgTok<NS>;
+    auto kern = ffn_gate_up_tokens_kernel<NS>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    if (max_items <= 0) return cudaSuccess;
+    long grid = moe_sm_count();                    // one CTA per SM (TMEM: 512 columns each)
+    if (grid > max_items) grid = max_items;
+    moe_prof_begin(MK_GEMM_GATE_UP, s);
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM, s>>>(maps, g);
+    moe_prof_end(MK_GEMM_GATE_UP, s);
+    moe_count_launches(1);
+    return cudaGetLastError();
+}
+
 template <int MODE>
 cudaError_t launch_mode(const GemmMaps& maps, const GemmArgs& g, long max_items, int bn, cudaStream_t s) {
     if constexpr (MODE == 1) {   // gate + up tiles per stage: 32 KB of weights at KCH = 1
@@ -407,7 +614,8 @@ cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches
     g1.b_scales = a.xsp;
     g1.hq = a.hq;
     g1.hsp = a.hsp;
-    e = launch_mode<1>(m1, g1, (long)a.work_max * g1.m_tiles, a.bn, s);
+    if (a.bn == 128) e = launch_tokens<4>(m1, g1, (long)a.work_max * g1.m_tiles, s);   // large batches
+    else e = launch_mode<1>(m1, g1, (long)a.work_max * g1.m_tiles, a.bn, s);
     if (e != cudaSuccess) return e;
 
     GemmArgs g2 = g;       // down
@@ -417,6 +625,7 @@ cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches
     g2.m_tiles = a.d / 128;
     g2.b_scales = a.hsp;
     g2.Y = a.Y;
+
     e = launch_mode<2>(m2, g2, (long)a.work_max * g2.m_tiles, a.bn, s);
     if (n_launches) *n_launches = 2;
     return e;

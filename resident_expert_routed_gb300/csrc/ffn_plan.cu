@@ -73,40 +73,42 @@ __global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restri
     }
 }
 
-// One thread per (pick, 32-element block): 64 bytes of bf16 in, 16 bytes of
-// codes to the pick's operand row and one scale byte to its tile's atom.
+// One thread per (pick, 128-element group): 256 bytes of bf16 in, 64 bytes of
+// codes to the pick's operand row and the group's four scale bytes (adjacent
+// in the tile's atom) as one 4-byte store.
 __global__ void __launch_bounds__(256) ffn_pack(const uint16_t* __restrict__ x, const int32_t* __restrict__ pos_of_pair,
                                                 int P, int k, int d, int bn, uint8_t* __restrict__ xp,
                                                 uint8_t* __restrict__ xsp) {
-    const int nb = d / 32;
-    const long total = (long)P * nb;
+    const int ng = d / 128;
+    const long total = (long)P * ng;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
-        const long p = i / nb;
-        const int b = (int)(i % nb);
+        const long p = i / ng;
+        const int g = (int)(i % ng);
         const int pos = pos_of_pair[p];
         if (pos < 0) continue;
         const long t = p / k;
-        const uint4* src = reinterpret_cast<const uint4*>(x + t * d + b * 32);
-        uint4 v[4];
+        uint32_t scales = 0;
+#pragma unroll 1
+        for (int b4 = 0; b4 < 4; ++b4) {
+            const int b = g * 4 + b4;
+            const uint4* src = reinterpret_cast<const uint4*>(x + t * d + b * 32);
+            uint4 v[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = src[q];
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(v);
-        float f[32];
-        float amax = 0.0f;
+            for (int q = 0; q < 4; ++q) v[q] = src[q];
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(v);
+            float f[32];
+            float amax = 0.0f;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) { f[q] = bf16_bits_to_float(h[q]); amax = fmaxf(amax, fabsf(f[q])); }
-        const int X = mx_shared_exp(amax);
-        const float inv = exp2_int(-X);
-        uint32_t w[4];
+            for (int q = 0; q < 32; ++q) { f[q] = bf16_bits_to_float(h[q]); amax = fmaxf(amax, fabsf(f[q])); }
+            const int X = mx_shared_exp(amax);
+            const float inv = exp2_int(-X);
+            uint32_t w[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) word |= e2m1_code(f[q * 8 + r], inv) << (4 * r);
-            w[q] = word;
+            for (int q = 0; q < 4; ++q) w[q] = e2m1x8(f + q * 8, inv);
+            *reinterpret_cast<uint4*>(xp + (size_t)pos * (d / 2) + b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+            scales |= (uint32_t)(X + 127) << (8 * b4);
         }
-        *reinterpret_cast<uint4*>(xp + (size_t)pos * (d / 2) + b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-        xsp[operand_scale_offset(pos, b, bn, d)] = (uint8_t)(X + 127);
+        *reinterpret_cast<uint32_t*>(xsp + operand_scale_offset(pos, g * 4, bn, d)) = scales;
     }
 }
 
@@ -149,7 +151,7 @@ cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
     moe_prof_end(MK_PLAN, s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const long tasks = (long)P * (a.d / 32);
+    const long tasks = (long)P * (a.d / 128);
     long blocks = (tasks + 255) / 256;
     if (blocks > 8L * moe_sm_count()) blocks = 8L * moe_sm_count();
     moe_prof_begin(MK_PACK, s);
