@@ -69,13 +69,13 @@ typedef enum {
  * ffn..2ffn-1) and W_dn [d, ffn]. The record stores them in the order the
  * tensor cores consume them, so that every pipeline stage is one contiguous
  * copy:
- *   off_gu_codes   (ffn/64) * ceil(d/256) * 16384 bytes, tile-major code blocks
+ *   off_gu_codes   (2*ffn/128) * ceil(d/256) * 16384 bytes, tile-major code blocks
  *   off_gu_scales  2*ffn*d/32 bytes, tile-atom order
  *   off_dn_codes   (d/128) * ceil(ffn/256) * 16384 bytes, tile-major code blocks
  *   off_dn_scales  d*ffn/32 bytes, tile-atom order
- * Tiles: rows are grouped in tiles of 128 -- for W_gu, tile g is gate rows
- * 64g..64g+63 followed by up rows ffn+64g..ffn+64g+63; for W_dn, rows
- * 128g..128g+127. Tile row r is the r-th row of that list.
+ * Tiles: rows are grouped in tiles of 128 consecutive logical rows -- tile g
+ * is rows 128g..128g+127 (for W_gu the gate tiles come first, then the up
+ * tiles). Tile row r is row 128g + r.
  * Tile-major code blocks: for tile g and chunk c of 256 elements along K
  * (128 bytes; zero past the row end), a 16 KB block of 128 rows x 128 bytes
  * at byte (g * ceil(K/256) + c) * 16384; within it, the 16-byte piece q of
@@ -113,6 +113,11 @@ typedef struct {
  * sel_slot int32, sel_w fp32 (the pick's own score, not renormalised);
  * when fewer than k experts are resident the tail is (-1, -1, 0).
  * workspace: >= moe_workspace_bytes(T, k, d, ffn, E, S) bytes (any ffn, S).
+ * hidden_bf16, w_router and workspace must be 16-byte aligned (MOE_EINVAL).
+ * Batches of more than 64 tokens with d % 64 == 0 and E % 16 == 0 are scored
+ * on the tensor cores: W_r is split exactly into three bf16 parts in the
+ * workspace and the products are accumulated in fp32, so the logits match
+ * the CUDA-core path up to fp32 rounding order.
  * Limits: 1 <= k <= 32, k <= E <= 1024, d % 32 == 0, T >= 1.
  */
 moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, const float* bias,
@@ -126,8 +131,11 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
  * this exists for callers of this library that cannot allocate device memory
  * when they route -- e.g. a serving loop whose memory budget was fixed at
  * start-up, or a plug-in whose host framework owns every allocation -- since
- * cudaMalloc can also synchronise the device). Same arguments, results and
- * limits as moe_route_resident, minus the workspace; it allocates nothing.
+ * cudaMalloc can also synchronise the device). Same arguments and limits as
+ * moe_route_resident, minus the workspace; it allocates nothing. It always
+ * scores on the CUDA cores, so for batches that moe_route_resident scores on
+ * the tensor cores (above 64 tokens) the logits can differ in the last fp32
+ * bits, and a pick at a near-tie can differ.
  * The split-K partial logits live in one fixed device array of 4 MiB
  * (2^20 fp32) inside the library, held by every GPU that loads the library
  * until the process exits; a call whose partials would not fit

@@ -79,8 +79,12 @@ FfnCarve ffn_carve(int T, int k, int d, int F, int S) {
     return c;
 }
 
+// Routing workspace: the split-K partial logits of the CUDA-core router, or,
+// for batches the tensor-core router takes, its three bf16 parts of W_r
+// followed by its partials.
 size_t route_bytes(int T, int E, int d) {
-    return align_up((size_t)route_splits(T, E, d) * T * E * 4, 256);
+    if (!router_tc_eligible(T, E, d)) return align_up((size_t)route_splits(T, E, d) * T * E * 4, 256);
+    return router_tc_split_bytes(E, d) + align_up((size_t)router_tc_splits(T, E, d) * T * E * 4, 256);
 }
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ECUDA; }
@@ -220,6 +224,7 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
     if (!hidden_bf16 || !w_router || !slot_of || !want_e || !want_s || !sel_e || !sel_slot || !sel_w || !workspace)
         return MOE_EINVAL;
     if (T < 1 || d < 32 || d % 32 || E < 1 || k < 1 || k > 32 || k > E) return MOE_EINVAL;
+    if (((uintptr_t)hidden_bf16 | (uintptr_t)w_router | (uintptr_t)workspace) & 15) return MOE_EINVAL;
     if (E > 1024) return MOE_EUNSUPPORTED;
     if ((size_t)T * E > ((size_t)1 << 31)) return MOE_EUNSUPPORTED;
     if (ws_bytes < route_bytes(T, E, d)) return MOE_ENOMEM;
@@ -232,6 +237,13 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
     a.splits = route_splits(T, E, d);
     a.want_e = want_e; a.want_s = want_s; a.sel_e = sel_e; a.sel_slot = sel_slot; a.sel_w = sel_w;
     a.partial = static_cast<float*>(workspace);
+    a.err = err_word();
+    if (!a.err) return MOE_ECUDA;
+    if (router_tc_eligible(T, E, d)) {
+        a.wsplit = workspace;
+        a.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + router_tc_split_bytes(E, d));
+        a.splits = router_tc_splits(T, E, d);
+    }
     return cuda_status(launch_route(a, static_cast<cudaStream_t>(stream)));
 }
 

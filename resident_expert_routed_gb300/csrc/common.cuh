@@ -303,7 +303,14 @@ struct RouteLaunch {
     int T, d, E, k, splits;
     int32_t* want_e; float* want_s; int32_t* sel_e; int32_t* sel_slot; float* sel_w;
     float* partial;
+    void* wsplit;           // non-null: tensor-core router, W split into three bf16 parts here
+    uint32_t* err;          // device error word (tensor-core router's bounded waits)
 };
+bool router_tc_eligible(int T, int E, int d);
+int router_tc_splits(int T, int E, int d);
+size_t router_tc_split_bytes(int E, int d);
+cudaError_t launch_router_tc(const uint16_t* x, const float* W, int T, int d, int E, int splits, void* wsplit,
+                             float* partial, uint32_t* err, cudaStream_t s);
 cudaError_t launch_route(const RouteLaunch& a, cudaStream_t s);
 int route_splits(int T, int E, int d);
 

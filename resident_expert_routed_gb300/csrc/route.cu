@@ -208,11 +208,17 @@ int route_splits(int T, int E, int d) {
 }
 
 cudaError_t launch_route(const RouteLaunch& a, cudaStream_t s) {
-    dim3 g1((a.E + BE - 1) / BE, (a.T + BT - 1) / BT, a.splits);
-    moe_prof_begin(MK_ROUTER_LOGITS, s);
-    router_logits_partial<<<g1, 256, 0, s>>>(a.x, a.w, a.T, a.d, a.E, a.d / a.splits, a.partial);
-    moe_prof_end(MK_ROUTER_LOGITS, s);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (a.wsplit) {
+        e = launch_router_tc(a.x, a.w, a.T, a.d, a.E, a.splits, a.wsplit, a.partial, a.err, s);
+    } else {
+        dim3 g1((a.E + BE - 1) / BE, (a.T + BT - 1) / BT, a.splits);
+        moe_prof_begin(MK_ROUTER_LOGITS, s);
+        router_logits_partial<<<g1, 256, 0, s>>>(a.x, a.w, a.T, a.d, a.E, a.d / a.splits, a.partial);
+        moe_prof_end(MK_ROUTER_LOGITS, s);
+        moe_count_launches(1);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     const int vpl = (a.E + 31) / 32;
     dim3 g2((a.T + 7) / 8);
@@ -228,7 +234,7 @@ cudaError_t launch_route(const RouteLaunch& a, cudaStream_t s) {
     else MOE_SEL(32);
 #undef MOE_SEL
     moe_prof_end(MK_ROUTE_SELECT, s);
-    moe_count_launches(2);
+    moe_count_launches(1);
     return cudaGetLastError();
 }
 
@@ -275,6 +281,7 @@ extern "C" moe_status moe_route_resident_noalloc(const void* hidden_bf16, const 
     if (!hidden_bf16 || !w_router || !slot_of || !want_e || !want_s || !sel_e || !sel_slot || !sel_w)
         return MOE_EINVAL;
     if (T < 1 || d < 32 || d % 32 || E < 1 || k < 1 || k > 32 || k > E) return MOE_EINVAL;
+    if (((uintptr_t)hidden_bf16 | (uintptr_t)w_router) & 15) return MOE_EINVAL;
     if (E > 1024) return MOE_EUNSUPPORTED;
     const int splits = route_splits(T, E, d);
     if ((size_t)splits * T * E > kNoAllocPartials) return MOE_EUNSUPPORTED;   // beyond the fixed array

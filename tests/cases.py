@@ -20,6 +20,10 @@ RAGGED = synth.LayerConfig("ragged E40 k3 d384 F256 R25", E=40, k=3, d=384, ffn=
 SPARSE = synth.LayerConfig("sparse E16 k4 d256 F128 R2", E=16, k=4, d=256, ffn=128, resident=2, sigma=None,
                            seed=0x7EED00A1)
 
+# Routing only: E below one 128-expert tile and an odd number of 64-element K chunks.
+ODD = synth.LayerConfig("odd E48 k6 d320 F128 R30", E=48, k=6, d=320, ffn=128, resident=30, sigma=1.0,
+                        seed=0x7EED00A2)
+
 
 @dataclasses.dataclass
 class Case:

@@ -52,6 +52,8 @@ def test_workspace_sizes():
     w1 = moe.moe_workspace_bytes(1, 8, 4096, 2048, 256, 166)
     w64 = moe.moe_workspace_bytes(64, 8, 4096, 2048, 256, 166)
     w8k = moe.moe_workspace_bytes(8192, 8, 4096, 2048, 256, 166)
+    # large batches route on the tensor cores: three bf16 parts of W_r plus the partial logits
+    assert moe.moe_workspace_bytes(8192, 8, 4096, 0, 256, 0) >= 3 * 256 * 4096 * 2 + 8192 * 256 * 4
     assert 0 < w1 < w64 < w8k
     # up to 64 tokens the FFN keeps one fp32 row per pick (T*k*d*4 bytes) for the ordered combine
     assert w64 >= 64 * 8 * 4096 * 4
@@ -80,6 +82,12 @@ def test_route_rejects_bad_arguments():
     assert L.moe_route_resident(*ok[:2], NULL, FAKE, 4, 64, 2048, 4, *outs, FAKE, 1 << 30, NULL) == moe.MOE_EUNSUPPORTED
     # workspace too small
     assert L.moe_route_resident(*ok[:2], NULL, FAKE, 64, 4096, 256, 8, *outs, FAKE, 16, NULL) == moe.MOE_ENOMEM
+    # hidden states, router weights or workspace not 16-byte aligned
+    odd = ctypes.c_void_p(0x1002)
+    assert L.moe_route_resident(odd, FAKE, NULL, FAKE, 4, 64, 16, 4, *outs, FAKE, 1 << 20, NULL) == moe.MOE_EINVAL
+    assert L.moe_route_resident(FAKE, odd, NULL, FAKE, 4, 64, 16, 4, *outs, FAKE, 1 << 20, NULL) == moe.MOE_EINVAL
+    assert L.moe_route_resident(FAKE, FAKE, NULL, FAKE, 4, 64, 16, 4, *outs, odd, 1 << 20, NULL) == moe.MOE_EINVAL
+    assert L.moe_route_resident_noalloc(odd, FAKE, NULL, FAKE, 4, 64, 16, 4, *outs, NULL) == moe.MOE_EINVAL
 
 
 def _arena(**kw):

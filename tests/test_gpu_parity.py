@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import synth
-from tests.cases import (RAGGED, SPARSE, device_arena, ffn_within_tolerance, hidden_dev, make_case,
+from tests.cases import (ODD, RAGGED, SPARSE, device_arena, ffn_within_tolerance, hidden_dev, make_case,
                          near_tie_tokens, oracle_experts, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -70,8 +70,11 @@ def check_route(c, g, rows):
     return ref
 
 
+# Up to 64 tokens the CUDA-core router scores; above, the tensor-core router (when d % 64 == 0 and
+# E % 16 == 0): ragged token tails, E below one 128-expert tile, one and two K slices.
 ROUTE_CASES = [(synth.TINY, 8), (RAGGED, 37), (SPARSE, 5), (synth.DECODE, 1), (synth.DECODE, 8),
-               (synth.DECODE, 64), (synth.GLM, 16)]
+               (synth.DECODE, 64), (synth.GLM, 16), (synth.TINY, 200), (ODD, 257), (RAGGED, 130),
+               (synth.DECODE, 65), (synth.DECODE, 300), (synth.GLM, 130)]
 
 
 @pytest.mark.parametrize("cfg,T", ROUTE_CASES, ids=[f"{c.name.split()[0]}-T{T}" for c, T in ROUTE_CASES])
