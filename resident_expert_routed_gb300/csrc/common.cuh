@@ -238,12 +238,6 @@ MOE_DEV void tc_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// Copy one 32-row x 16-byte scale-factor atom from shared memory into four
-// TMEM columns, replicated into all four 32-lane quadrants.
-MOE_DEV void tc_cp_sf_atom(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // D[tmem] (+)= A[smem] * B[smem]^T, e2m1 x e2m1 with e8m0 block-32 scales from TMEM.
 MOE_DEV void tc_mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
                          uint32_t sfb_tmem, uint32_t accumulate) {
@@ -266,6 +260,14 @@ MOE_DEV void tc_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 MOE_DEV void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Each lane of the warp writes 8 consecutive 32-bit columns of its own TMEM lane.
+MOE_DEV void tc_st_x8(uint32_t taddr, uint4 lo, uint4 hi) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"r"(taddr), "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                 : "memory");
+}
+MOE_DEV void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Shared-memory matrix descriptor, K-major operand tile with 128-byte rows in
 // the 128-byte swizzle layout written by TMA (8-row groups 1024 B apart).
 MOE_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
@@ -275,16 +277,6 @@ MOE_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
     d |= (uint64_t)(1024u >> 4) << 32;    // stride byte offset: next 8-row group
     d |= (uint64_t)1 << 46;               // descriptor version for the sm_100 family
     d |= (uint64_t)2 << 61;               // 128-byte swizzle
-    return d;
-}
-
-// Descriptor of a 32-row x 16-byte scale atom stored densely (no swizzle).
-MOE_DEV uint64_t smem_desc_sf(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)(128u >> 4) << 16;
-    d |= (uint64_t)(128u >> 4) << 32;
-    d |= (uint64_t)1 << 46;
     return d;
 }
 

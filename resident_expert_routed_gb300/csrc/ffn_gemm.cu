@@ -17,17 +17,18 @@
 //
 // The weight tiles are the MMA's A operand (M = 128) and the few routed rows
 // the B operand (N = 16..128), so a decode-sized tile still streams whole
-// weight tiles at full width. Every operand arrives by bulk copy / TMA issued
-// by one thread, so a stage costs one DRAM round trip and nothing else:
+// weight tiles at full width. Roles:
 //   warp 4     lane 0, per stage: 32 KB of weight codes as contiguous bulk
 //              copies (the arena keeps codes in tile-major 16 KB blocks, already
-//              in the 128-byte swizzle), TMA boxes of activation rows (their
-//              height the tile's row count rounded up), and 1-D bulk copies of
-//              scale atoms (weights: from the arena, which keeps scales in the
-//              tensor cores' atom order; activations: from the workspace,
-//              written in that order by ffn_pack / the gate/up epilogue);
-//   warp 5     TMEM allocator; lane 0 issues tcgen05.cp (scales -> TMEM) and
-//              tcgen05.mma, and commits to the stage / accumulator barriers;
+//              in the 128-byte swizzle) and TMA boxes of activation rows (their
+//              height the tile's row count rounded up);
+//   warps 6-9  scale factors: each warp (one TMEM lane quadrant) loads the
+//              stage's scale atoms (weights: from the arena, which keeps them in
+//              the tensor cores' atom order; activations: from the workspace,
+//              written in that order by ffn_pack / the gate/up epilogue) and
+//              writes them into TMEM with tcgen05.st (see scale_writer);
+//   warp 5     TMEM allocator; lane 0 issues tcgen05.mma and commits to the
+//              stage / accumulator barriers;
 //   warps 0-3  epilogue: tcgen05.ld of their 32-lane quadrant of the
 //              (double-buffered) accumulators, then the per-mode epilogue.
 // The grid is persistent (one CTA per SM) over the flattened (tile, 128-row
@@ -65,6 +66,45 @@ struct GemmArgs {
     uint32_t* err;
 };
 
+// Scale factors reach TMEM through registers, not tcgen05.cp: the copy that
+// replicates a 32-row atom into the four TMEM lane quadrants occupies the
+// tensor pipe for about half an MMA, and a stage needs one per 128 K of every
+// operand. Warps 6-9 (one per lane quadrant) instead load each stage's atoms
+// from global memory PF stages ahead and write them with tcgen05.st, which
+// runs beside the MMAs; they signal the MMA thread through sfull[stage]. Lane
+// i of every quadrant holds row i (16 bytes) of each 512-byte atom, the layout
+// the 32x128b.warpx4 copy produces. load(g, v) fills the NV atoms of stage g
+// (zeros past the end of K) and returns false past the last stage.
+template <int NV, int PF, int NS, typename Load>
+__device__ __forceinline__ void scale_writer(int n_stages, const Load& load, uint64_t* empty, uint64_t* sfull,
+                                             uint32_t sf_base, int sf_cols, volatile int* abort_flag) {
+    static_assert(NV % 2 == 0, "atoms are written in pairs");
+    const int lane = threadIdx.x & 31;
+    uint4 v[PF][NV];
+#pragma unroll
+    for (int p = 0; p < PF; ++p) load(p, v[p]);
+    bool ok_run = true;
+    for (int g0 = 0; g0 < n_stages && ok_run; g0 += PF) {
+#pragma unroll
+        for (int p = 0; p < PF; ++p) {
+            const int g = g0 + p;
+            if (g >= n_stages) break;
+            const int s = g % NS;
+            const uint32_t r = (uint32_t)(g / NS);
+            if (!warp_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
+            tc_fence_after();
+            const uint32_t sfc = sf_base + s * sf_cols;
+#pragma unroll
+            for (int q = 0; q < NV; q += 2) tc_st_x8(sfc + 4 * q, v[p][q], v[p][q + 1]);
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sfull[s]);
+            load(g + PF, v[p]);
+        }
+    }
+}
+
 // Per pipeline stage: KCH chunks of 256 elements along K. The gate/up GEMM
 // loads, per chunk, one 16 KB code block of the gate tile and one of the up
 // tile (rows f0..f0+127 and ffn+f0..ffn+f0+127) and accumulates them into two
@@ -72,21 +112,20 @@ struct GemmArgs {
 // feature; the down GEMM loads one tile. Stages carry 32 KB of weights.
 template <int MODE, int BN, int NS, int KCH, int NBUF>
 struct Cfg {
-    static constexpr int THREADS = 192;           // warps 0-3 epilogue, 4 TMA, 5 MMA
+    static constexpr int THREADS = 320;           // warps 0-3 epilogue, 4 TMA, 5 MMA, 6-9 scales
     static constexpr int NMAT = MODE == 1 ? 2 : 1;
     static constexpr int BLK = 128 * 128;         // one 16 KB code block: 128 rows x 256 e2m1
     static constexpr int A_BYTES = NMAT * KCH * BLK;
     static constexpr int B_CHUNK = BN * 128;
     static constexpr int B_BYTES = KCH * B_CHUNK;
-    static constexpr int SFA_MAT = KCH * 1024;    // weight atoms of one matrix (2 per chunk)
-    static constexpr int SF_BYTES = (NMAT + 1) * SFA_MAT;
-    static constexpr int SF_COLS = (NMAT + 1) * 8 * KCH;   // TMEM columns of one stage's scales
+    static constexpr int NV = (NMAT + 1) * 2 * KCH;        // scale atoms per stage (weights, then activations)
+    static constexpr int PF = 4 / KCH;                     // stages of scales loaded ahead
+    static constexpr int SF_COLS = 4 * NV;                 // TMEM columns of one stage's scales
     static constexpr int ACC_COLS = NMAT * BN;    // one accumulator buffer (gate, then up)
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + NS * A_BYTES;
-    static constexpr int OFF_SF = OFF_B + NS * B_BYTES;
-    static constexpr int OFF_BAR = OFF_SF + NS * SF_BYTES;
-    static constexpr int N_BARS = 2 * NS + 2 * NBUF;
+    static constexpr int OFF_BAR = OFF_B + NS * B_BYTES;
+    static constexpr int N_BARS = 3 * NS + 2 * NBUF;
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
     static constexpr int TMEM_USED = NBUF * ACC_COLS + SF_COLS * NS;
@@ -100,20 +139,21 @@ struct Cfg {
 };
 
 template <int MODE, int BN, int NS, int KCH, int NBUF>
-__global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
+__global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     using C = Cfg<MODE, BN, NS, KCH, NBUF>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* empty = full + NS;
-    uint64_t* accf = empty + NS;
+    uint64_t* sfull = empty + NS;
+    uint64_t* accf = sfull + NS;
     uint64_t* acce = accf + NBUF;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sfull[s], 4); }
         for (int b = 0; b < NBUF; ++b) { mbar_init(&accf[b], 1); mbar_init(&acce[b], 4); }
         *abort_flag = 0;
         fence_barrier_init();
@@ -149,33 +189,21 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
                 const int tile0 = mt, tile1 = a.F / 128 + mt;
                 const uint8_t* codes0 = rec + a.off_codes + (size_t)tile0 * nc * C::BLK;
                 const uint8_t* codes1 = rec + a.off_codes + (size_t)tile1 * nc * C::BLK;
-                const uint8_t* sfa0 = rec + a.off_scales + (size_t)tile0 * atoms * 512;
-                const uint8_t* sfa1 = rec + a.off_scales + (size_t)tile1 * atoms * 512;
-                const uint8_t* sfb = a.b_scales + (size_t)(pos0 / BN) * atoms * 512;
                 for (int st = 0; st < nst; ++st, ++it) {
                     const int s = (int)(it % NS);
                     const uint32_t r = it / NS;
                     if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
                     uint8_t* As = smem + C::OFF_A + s * C::A_BYTES;
                     uint8_t* Bs = smem + C::OFF_B + s * C::B_BYTES;
-                    uint8_t* SFs = smem + C::OFF_SF + s * C::SF_BYTES;
                     const int c0 = st * KCH;
                     const int chunks = nc - c0 < KCH ? nc - c0 : KCH;
-                    const int at0 = 2 * c0;
-                    const int ats = atoms - at0 < 2 * KCH ? atoms - at0 : 2 * KCH;
-                    const uint32_t sf_bytes = (uint32_t)ats * 512u;
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)chunks * (C::NMAT * C::BLK + b_bytes) +
-                                                        (C::NMAT + 1) * sf_bytes);
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)chunks * (C::NMAT * C::BLK + b_bytes));
                     bulk_load(As, codes0 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK, &full[s]);
-                    bulk_load(SFs, sfa0 + (size_t)at0 * 512, sf_bytes, &full[s]);
-                    if (C::NMAT == 2) {
+                    if (C::NMAT == 2)
                         bulk_load(As + KCH * C::BLK, codes1 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK,
                                   &full[s]);
-                        bulk_load(SFs + C::SFA_MAT, sfa1 + (size_t)at0 * 512, sf_bytes, &full[s]);
-                    }
                     for (int q = 0; q < chunks; ++q)
                         tma_load_2d(Bs + q * C::B_CHUNK, &maps.b[hb], &full[s], (c0 + q) * 128, pos0);
-                    bulk_load(SFs + C::NMAT * C::SFA_MAT, sfb + (size_t)at0 * 512, sf_bytes, &full[s]);
                 }
             }
         }
@@ -195,16 +223,15 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
                 for (int st = 0; st < nst; ++st, ++it) {
                     const int s = (int)(it % NS);
                     const uint32_t r = it / NS;
-                    if (!mbar_wait(&full[s], r & 1, abort_flag)) { ok_run = false; break; }
+                    if (!mbar_wait(&full[s], r & 1, abort_flag) || !mbar_wait(&sfull[s], r & 1, abort_flag)) {
+                        ok_run = false;
+                        break;
+                    }
                     tc_fence_after();
                     const int rem = (a.K - st * 256 * KCH) / 64;
                     const int ksteps = rem < 4 * KCH ? rem : 4 * KCH;      // MMAs of K = 64
-                    const int ats = (ksteps + 1) / 2;                        // scale atoms used (2 MMAs each)
+                    // scale columns: weight matrices m < NMAT, then activations, 8 KCH columns each
                     const uint32_t sfc = tmem + NBUF * C::ACC_COLS + s * C::SF_COLS;
-                    const uint32_t sfs = smem_u32(smem + C::OFF_SF + s * C::SF_BYTES);
-                    for (int m = 0; m <= C::NMAT; ++m)                       // weight atoms, then activation atoms
-                        for (int q = 0; q < ats; ++q)
-                            tc_cp_sf_atom(sfc + 8 * KCH * m + 4 * q, smem_desc_sf(sfs + C::SFA_MAT * m + 512 * q));
                     const uint32_t as = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
                     const uint32_t bs = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
                     const uint32_t sfb = sfc + 8 * KCH * C::NMAT;
@@ -222,6 +249,36 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
                 if (ok_run) tc_commit(&accf[b]);
             }
         }
+    } else if (warp >= 6) {
+        // ------------------------------------------------------------ scale factors -> TMEM
+        const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        auto load = [&](int g, uint4 (&v)[C::NV]) {
+#pragma unroll
+            for (int q = 0; q < C::NV; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
+            if (g >= my_items * nst) return;
+            const int li = g / nst, st = g - li * nst;
+            const int item = blockIdx.x + li * gridDim.x;
+            const int wi = item / a.m_tiles;
+            const int4 w = a.work[wi];
+            const int mt = item - wi * a.m_tiles;
+            const uint8_t* sc = a.arena + (size_t)w.x * a.slot_bytes + a.off_scales;
+            const uint8_t* src[C::NMAT + 1];
+            src[0] = sc + (size_t)mt * atoms * 512;
+            if (C::NMAT == 2) src[1] = sc + (size_t)(a.F / 128 + mt) * atoms * 512;
+            src[C::NMAT] = a.b_scales + (size_t)(w.y / BN) * atoms * 512;
+            const int at0 = 2 * KCH * st;
+            const int ats = atoms - at0 < 2 * KCH ? atoms - at0 : 2 * KCH;
+#pragma unroll
+            for (int m = 0; m <= C::NMAT; ++m)
+#pragma unroll
+                for (int q = 0; q < 2 * KCH; ++q)
+                    if (q < ats)
+                        v[m * 2 * KCH + q] =
+                            *reinterpret_cast<const uint4*>(src[m] + (size_t)(at0 + q) * 512 + lane * 16);
+        };
+        scale_writer<C::NV, C::PF, NS>(my_items * nst, load, empty, sfull,
+                                       tmem + ((uint32_t)((warp & 3) * 32) << 16) + NBUF * C::ACC_COLS, C::SF_COLS,
+                                       abort_flag);
     } else {
         // ------------------------------------------------------------ epilogue (warps 0..3)
         uint32_t j = 0;
@@ -298,30 +355,38 @@ __global__ void __launch_bounds__(192, 1) ffn_gemm_kernel(const __grid_constant_
 // M = 128 routed rows, N = 256 (gate features f0..f0+127, then up), K = d.
 // The epilogue thread of TMEM lane r holds the 128 gate and 128 up values of
 // its row, so h = silu(g) * u and its MXFP4 blocks of 32 features are formed
-// in registers, with no shuffles. One accumulator buffer (256 columns).
+// in registers, with no shuffles. One accumulator buffer (256 columns). (The
+// down GEMM stays weight-major at every batch size: there a warp's 32 lanes
+// are 32 consecutive output dims, so its stores of Y are coalesced.)
+//
+// Scale factors reach TMEM through registers, not tcgen05.cp: the copy that
+// replicates a 32-row atom into the four lane quadrants occupies the tensor
+// pipe for about half an MMA, and a stage needs six of them for four MMAs.
+// Warps 6-9 (one per lane quadrant) instead load each stage's six atoms from
+// global memory a few stages ahead and write them with tcgen05.st, which runs
+// beside the MMAs; they signal the MMA thread through sfull[stage].
 template <int NS>
 struct CfgTok {
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 320;                 // warps 0-3 epilogue, 4 TMA, 5 MMA, 6-9 scales
     static constexpr int BLK = 128 * 128;
     static constexpr int A_BYTES = BLK;                 // 128 activation rows x 256 e2m1
     static constexpr int B_BYTES = 2 * BLK;             // gate block, up block (256 rows)
-    static constexpr int SF_BYTES = 3 * 1024;           // activation atoms, gate atoms, up atoms
-    static constexpr int SF_COLS = 24;                  // activation 8, weights 16 (per k-group: gate 4 | up 4)
+    static constexpr int SF_COLS = 24;                  // activation 8, then per k-group: gate 4 | up 4
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + NS * A_BYTES;
-    static constexpr int OFF_SF = OFF_B + NS * B_BYTES;
-    static constexpr int OFF_BAR = OFF_SF + NS * SF_BYTES;
-    static constexpr int N_BARS = 2 * NS + 2;
+    static constexpr int OFF_BAR = OFF_B + NS * B_BYTES;
+    static constexpr int N_BARS = 3 * NS + 2;
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;
     static constexpr int TMEM_USED = 256 + SF_COLS * NS;
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
+    static constexpr int PF = 4;                        // stages of scales loaded ahead
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(TMEM_USED <= 512, "TMEM");
 };
 
 template <int NS>
-__global__ void __launch_bounds__(192, 1) ffn_gate_up_tokens_kernel(const __grid_constant__ GemmMaps maps,
+__global__ void __launch_bounds__(320, 1) ffn_gate_up_tokens_kernel(const __grid_constant__ GemmMaps maps,
                                                                     const GemmArgs a) {
     using C = CfgTok<NS>;
     constexpr int BN = 128;
@@ -329,14 +394,15 @@ __global__ void __launch_bounds__(192, 1) ffn_gate_up_tokens_kernel(const __grid
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* empty = full + NS;
-    uint64_t* accf = empty + NS;
+    uint64_t* sfull = empty + NS;
+    uint64_t* accf = sfull + NS;
     uint64_t* acce = accf + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sfull[s], 4); }
         mbar_init(accf, 1);
         mbar_init(acce, 4);
         *abort_flag = 0;
@@ -366,29 +432,18 @@ __global__ void __launch_bounds__(192, 1) ffn_gate_up_tokens_kernel(const __grid
                 const int mt = item % a.m_tiles;
                 const int slot = w.x, pos0 = w.y;
                 const uint8_t* rec = a.arena + (size_t)slot * a.slot_bytes;
-                const int tg = mt, tu = a.F / 128 + mt;               // gate tile, up tile
-                const uint8_t* cg = rec + a.off_codes + (size_t)tg * nc * C::BLK;
-                const uint8_t* cu = rec + a.off_codes + (size_t)tu * nc * C::BLK;
-                const uint8_t* sg = rec + a.off_scales + (size_t)tg * atoms * 512;
-                const uint8_t* su = rec + a.off_scales + (size_t)tu * atoms * 512;
-                const uint8_t* sa = a.b_scales + (size_t)(pos0 / BN) * atoms * 512;
+                const uint8_t* cg = rec + a.off_codes + (size_t)mt * nc * C::BLK;                  // gate tile
+                const uint8_t* cu = rec + a.off_codes + (size_t)(a.F / 128 + mt) * nc * C::BLK;    // up tile
                 for (int kc = 0; kc < nc; ++kc, ++it) {
                     const int s = (int)(it % NS);
                     const uint32_t r = it / NS;
                     if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
                     uint8_t* As = smem + C::OFF_A + s * C::A_BYTES;
                     uint8_t* Bs = smem + C::OFF_B + s * C::B_BYTES;
-                    uint8_t* SFs = smem + C::OFF_SF + s * C::SF_BYTES;
-                    const int at0 = 2 * kc;
-                    const int ats = atoms - at0 < 2 ? atoms - at0 : 2;
-                    const uint32_t sf_bytes = (uint32_t)ats * 512u;
-                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES + 3 * sf_bytes);
+                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
                     tma_load_2d(As, &maps.b[3], &full[s], kc * 128, pos0);
                     bulk_load(Bs, cg + (size_t)kc * C::BLK, C::BLK, &full[s]);
                     bulk_load(Bs + C::BLK, cu + (size_t)kc * C::BLK, C::BLK, &full[s]);
-                    bulk_load(SFs, sa + (size_t)at0 * 512, sf_bytes, &full[s]);
-                    bulk_load(SFs + 1024, sg + (size_t)at0 * 512, sf_bytes, &full[s]);
-                    bulk_load(SFs + 2048, su + (size_t)at0 * 512, sf_bytes, &full[s]);
                 }
             }
         }
@@ -403,18 +458,14 @@ __global__ void __launch_bounds__(192, 1) ffn_gate_up_tokens_kernel(const __grid
                 for (int kc = 0; kc < nc; ++kc, ++it) {
                     const int s = (int)(it % NS);
                     const uint32_t r = it / NS;
-                    if (!mbar_wait(&full[s], r & 1, abort_flag)) { ok_run = false; break; }
+                    if (!mbar_wait(&full[s], r & 1, abort_flag) || !mbar_wait(&sfull[s], r & 1, abort_flag)) {
+                        ok_run = false;
+                        break;
+                    }
                     tc_fence_after();
                     const int rem = (a.K - kc * 256) / 64;
                     const int ksteps = rem < 4 ? rem : 4;
-                    const int ats = (ksteps + 1) / 2;
                     const uint32_t sfc = tmem + 256 + s * C::SF_COLS;
-                    const uint32_t sfs = smem_u32(smem + C::OFF_SF + s * C::SF_BYTES);
-                    for (int q = 0; q < ats; ++q) {
-                        tc_cp_sf_atom(sfc + 4 * q, smem_desc_sf(sfs + 512 * q));               // activations
-                        tc_cp_sf_atom(sfc + 8 + 8 * q, smem_desc_sf(sfs + 1024 + 512 * q));    // gate rows 0..127
-                        tc_cp_sf_atom(sfc + 12 + 8 * q, smem_desc_sf(sfs + 2048 + 512 * q));   // up rows 128..255
-                    }
                     const uint32_t as = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
                     const uint32_t bs = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
                     for (int kk = 0; kk < ksteps; ++kk)
@@ -426,6 +477,35 @@ __global__ void __launch_bounds__(192, 1) ffn_gate_up_tokens_kernel(const __grid
                 if (ok_run) tc_commit(accf);
             }
         }
+    } else if (warp >= 6) {
+        // ------------------------------------------------------------ scale factors -> TMEM
+        // stage g of this CTA is K chunk g % nc of its item g / nc; atoms in column
+        // order: activations q = 0, 1, then (gate, up) per q
+        const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        auto load = [&](int g, uint4 (&v)[6]) {
+#pragma unroll
+            for (int q = 0; q < 6; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
+            if (g >= my_items * nc) return;
+            const int li = g / nc, kc = g - li * nc;
+            const int item = blockIdx.x + li * gridDim.x;
+            const int wi = item / a.m_tiles;
+            const int4 w = a.work[wi];
+            const int mt = item - wi * a.m_tiles;
+            const uint8_t* sc = a.arena + (size_t)w.x * a.slot_bytes + a.off_scales;
+            const uint8_t* sa = a.b_scales + (size_t)(w.y / BN) * atoms * 512;
+            const uint8_t* sg = sc + (size_t)mt * atoms * 512;
+            const uint8_t* su = sc + (size_t)(a.F / 128 + mt) * atoms * 512;
+            const int at0 = 2 * kc;
+            const int ats = atoms - at0 < 2 ? atoms - at0 : 2;
+            for (int q = 0; q < ats; ++q) {
+                const size_t o = (size_t)(at0 + q) * 512 + lane * 16;
+                v[q] = *reinterpret_cast<const uint4*>(sa + o);
+                v[2 + 2 * q] = *reinterpret_cast<const uint4*>(sg + o);
+                v[3 + 2 * q] = *reinterpret_cast<const uint4*>(su + o);
+            }
+        };
+        scale_writer<6, C::PF, NS>(my_items * nc, load, empty, sfull,
+                                   tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256, C::SF_COLS, abort_flag);
     } else {
         // ------------------------------------------------------------ epilogue: lane = routed row
         uint32_t j = 0;

@@ -11,11 +11,12 @@
 //   each slot a segment of positions padded to a multiple of the tile height
 //   BN, gives every pick a position in its slot's segment, and writes the GEMM
 //   work list: (slot, first position, rows) per tile of at most BN rows.
-// ffn_pack: for every pick, quantises its token row of x to MXFP4 (OCP MX
-//   v1.0: exponent floor(log2 amax) - 2, round to nearest even, saturate at
-//   6; two codes per byte, even element low) straight into row `position` of
-//   the gate/up GEMM's activation operand, and its scales into the tile's
-//   scale atoms, so the GEMM fetches both with plain TMA / bulk copies.
+// ffn_pack: quantises every token row of x to MXFP4 once (OCP MX v1.0:
+//   exponent floor(log2 amax) - 2, round to nearest even, saturate at 6; two
+//   codes per byte, even element low) and writes it into row `position` of
+//   the gate/up GEMM's activation operand for each of the token's picks, with
+//   its scales in the tile's scale atoms, so the GEMM fetches both with plain
+//   TMA / bulk copies.
 // ffn_combine: out[t] = sum_j sel_w[t,j] * Y[t*k + j], j in order.
 #include "common.cuh"
 
@@ -73,22 +74,21 @@ __global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restri
     }
 }
 
-// One thread per (pick, 128-element group): 256 bytes of bf16 in, 64 bytes of
-// codes to the pick's operand row and the group's four scale bytes (adjacent
-// in the tile's atom) as one 4-byte store.
+// One thread per (token, 128-element group): the token's 256 bytes of bf16
+// are quantised once (not once per pick), then the 64 bytes of codes go to
+// the operand row of each of the token's picks and the group's four scale
+// bytes (adjacent in the tile's atom) to its atom as one 4-byte store.
 __global__ void __launch_bounds__(256) ffn_pack(const uint16_t* __restrict__ x, const int32_t* __restrict__ pos_of_pair,
-                                                int P, int k, int d, int bn, uint8_t* __restrict__ xp,
+                                                int T, int k, int d, int bn, uint8_t* __restrict__ xp,
                                                 uint8_t* __restrict__ xsp) {
     const int ng = d / 128;
-    const long total = (long)P * ng;
+    const long total = (long)T * ng;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
-        const long p = i / ng;
+        const long t = i / ng;
         const int g = (int)(i % ng);
-        const int pos = pos_of_pair[p];
-        if (pos < 0) continue;
-        const long t = p / k;
+        uint4 codes[4];
         uint32_t scales = 0;
-#pragma unroll 1
+#pragma unroll
         for (int b4 = 0; b4 < 4; ++b4) {
             const int b = g * 4 + b4;
             const uint4* src = reinterpret_cast<const uint4*>(x + t * d + b * 32);
@@ -102,13 +102,17 @@ __global__ void __launch_bounds__(256) ffn_pack(const uint16_t* __restrict__ x, 
             for (int q = 0; q < 32; ++q) { f[q] = bf16_bits_to_float(h[q]); amax = fmaxf(amax, fabsf(f[q])); }
             const int X = mx_shared_exp(amax);
             const float inv = exp2_int(-X);
-            uint32_t w[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) w[q] = e2m1x8(f + q * 8, inv);
-            *reinterpret_cast<uint4*>(xp + (size_t)pos * (d / 2) + b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+            codes[b4] = make_uint4(e2m1x8(f, inv), e2m1x8(f + 8, inv), e2m1x8(f + 16, inv), e2m1x8(f + 24, inv));
             scales |= (uint32_t)(X + 127) << (8 * b4);
         }
-        *reinterpret_cast<uint32_t*>(xsp + operand_scale_offset(pos, g * 4, bn, d)) = scales;
+        for (int j = 0; j < k; ++j) {
+            const int pos = pos_of_pair[t * k + j];
+            if (pos < 0) continue;
+            uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)pos * (d / 2) + g * 64);
+#pragma unroll
+            for (int b4 = 0; b4 < 4; ++b4) dst[b4] = codes[b4];
+            *reinterpret_cast<uint32_t*>(xsp + operand_scale_offset(pos, g * 4, bn, d)) = scales;
+        }
     }
 }
 
@@ -151,11 +155,11 @@ cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
     moe_prof_end(MK_PLAN, s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const long tasks = (long)P * (a.d / 128);
+    const long tasks = (long)a.T * (a.d / 128);
     long blocks = (tasks + 255) / 256;
     if (blocks > 8L * moe_sm_count()) blocks = 8L * moe_sm_count();
     moe_prof_begin(MK_PACK, s);
-    ffn_pack<<<(unsigned)blocks, 256, 0, s>>>(a.x, a.pos_of_pair, P, a.k, a.d, a.bn, a.xp, a.xsp);
+    ffn_pack<<<(unsigned)blocks, 256, 0, s>>>(a.x, a.pos_of_pair, a.T, a.k, a.d, a.bn, a.xp, a.xsp);
     moe_prof_end(MK_PACK, s);
     moe_count_launches(2);
     return cudaGetLastError();
