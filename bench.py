@@ -193,6 +193,12 @@ def max_over_ranks(x: float, ws: int) -> float:
     return float(t.item())
 
 
+def job_throughput(step_ms: float, ws: int, units_per_rank: int):
+    """Whole-job rate: every rank processed units_per_rank per step; the job's step is the slowest rank's."""
+    step_ms_max = max_over_ranks(step_ms, ws)
+    return step_ms_max, ws * units_per_rank / (step_ms_max / 1000.0)
+
+
 def barrier(ws: int):
     if ws > 1:
         import torch.distributed as dist
@@ -368,8 +374,7 @@ def run_ours(args, rank, ws, local):
     wall = time.perf_counter() - t_wall
     clocks = clk.summary()
     step_ms = sum(ms) / len(ms)
-    step_ms_max = max_over_ranks(step_ms, ws)
-    value = ws * T / (step_ms_max / 1000.0)
+    step_ms_max, value = job_throughput(step_ms, ws, T)
 
     prof = profiled_steps(layer, min(args.steps, 16), scratch)
     dom = max(prof.items(), key=lambda kv: kv[1][1])
