@@ -8,6 +8,8 @@
 #include <cuda.h>
 #include <cuda_fp4.h>
 #include <cuda_runtime.h>
+
+#include <utility>
 #include <stdint.h>
 
 #include "../../include/moe_resident.h"
@@ -339,6 +341,31 @@ cudaError_t launch_replan(const unsigned long long* demand, int n, int n_main, i
                           uint32_t* err);
 cudaError_t launch_ring_install(int32_t* slot_of, int32_t* owner, int ring_slot, int flat, cudaStream_t s,
                                 uint32_t* err);
+
+// Programmatic dependent launch. Every kernel of the library is launched with
+// moe_launch (programmatic stream serialisation allowed) and starts with
+// pdl_trigger() then, after any prologue that touches no input, pdl_wait()
+// before reading anything: so the next kernel on the stream is launched and
+// runs its own prologue while this one finishes, and every kernel still sees
+// all the memory of everything launched before it (each grid completes only
+// after its wait, so completion is transitive down the stream).
+MOE_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+MOE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t moe_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Kernel launch counter kept by abi.cu.
 void moe_count_launches(int n);

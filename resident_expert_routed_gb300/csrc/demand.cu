@@ -25,7 +25,9 @@ __global__ void __launch_bounds__(512) demand_accumulate(const int32_t* __restri
                                                          float* __restrict__ miss_max) {
     extern __shared__ unsigned long long hist[];                 // [E] demand, then [E] miss bits
     uint32_t* mbits = reinterpret_cast<uint32_t*>(hist + E);
+    pdl_trigger();
     for (int e = threadIdx.x; e < E; e += blockDim.x) { hist[e] = 0ull; mbits[e] = 0u; }
+    pdl_wait();
     __syncthreads();
     for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P; p += gridDim.x * blockDim.x) {
         const int e = want_e[p];
@@ -57,6 +59,8 @@ __global__ void __launch_bounds__(1024) hot_miss_select(float* __restrict__ M, i
     __shared__ int count;
     __shared__ int n_cand;
     __shared__ unsigned long long cand[MAX_CAND];
+    pdl_trigger();
+    pdl_wait();
     if (threadIdx.x == 0) { picked = ~0ull; count = 0; n_cand = 0; }
     __syncthreads();
     // usual case: few shares pass the threshold; rank them directly by their keys (all distinct)
@@ -133,18 +137,19 @@ cudaError_t launch_demand(const int32_t* want_e, const float* want_s, const int3
     if (grid > 2 * moe_sm_count()) grid = 2 * moe_sm_count();
     const size_t smem = (size_t)E * (sizeof(unsigned long long) + sizeof(uint32_t));
     moe_prof_begin(MK_DEMAND, s);
-    demand_accumulate<<<grid, 512, smem, s>>>(want_e, want_s, slot_of, P, E, demand + (size_t)layer * E,
-                                              miss_max + (size_t)layer * E);
+    const cudaError_t e = moe_launch(demand_accumulate, dim3(grid), dim3(512), smem, s, want_e, want_s, slot_of, P,
+                                     E, demand + (size_t)layer * E, miss_max + (size_t)layer * E);
     moe_prof_end(MK_DEMAND, s);
     moe_count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_hot_miss(float* miss_max, int n, float threshold, int cap, int32_t* out_flat, float* out_share,
                             int32_t* n_out, cudaStream_t s) {
     moe_prof_begin(MK_HOT_MISS, s);
-    hot_miss_select<<<1, 1024, 0, s>>>(miss_max, n, threshold, cap, out_flat, out_share, n_out);
+    const cudaError_t e = moe_launch(hot_miss_select, dim3(1), dim3(1024), 0, s, miss_max, n, threshold, cap,
+                                     out_flat, out_share, n_out);
     moe_prof_end(MK_HOT_MISS, s);
     moe_count_launches(1);
-    return cudaGetLastError();
+    return e;
 }

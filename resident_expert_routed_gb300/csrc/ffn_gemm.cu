@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sfull[s], 4); }
         for (int b = 0; b < NBUF; ++b) { mbar_init(&accf[b], 1); mbar_init(&acce[b], 4); }
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    pdl_wait();                                      // the work list is the plan kernel's output
     const int n_items = *a.n_work * a.m_tiles;
     const int nc = (a.K + 255) / 256;                 // 256-element chunks along K
     const int nst = (nc + KCH - 1) / KCH;             // pipeline stages per item
@@ -288,6 +290,16 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             const int pos0 = w.y, nv = w.z;
             const int b = (int)(j % NBUF);
             const uint32_t u = j / NBUF;
+            // down: the picks of the tile's columns, fetched before the accumulator is ready
+            // (lane l holds column 32 q + l in pp[q])
+            int pp[BN / 32 > 0 ? BN / 32 : 1];
+            if (MODE == 2) {
+#pragma unroll
+                for (int q = 0; q * 32 < BN; ++q) {
+                    const int col = q * 32 + lane;
+                    pp[q] = col < nv ? a.pair_of_pos[pos0 + col] : 0;
+                }
+            }
             if (!warp_wait(&accf[b], u & 1, abort_flag)) break;
             tc_fence_after();
             const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16) + b * C::ACC_COLS;
@@ -322,16 +334,19 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     }
                 }
             } else {
-                const int dr = mt * 128 + warp * 32 + lane;
-                for (int c0 = 0; c0 < nv; c0 += 16) {
+                // lane = output dim dr; each column is one pick: a warp stores 128 contiguous bytes of Y
+                float* ycol = a.Y + mt * 128 + warp * 32 + lane;
+#pragma unroll
+                for (int c0 = 0; c0 < BN; c0 += 16) {
+                    if (c0 >= nv) break;                                      // warp-uniform
                     uint32_t v[16];
                     tc_ld_x16(trow + c0, v);
                     tc_wait_ld();
-                    const int myp = (lane < 16 && c0 + lane < nv) ? a.pair_of_pos[pos0 + c0 + lane] : 0;
+                    const int q = c0 / 32;          // compile-time after unrolling
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int pp = __shfl_sync(0xFFFFFFFFu, myp, i);
-                        if (c0 + i < nv) a.Y[(size_t)pp * a.d + dr] = __uint_as_float(v[i]);
+                        const int pick = __shfl_sync(0xFFFFFFFFu, BN >= 32 ? pp[q] : pp[0], (c0 % 32) + i);
+                        if (c0 + i < nv) ycol[(size_t)pick * a.d] = __uint_as_float(v[i]);
                     }
                 }
             }
@@ -367,7 +382,9 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
 // beside the MMAs; they signal the MMA thread through sfull[stage].
 template <int NS>
 struct CfgTok {
-    static constexpr int THREADS = 320;                 // warps 0-3 epilogue, 4 TMA, 5 MMA, 6-9 scales
+    // warps 0-3 and 10-13 epilogue (feature blocks 0-1 and 2-3 of their lane quadrant), 4 TMA, 5 MMA,
+    // 6-9 scales
+    static constexpr int THREADS = 448;
     static constexpr int BLK = 128 * 128;
     static constexpr int A_BYTES = BLK;                 // 128 activation rows x 256 e2m1
     static constexpr int B_BYTES = 2 * BLK;             // gate block, up block (256 rows)
@@ -386,7 +403,7 @@ struct CfgTok {
 };
 
 template <int NS>
-__global__ void __launch_bounds__(320, 1) ffn_gate_up_tokens_kernel(const __grid_constant__ GemmMaps maps,
+__global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid_constant__ GemmMaps maps,
                                                                     const GemmArgs a) {
     using C = CfgTok<NS>;
     constexpr int BN = 128;
@@ -401,10 +418,11 @@ __global__ void __launch_bounds__(320, 1) ffn_gate_up_tokens_kernel(const __grid
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sfull[s], 4); }
         mbar_init(accf, 1);
-        mbar_init(acce, 4);
+        mbar_init(acce, 8);
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&maps.b[3]);
@@ -415,6 +433,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gate_up_tokens_kernel(const __grid
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    pdl_wait();                                      // the work list is the plan kernel's output
     const int n_items = *a.n_work * a.m_tiles;
     const int nc = (a.K + 255) / 256;
     const int atoms = a.K / 128;
@@ -477,7 +496,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gate_up_tokens_kernel(const __grid
                 if (ok_run) tc_commit(accf);
             }
         }
-    } else if (warp >= 6) {
+    } else if (warp >= 6 && warp < 10) {
         // ------------------------------------------------------------ scale factors -> TMEM
         // stage g of this CTA is K chunk g % nc of its item g / nc; atoms in column
         // order: activations q = 0, 1, then (gate, up) per q
@@ -515,10 +534,12 @@ __global__ void __launch_bounds__(320, 1) ffn_gate_up_tokens_kernel(const __grid
             const int pos0 = w.y, nv = w.z;
             if (!warp_wait(accf, j & 1, abort_flag)) break;
             tc_fence_after();
-            const int row = warp * 32 + lane;
+            const int quad = warp & 3;                              // TMEM lane quadrant of this warp
+            const int row = quad * 32 + lane;
             const int pos = pos0 + row;
-            const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-            for (int fb = 0; fb < 4; ++fb) {                        // 4 blocks of 32 features
+            const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+            const int fb0 = warp < 4 ? 0 : 2;
+            for (int fb = fb0; fb < fb0 + 2; ++fb) {                // 2 of the 4 blocks of 32 features
                 uint32_t g0[16], g1[16], u0[16], u1[16];
                 tc_ld_x16(trow + 32 * fb, g0);
                 tc_ld_x16(trow + 32 * fb + 16, g1);
@@ -620,10 +641,10 @@ cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& g, long max_items, 
     long grid = (long)occ * moe_sm_count();
     if (grid > max_items) grid = max_items;
     moe_prof_begin(MODE == 1 ? MK_GEMM_GATE_UP : MK_GEMM_DOWN, s);
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM, s>>>(maps, g);
+    const cudaError_t e = moe_launch(kern, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, s, maps, g);
     moe_prof_end(MODE == 1 ? MK_GEMM_GATE_UP : MK_GEMM_DOWN, s);
     moe_count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 template <int NS>
@@ -642,10 +663,10 @@ cudaError_t launch_tokens(const GemmMaps& maps, const GemmArgs& g, long max_item
     long grid = moe_sm_count();                    // one CTA per SM (TMEM: 512 columns each)
     if (grid > max_items) grid = max_items;
     moe_prof_begin(MK_GEMM_GATE_UP, s);
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM, s>>>(maps, g);
+    const cudaError_t e = moe_launch(kern, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, s, maps, g);
     moe_prof_end(MK_GEMM_GATE_UP, s);
     moe_count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 template <int MODE>

@@ -33,7 +33,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restri
     extern __shared__ int32_t cnt[];
     __shared__ unsigned long long scan_scratch[32];
     const int tid = threadIdx.x;
+    pdl_trigger();
     for (int i = tid; i < S; i += PLAN_THREADS) cnt[i] = 0;
+    pdl_wait();
     __syncthreads();
     for (int p = tid; p < P; p += PLAN_THREADS) {
         int s = sel_slot[p];
@@ -74,44 +76,38 @@ __global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restri
     }
 }
 
-// One thread per (token, 128-element group): the token's 256 bytes of bf16
-// are quantised once (not once per pick), then the 64 bytes of codes go to
-// the operand row of each of the token's picks and the group's four scale
-// bytes (adjacent in the tile's atom) to its atom as one 4-byte store.
+// One thread per (token, 32-element block): the token's 64 bytes of bf16 are
+// quantised once (not once per pick), then the 16 bytes of codes go to the
+// operand row of each of the token's picks and the block's scale byte to its
+// place in the tile's scale atom.
 __global__ void __launch_bounds__(256) ffn_pack(const uint16_t* __restrict__ x, const int32_t* __restrict__ pos_of_pair,
                                                 int T, int k, int d, int bn, uint8_t* __restrict__ xp,
                                                 uint8_t* __restrict__ xsp) {
-    const int ng = d / 128;
-    const long total = (long)T * ng;
+    pdl_trigger();
+    pdl_wait();
+    const int nb = d / 32;
+    const long total = (long)T * nb;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
-        const long t = i / ng;
-        const int g = (int)(i % ng);
-        uint4 codes[4];
-        uint32_t scales = 0;
+        const long t = i / nb;
+        const int b = (int)(i % nb);
+        const uint4* src = reinterpret_cast<const uint4*>(x + t * d + b * 32);
+        uint4 v[4];
 #pragma unroll
-        for (int b4 = 0; b4 < 4; ++b4) {
-            const int b = g * 4 + b4;
-            const uint4* src = reinterpret_cast<const uint4*>(x + t * d + b * 32);
-            uint4 v[4];
+        for (int q = 0; q < 4; ++q) v[q] = src[q];
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(v);
+        float f[32];
+        float amax = 0.0f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) v[q] = src[q];
-            const uint16_t* h = reinterpret_cast<const uint16_t*>(v);
-            float f[32];
-            float amax = 0.0f;
-#pragma unroll
-            for (int q = 0; q < 32; ++q) { f[q] = bf16_bits_to_float(h[q]); amax = fmaxf(amax, fabsf(f[q])); }
-            const int X = mx_shared_exp(amax);
-            const float inv = exp2_int(-X);
-            codes[b4] = make_uint4(e2m1x8(f, inv), e2m1x8(f + 8, inv), e2m1x8(f + 16, inv), e2m1x8(f + 24, inv));
-            scales |= (uint32_t)(X + 127) << (8 * b4);
-        }
+        for (int q = 0; q < 32; ++q) { f[q] = bf16_bits_to_float(h[q]); amax = fmaxf(amax, fabsf(f[q])); }
+        const int X = mx_shared_exp(amax);
+        const float inv = exp2_int(-X);
+        const uint4 codes = make_uint4(e2m1x8(f, inv), e2m1x8(f + 8, inv), e2m1x8(f + 16, inv), e2m1x8(f + 24, inv));
+        const uint8_t scale = (uint8_t)(X + 127);
         for (int j = 0; j < k; ++j) {
             const int pos = pos_of_pair[t * k + j];
             if (pos < 0) continue;
-            uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)pos * (d / 2) + g * 64);
-#pragma unroll
-            for (int b4 = 0; b4 < 4; ++b4) dst[b4] = codes[b4];
-            *reinterpret_cast<uint32_t*>(xsp + operand_scale_offset(pos, g * 4, bn, d)) = scales;
+            *reinterpret_cast<uint4*>(xp + (size_t)pos * (d / 2) + b * 16) = codes;
+            xsp[operand_scale_offset(pos, b, bn, d)] = scale;
         }
     }
 }
@@ -119,6 +115,8 @@ __global__ void __launch_bounds__(256) ffn_pack(const uint16_t* __restrict__ x, 
 __global__ void __launch_bounds__(256) ffn_combine(const float* __restrict__ Y, const int32_t* __restrict__ sel_slot,
                                                    const float* __restrict__ sel_w, int k, int d, int S,
                                                    float* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x;
     const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
     if (c >= d) return;
@@ -150,26 +148,27 @@ cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
         attr_set[dev] = true;
     }
     moe_prof_begin(MK_PLAN, s);
-    ffn_plan<<<1, PLAN_THREADS, smem, s>>>(a.sel_slot, P, a.S, a.bn, a.pos_of_pair, a.pair_of_pos, a.seg, a.tile_off,
-                                           a.work, a.n_work, a.err);
+    cudaError_t e = moe_launch(ffn_plan, dim3(1), dim3(PLAN_THREADS), smem, s, a.sel_slot, P, a.S, a.bn,
+                               a.pos_of_pair, a.pair_of_pos, a.seg, a.tile_off, a.work, a.n_work, a.err);
     moe_prof_end(MK_PLAN, s);
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const long tasks = (long)a.T * (a.d / 128);
+    const long tasks = (long)a.T * (a.d / 32);
     long blocks = (tasks + 255) / 256;
     if (blocks > 8L * moe_sm_count()) blocks = 8L * moe_sm_count();
     moe_prof_begin(MK_PACK, s);
-    ffn_pack<<<(unsigned)blocks, 256, 0, s>>>(a.x, a.pos_of_pair, a.T, a.k, a.d, a.bn, a.xp, a.xsp);
+    e = moe_launch(ffn_pack, dim3((unsigned)blocks), dim3(256), 0, s, a.x, a.pos_of_pair, a.T, a.k, a.d, a.bn,
+                   a.xp, a.xsp);
     moe_prof_end(MK_PACK, s);
     moe_count_launches(2);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_ffn_combine(const FfnLaunch& a, cudaStream_t s) {
     dim3 g(a.T, (a.d / 4 + 255) / 256);
     moe_prof_begin(MK_COMBINE, s);
-    ffn_combine<<<g, 256, 0, s>>>(a.Y, a.sel_slot, a.sel_w, a.k, a.d, a.S, a.out);
+    const cudaError_t e = moe_launch(ffn_combine, g, dim3(256), 0, s, a.Y, a.sel_slot, a.sel_w, a.k, a.d, a.S,
+                                     a.out);
     moe_prof_end(MK_COMBINE, s);
     moe_count_launches(1);
-    return cudaGetLastError();
+    return e;
 }

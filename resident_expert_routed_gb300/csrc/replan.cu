@@ -46,6 +46,8 @@ __global__ void __launch_bounds__(RP_THREADS) arena_replan(const unsigned long l
                                                            int32_t* __restrict__ free_list, uint32_t* err) {
     __shared__ unsigned long long part[RP_THREADS];
     __shared__ int bad;
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x;
     if (tid == 0) bad = 0;
     __syncthreads();
@@ -137,6 +139,8 @@ __global__ void __launch_bounds__(RP_THREADS) arena_replan(const unsigned long l
 }
 
 __global__ void ring_install(int32_t* slot_of, int32_t* owner, int ring_slot, int flat, uint32_t* err) {
+    pdl_trigger();
+    pdl_wait();
     if (slot_of[flat] >= 0) { record_error(err, MOE_DEV_RESIDENT); return; }
     const int old = owner[ring_slot];
     if (old >= 0) slot_of[old] = -1;
@@ -163,18 +167,18 @@ cudaError_t launch_replan(const unsigned long long* demand, int n, int n_main, i
     int32_t* flag = reinterpret_cast<int32_t*>(p + (size_t)n2 * 12);
     int32_t* free_list = flag + n;
     moe_prof_begin(MK_REPLAN, s);
-    arena_replan<<<1, RP_THREADS, 0, s>>>(demand, n, n2, n_main, n_slots, slot_of, owner, loads, n_loads, kd, ks, flag,
-                                          free_list, err);
+    const cudaError_t e = moe_launch(arena_replan, dim3(1), dim3(RP_THREADS), 0, s, demand, n, n2, n_main, n_slots,
+                                     slot_of, owner, loads, n_loads, kd, ks, flag, free_list, err);
     moe_prof_end(MK_REPLAN, s);
     moe_count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_ring_install(int32_t* slot_of, int32_t* owner, int ring_slot, int flat, cudaStream_t s,
                                 uint32_t* err) {
     moe_prof_begin(MK_RING, s);
-    ring_install<<<1, 1, 0, s>>>(slot_of, owner, ring_slot, flat, err);
+    const cudaError_t e = moe_launch(ring_install, dim3(1), dim3(1), 0, s, slot_of, owner, ring_slot, flat, err);
     moe_prof_end(MK_RING, s);
     moe_count_launches(1);
-    return cudaGetLastError();
+    return e;
 }

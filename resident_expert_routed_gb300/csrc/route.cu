@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256) router_logits_partial(const uint16_t* __r
                                                              int kslice, float* __restrict__ partial) {
     __shared__ float xs[BK][BT + 4];
     __shared__ float ws[BK][BE + 4];
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x;
     const int tx = tid & 15, ty = tid >> 4;       // 16 x 16 threads, 4 x 4 outputs each
     const int e0 = blockIdx.x * BE, t0 = blockIdx.y * BT;
@@ -95,48 +97,18 @@ __device__ __forceinline__ void warp_argmax(float& v, int& idx) {
     }
 }
 
+// Bias, softmax over all E, wanted top-k over all experts and resident top-k,
+// for one token whose summed logits lg[i] (expert lane + 32 i) one warp holds.
+// Order by logit (monotone in the score), ties to the lower expert index.
 template <int VPL>
-__global__ void __launch_bounds__(256) route_select(const float* __restrict__ partial, int splits,
-                                                    const float* __restrict__ bias,
-                                                    const int32_t* __restrict__ slot_of, int T, int E, int k,
-                                                    int32_t* __restrict__ want_e, float* __restrict__ want_s,
-                                                    int32_t* __restrict__ sel_e, int32_t* __restrict__ sel_slot,
-                                                    float* __restrict__ sel_w) {
+__device__ __forceinline__ void select_token(float (&lg)[VPL], int t, const float* __restrict__ bias,
+                                             const int32_t* __restrict__ slot_of, int E, int k,
+                                             int32_t* __restrict__ want_e, float* __restrict__ want_s,
+                                             int32_t* __restrict__ sel_e, int32_t* __restrict__ sel_slot,
+                                             float* __restrict__ sel_w) {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= T) return;
     const float NEG = -__int_as_float(0x7F800000);   // -inf
-    float lg[VPL];
     int slot[VPL];
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) lg[i] = 0.0f;
-    // K slices summed in slice order (deterministic); U slices' loads are issued together
-    constexpr int U = VPL >= 16 ? 1 : 64 / (VPL * 2);
-    int zs = 0;
-    for (; zs + U <= splits; zs += U) {
-        float v[U][VPL];
-#pragma unroll
-        for (int q = 0; q < U; ++q) {
-            const float* pz = partial + ((size_t)(zs + q) * T + t) * E;
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                const int e = lane + 32 * i;
-                v[q][i] = e < E ? pz[e] : 0.0f;
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < U; ++q)
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) lg[i] += v[q][i];
-    }
-    for (; zs < splits; ++zs) {
-        const float* pz = partial + ((size_t)zs * T + t) * E;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E) lg[i] += pz[e];
-        }
-    }
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
         const int e = lane + 32 * i;
@@ -162,8 +134,6 @@ __global__ void __launch_bounds__(256) route_select(const float* __restrict__ pa
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
     const float inv_z = 1.0f / z;
 
-    // wanted top-k over all experts, then resident top-k; order by logit
-    // (monotone in the score), ties to the lower expert index.
     for (int pass = 0; pass < 2; ++pass) {
         uint32_t taken = 0;
         for (int j = 0; j < k; ++j) {
@@ -197,6 +167,92 @@ __global__ void __launch_bounds__(256) route_select(const float* __restrict__ pa
     }
 }
 
+// One warp per token (few K slices): the slices are summed in slice order;
+// U slices' loads are issued together.
+template <int VPL>
+__global__ void __launch_bounds__(256) route_select(const float* __restrict__ partial, int splits,
+                                                    const float* __restrict__ bias,
+                                                    const int32_t* __restrict__ slot_of, int T, int E, int k,
+                                                    int32_t* __restrict__ want_e, float* __restrict__ want_s,
+                                                    int32_t* __restrict__ sel_e, int32_t* __restrict__ sel_slot,
+                                                    float* __restrict__ sel_w) {
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    float lg[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) lg[i] = 0.0f;
+    constexpr int U = VPL >= 16 ? 1 : 64 / (VPL * 2);
+    int zs = 0;
+    for (; zs + U <= splits; zs += U) {
+        float v[U][VPL];
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const float* pz = partial + ((size_t)(zs + q) * T + t) * E;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                const int e = lane + 32 * i;
+                v[q][i] = e < E ? pz[e] : 0.0f;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < U; ++q)
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) lg[i] += v[q][i];
+    }
+    for (; zs < splits; ++zs) {
+        const float* pz = partial + ((size_t)zs * T + t) * E;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) lg[i] += pz[e];
+        }
+    }
+    select_token<VPL>(lg, t, bias, slot_of, E, k, want_e, want_s, sel_e, sel_slot, sel_w);
+}
+
+// One CTA of 8 warps per token (many K slices, small batches): warp w sums
+// slices w, w + 8, ... in order; warp 0 adds the eight sums in warp order and
+// selects. One round of independent loads instead of a chain per token.
+template <int VPL>
+__global__ void __launch_bounds__(256) route_select_cta(const float* __restrict__ partial, int splits,
+                                                        const float* __restrict__ bias,
+                                                        const int32_t* __restrict__ slot_of, int T, int E, int k,
+                                                        int32_t* __restrict__ want_e, float* __restrict__ want_s,
+                                                        int32_t* __restrict__ sel_e, int32_t* __restrict__ sel_slot,
+                                                        float* __restrict__ sel_w) {
+    __shared__ float part[8][VPL * 32];
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x;
+    float acc[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) acc[i] = 0.0f;
+    for (int z = warp; z < splits; z += 8) {
+        const float* pz = partial + ((size_t)z * T + t) * E;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) acc[i] += pz[e];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) part[warp][lane + 32 * i] = acc[i];
+    __syncthreads();
+    if (warp != 0) return;
+    float lg[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        lg[i] = part[0][lane + 32 * i];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) lg[i] += part[w][lane + 32 * i];
+    }
+    select_token<VPL>(lg, t, bias, slot_of, E, k, want_e, want_s, sel_e, sel_slot, sel_w);
+}
+
 }  // namespace
 
 int route_splits(int T, int E, int d) {
@@ -214,28 +270,29 @@ cudaError_t launch_route(const RouteLaunch& a, cudaStream_t s) {
     } else {
         dim3 g1((a.E + BE - 1) / BE, (a.T + BT - 1) / BT, a.splits);
         moe_prof_begin(MK_ROUTER_LOGITS, s);
-        router_logits_partial<<<g1, 256, 0, s>>>(a.x, a.w, a.T, a.d, a.E, a.d / a.splits, a.partial);
+        e = moe_launch(router_logits_partial, g1, dim3(256), 0, s, a.x, a.w, a.T, a.d, a.E, a.d / a.splits,
+                       a.partial);
         moe_prof_end(MK_ROUTER_LOGITS, s);
         moe_count_launches(1);
-        e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
     const int vpl = (a.E + 31) / 32;
-    dim3 g2((a.T + 7) / 8);
+    const bool per_cta = a.splits >= 8;             // many K slices: one CTA per token
+    dim3 g2(per_cta ? a.T : (a.T + 7) / 8);
 #define MOE_SEL(V)                                                                                       \
-    route_select<V><<<g2, 256, 0, s>>>(a.partial, a.splits, a.bias, a.slot_of, a.T, a.E, a.k, a.want_e, \
-                                       a.want_s, a.sel_e, a.sel_slot, a.sel_w)
+    moe_launch(per_cta ? route_select_cta<V> : route_select<V>, g2, dim3(256), 0, s, a.partial, a.splits, \
+               a.bias, a.slot_of, a.T, a.E, a.k, a.want_e, a.want_s, a.sel_e, a.sel_slot, a.sel_w)
     moe_prof_begin(MK_ROUTE_SELECT, s);
-    if (vpl <= 1) MOE_SEL(1);
-    else if (vpl <= 2) MOE_SEL(2);
-    else if (vpl <= 4) MOE_SEL(4);
-    else if (vpl <= 8) MOE_SEL(8);
-    else if (vpl <= 16) MOE_SEL(16);
-    else MOE_SEL(32);
+    if (vpl <= 1) e = MOE_SEL(1);
+    else if (vpl <= 2) e = MOE_SEL(2);
+    else if (vpl <= 4) e = MOE_SEL(4);
+    else if (vpl <= 8) e = MOE_SEL(8);
+    else if (vpl <= 16) e = MOE_SEL(16);
+    else e = MOE_SEL(32);
 #undef MOE_SEL
     moe_prof_end(MK_ROUTE_SELECT, s);
     moe_count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 // ------------------------------------------------------------------ routing without a caller workspace

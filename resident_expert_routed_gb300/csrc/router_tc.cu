@@ -45,6 +45,8 @@ constexpr int RT_SMEM = RT_NS * RT_STAGE + (2 * RT_NS + 4) * 8 + 16 + 1024;
 __global__ void __launch_bounds__(256) split_router_weights(const float* __restrict__ W, long n,
                                                             __nv_bfloat16* __restrict__ w1, __nv_bfloat16* __restrict__ w2,
                                                             __nv_bfloat16* __restrict__ w3) {
+    pdl_trigger();
+    pdl_wait();
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
         const float w = W[i];
         const __nv_bfloat16 a = __float2bfloat16_rn(w);
@@ -89,6 +91,7 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc(const __grid_constant
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * 128, e0 = blockIdx.y * 128, z = blockIdx.z;
+    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < RT_NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 128); }
@@ -101,6 +104,7 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc(const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();
     const uint32_t tmem = *tmem_slot;
     const int kc0 = z * kchunks;
     const int n_epochs = (kchunks + RT_EPOCH - 1) / RT_EPOCH;
@@ -232,9 +236,11 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* W, int T, int d, in
     long blocks = (n + 255) / 256;
     if (blocks > 4L * moe_sm_count()) blocks = 4L * moe_sm_count();
     moe_prof_begin(MK_ROUTER_LOGITS, s);
-    split_router_weights<<<(unsigned)blocks, 256, 0, s>>>(W, n, w1, w1 + n, w1 + 2 * n);
+    cudaError_t e = moe_launch(split_router_weights, dim3((unsigned)blocks), dim3(256), 0, s, W, n, w1, w1 + n,
+                               w1 + 2 * n);
+    if (e != cudaSuccess) return e;
     RouterMaps maps;
-    cudaError_t e = bf16_map(&maps.x, x, (uint64_t)d, (uint64_t)T);
+    e = bf16_map(&maps.x, x, (uint64_t)d, (uint64_t)T);
     if (e == cudaSuccess) e = bf16_map(&maps.w, w1, (uint64_t)d, (uint64_t)3 * E);
     if (e != cudaSuccess) return e;
     static bool attr_set[64] = {};
@@ -246,8 +252,8 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* W, int T, int d, in
         attr_set[dev] = true;
     }
     dim3 grid((T + 127) / 128, (E + 127) / 128, splits);
-    router_logits_tc<<<grid, 192, RT_SMEM, s>>>(maps, T, E, (d / 64) / splits, partial, err);
+    e = moe_launch(router_logits_tc, grid, dim3(192), RT_SMEM, s, maps, T, E, (d / 64) / splits, partial, err);
     moe_prof_end(MK_ROUTER_LOGITS, s);
     moe_count_launches(2);
-    return cudaGetLastError();
+    return e;
 }
