@@ -58,6 +58,7 @@ def _declare(L):
     L.or_topk.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]
     L.or_demand.argtypes = [_P, _P, _P, _I, _I, _I, _I, _P, _P]
     L.or_hot_miss_select.argtypes = [_P, _I, _I, _D, _I, _P, _P, _P]
+    L.or_demand_decay_fixed.argtypes = [_P, ctypes.c_int64, _D]
     L.or_expert_pair.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
     L.or_ffn.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]
     L.or_replan.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P]
@@ -146,6 +147,13 @@ def demand(want_e, want_s, slot_of, layer: int, D: np.ndarray, M: np.ndarray) ->
     T, k = we.shape
     E = D.shape[-1]
     lib().or_demand(_ptr(we), _ptr(ws), _ptr(so), T, k, layer, E, _ptr(D), _ptr(M))
+
+
+def demand_decay_fixed(D: np.ndarray, factor: float) -> np.ndarray:
+    """The stored demand table (uint64, units of 2^-40) after forgetting with `factor` (a new array)."""
+    out = np.ascontiguousarray(D, dtype=np.uint64).copy()
+    lib().or_demand_decay_fixed(_ptr(out), out.size, float(factor))
+    return out
 
 
 def hot_miss_select(M: np.ndarray, threshold: float = 0.2, cap: int = 16):

@@ -190,6 +190,17 @@ void or_demand(const int32_t* want_e, const double* want_s, const int32_t* slot_
         }
 }
 
+// Forgetting in the demand history (README "Settings worth knowing": the
+// adaptation setting sets "how fast the resident set follows new traffic"; no
+// formula is given). Reading: exponential decay applied between re-plans to
+// the stored table, which keeps demand as an integer count of 2^-40 units.
+// The factor is rounded to a multiple of 2^-32 (ties to even) and each entry
+// becomes the floor of its exact product with it.
+void or_demand_decay_fixed(uint64_t* D, int64_t n, double factor) {
+    const unsigned __int128 q = (unsigned __int128)std::nearbyint(factor * 4294967296.0);
+    for (int64_t i = 0; i < n; ++i) D[i] = (uint64_t)(((unsigned __int128)D[i] * q) >> 32);
+}
+
 // Heavy misses (README item 3: "the heaviest misses"; ">= 0.2 of the routing
 // weight, at most 16 a step"). Candidates are the (layer, expert) with
 // M >= threshold, ordered by M descending then flat index ascending; the first

@@ -417,3 +417,29 @@ def test_ring_install():
     assert list(owner) == [0, -1, -1, 1, 2] and slot_of[3] == -1 and slot_of[2] == 4
     assert oracle.ring_install(slot_of, owner, 3, 0) == 1      # already resident: no change
     assert list(owner) == [0, -1, -1, 1, 2]
+
+
+# ------------------------------------------------------------------ demand forgetting (fixed point)
+
+def test_demand_decay_identity_zero_and_shifts():
+    rng = np.random.default_rng(5)
+    D = np.concatenate([rng.integers(0, 2**63, 64, dtype=np.uint64),
+                        np.array([0, 1, 2, 3, 2**40, 2**64 - 1], dtype=np.uint64)])
+    assert np.array_equal(oracle.demand_decay_fixed(D, 1.0), D)                 # factor 1: unchanged
+    assert not oracle.demand_decay_fixed(D, 0.0).any()                          # factor 0: forgotten
+    for m in range(1, 12):                                                      # 2^-m: a right shift (floor)
+        assert np.array_equal(oracle.demand_decay_fixed(D, 2.0 ** -m), D >> np.uint64(m)), m
+
+
+def test_demand_decay_tracks_the_real_product():
+    rng = np.random.default_rng(6)
+    D = rng.integers(0, 2**62, 200, dtype=np.uint64)
+    prev = np.zeros_like(D)
+    for f in (0.001, 0.1, 0.3, 0.5, 0.7, 0.9, 0.99, 0.999999):
+        got = oracle.demand_decay_fixed(D, np.float32(f))
+        for d, g in zip(D.tolist(), got.tolist()):
+            exact = d * float(np.float32(f))
+            # factor rounded to a multiple of 2^-32, then floor: within 1 + d * 2^-33 of d * f
+            assert abs(g - exact) <= 1 + d * 2.0 ** -33 + exact * 1e-15
+        assert np.all(got >= prev)                                                # monotone in the factor
+        prev = got
