@@ -48,7 +48,8 @@ typedef enum {
     MOE_ENOMEM = 3,        /* workspace smaller than the matching *_workspace_bytes() */
     MOE_ETIMEOUT = 4,      /* device error word: a bounded wait in a kernel ran out */
     MOE_EDEVICE = 5,       /* device error word: bad slot id / NaN scale / bad table */
-    MOE_EUNSUPPORTED = 6   /* a size past a documented limit */
+    MOE_EUNSUPPORTED = 6,  /* a size past a documented limit */
+    MOE_EIO = 7            /* a file could not be read or written (demand history) */
 } moe_status;
 
 /* Bits of the device error word (moe_device_status). */
@@ -234,6 +235,35 @@ moe_status moe_ring_install(int32_t* slot_of, int32_t* owner, int ring_slot, int
 /* Workspace sizes (bytes) for the calls above. */
 size_t moe_workspace_bytes(int T, int k, int d, int ffn, int E, int n_slots);
 size_t moe_replan_workspace_bytes(int L, int E);
+
+/*
+ * Forgetting in the demand history (README "Settings worth knowing": the
+ * adaptation setting decides "how fast the resident set follows new traffic";
+ * the pages give no formula). Reading: the caller applies an exponential
+ * decay between re-plans; every entry is scaled exactly in fixed point:
+ *   q = round(factor * 2^32)  (factor in [0, 1]; ties to even)
+ *   demand[i] = floor(demand[i] * q / 2^32)        (128-bit product)
+ * so factor 1 leaves the table unchanged and 0.5 halves it (floor).
+ * demand: device uint64 [n] in units of 2^-40. Bad factor or n < 0: MOE_EINVAL.
+ */
+moe_status moe_demand_decay(uint64_t* demand, int64_t n, float factor, void* stream);
+
+/*
+ * Persistence of the demand history (README item 1: the history "persists
+ * across restarts"; "Settings worth knowing": the engine keeps it in a state
+ * database). File format, little-endian:
+ *   bytes 0-7   magic "MOEDEMD1"
+ *   bytes 8-15  int32 L, int32 E
+ *   bytes 16-23 int32 fraction bits (40), int32 0
+ *   then L*E uint64 demand values, row-major [L, E], in units of 2^-40.
+ * demand: device uint64 [L, E]. Both calls order their copy on `stream` and
+ * synchronise it (host I/O). save writes `path` whole (a temporary file
+ * renamed over it). load checks the header against L and E (MOE_EINVAL on a
+ * mismatch or a bad magic) before touching the device; I/O errors give
+ * MOE_EIO.
+ */
+moe_status moe_demand_save(const uint64_t* demand, int L, int E, const char* path, void* stream);
+moe_status moe_demand_load(uint64_t* demand, int L, int E, const char* path, void* stream);
 
 /*
  * Reads and clears the current device's error word (synchronises `stream`).

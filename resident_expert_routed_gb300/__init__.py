@@ -23,14 +23,15 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe_resident.so")
 
-MOE_OK, MOE_EINVAL, MOE_ECUDA, MOE_ENOMEM, MOE_ETIMEOUT, MOE_EDEVICE, MOE_EUNSUPPORTED = range(7)
+MOE_OK, MOE_EINVAL, MOE_ECUDA, MOE_ENOMEM, MOE_ETIMEOUT, MOE_EDEVICE, MOE_EUNSUPPORTED, MOE_EIO = range(8)
 MOE_DEV_BAD_SLOT, MOE_DEV_NAN_SCALE, MOE_DEV_TIMEOUT, MOE_DEV_BAD_TABLE, MOE_DEV_RESIDENT = 0x1, 0x2, 0x4, 0x8, 0x10
 
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accumulate", "moe_hot_miss_select", "moe_expert_ffn_mxfp4",
            "moe_arena_replan", "moe_ring_install", "moe_workspace_bytes", "moe_replan_workspace_bytes",
            "moe_device_status", "moe_status_str", "moe_kernel_launches", "moe_profile_enable",
-           "moe_profile_kernel_count", "moe_profile_read", "moe_profile_reset")
+           "moe_profile_kernel_count", "moe_profile_read", "moe_profile_reset", "moe_demand_decay",
+           "moe_demand_save", "moe_demand_load")
 
 
 class MoeError(RuntimeError):
@@ -82,10 +83,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                    ctypes.POINTER(ctypes.c_double)]
     L.moe_profile_reset.restype = None
     L.moe_profile_reset.argtypes = []
+    L.moe_demand_decay.argtypes = [_P, ctypes.c_int64, _F, _P]
+    L.moe_demand_save.argtypes = [_P, _I, _I, ctypes.c_char_p, _P]
+    L.moe_demand_load.argtypes = [_P, _I, _I, ctypes.c_char_p, _P]
     for name in ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accumulate", "moe_hot_miss_select",
                  "moe_expert_ffn_mxfp4",
                  "moe_arena_replan", "moe_ring_install", "moe_device_status", "moe_profile_enable",
-                 "moe_profile_read"):
+                 "moe_profile_read", "moe_demand_decay", "moe_demand_save", "moe_demand_load"):
         L[name].restype = _I
     _lib = L
     return L
@@ -231,3 +235,20 @@ def moe_profile_read() -> dict:
         if n.value:
             out[name.value.decode()] = (n.value, ms.value)
     return out
+
+
+def moe_demand_decay(demand: torch.Tensor, factor: float, stream=None) -> None:
+    """demand int64/uint64 [..] in units of 2^-40, scaled in place by factor in [0, 1] (fixed point, floor)."""
+    _check("moe_demand_decay", load().moe_demand_decay(_ptr(demand), demand.numel(), float(factor), _stream(stream)))
+
+
+def moe_demand_save(demand: torch.Tensor, path: str, stream=None) -> None:
+    """Write the [L, E] demand history to `path` (see the header for the format)."""
+    L, E = demand.shape
+    _check("moe_demand_save", load().moe_demand_save(_ptr(demand), L, E, os.fsencode(path), _stream(stream)))
+
+
+def moe_demand_load(demand: torch.Tensor, path: str, stream=None) -> None:
+    """Read an [L, E] demand history written by moe_demand_save into `demand`."""
+    L, E = demand.shape
+    _check("moe_demand_load", load().moe_demand_load(_ptr(demand), L, E, os.fsencode(path), _stream(stream)))

@@ -53,6 +53,20 @@ def build_library(sources: list[str], lib: str, obj_dir: str, headers: list[str]
     return lib
 
 
+MICROBENCH_SRC = os.path.join(PKG, "microbench", "mma_scale_rate.cu")
+MICROBENCH_BIN = os.path.join(PKG, "microbench", "mma_scale_rate")
+
+
+def build_microbench() -> str:
+    """The tensor-pipe microbenchmark that bench.py runs for the measured FP4 MMA rate."""
+    if _needs(MICROBENCH_BIN, [MICROBENCH_SRC, os.path.join(CSRC, "common.cuh")]):
+        tmp = MICROBENCH_BIN + f".tmp{os.getpid()}"
+        subprocess.check_call([NVCC] + ARCH + ["-O3", "-std=c++17", "-I", os.path.join(ROOT, "include"), "-o", tmp,
+                               MICROBENCH_SRC])
+        os.replace(tmp, MICROBENCH_BIN)
+    return MICROBENCH_BIN
+
+
 def build(verbose_ptxas: bool = False) -> str:
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(ROOT, "include", "moe_resident.h")]

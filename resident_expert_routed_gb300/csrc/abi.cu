@@ -5,7 +5,11 @@
 // in the kernels of route.cu, demand.cu, ffn_plan.cu, ffn_gemm.cu and
 // replan.cu; nothing here computes on the host.
 #include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
 #include <mutex>
+#include <string>
 #include <vector>
 
 #include "common.cuh"
@@ -173,6 +177,7 @@ const char* moe_status_str(moe_status s) {
         case MOE_ETIMEOUT: return "device wait timed out";
         case MOE_EDEVICE: return "device reported bad data (slot id, scale byte or table)";
         case MOE_EUNSUPPORTED: return "size beyond a documented limit";
+        case MOE_EIO: return "file could not be read or written";
     }
     return "unknown status";
 }
@@ -360,3 +365,71 @@ moe_status moe_device_status(void* stream, uint32_t* bits) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ demand history: decay and persistence
+
+moe_status moe_demand_decay(uint64_t* demand, int64_t n, float factor, void* stream) {
+    if (n < 0 || !(factor >= 0.0f && factor <= 1.0f) || (n > 0 && !demand)) return MOE_EINVAL;
+    if (n == 0) return MOE_OK;
+    const unsigned long long q = (unsigned long long)std::nearbyint((double)factor * 4294967296.0);
+    return cuda_status(launch_demand_decay(reinterpret_cast<unsigned long long*>(demand), (long)n, q,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+
+constexpr char kDemandMagic[8] = {'M', 'O', 'E', 'D', 'E', 'M', 'D', '1'};
+
+struct DemandHeader {
+    char magic[8];
+    int32_t L, E, frac_bits, zero;
+};
+static_assert(sizeof(DemandHeader) == 24, "demand file header");
+
+}  // namespace
+
+moe_status moe_demand_save(const uint64_t* demand, int L, int E, const char* path, void* stream) {
+    if (!demand || !path || L < 1 || E < 1) return MOE_EINVAL;
+    const size_t n = (size_t)L * E;
+    std::vector<uint64_t> host(n);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(host.data(), demand, n * sizeof(uint64_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ECUDA;
+    DemandHeader h{};
+    std::memcpy(h.magic, kDemandMagic, 8);
+    h.L = L;
+    h.E = E;
+    h.frac_bits = 40;
+    const std::string tmp = std::string(path) + ".tmp";
+    FILE* f = std::fopen(tmp.c_str(), "wb");
+    if (!f) return MOE_EIO;
+    const bool ok = std::fwrite(&h, sizeof h, 1, f) == 1 && std::fwrite(host.data(), sizeof(uint64_t), n, f) == n;
+    if (std::fclose(f) != 0 || !ok || std::rename(tmp.c_str(), path) != 0) {
+        std::remove(tmp.c_str());
+        return MOE_EIO;
+    }
+    return MOE_OK;
+}
+
+moe_status moe_demand_load(uint64_t* demand, int L, int E, const char* path, void* stream) {
+    if (!demand || !path || L < 1 || E < 1) return MOE_EINVAL;
+    FILE* f = std::fopen(path, "rb");
+    if (!f) return MOE_EIO;
+    DemandHeader h{};
+    if (std::fread(&h, sizeof h, 1, f) != 1) { std::fclose(f); return MOE_EIO; }
+    if (std::memcmp(h.magic, kDemandMagic, 8) != 0 || h.L != L || h.E != E || h.frac_bits != 40) {
+        std::fclose(f);
+        return MOE_EINVAL;
+    }
+    const size_t n = (size_t)L * E;
+    std::vector<uint64_t> host(n);
+    const bool ok = std::fread(host.data(), sizeof(uint64_t), n, f) == n;
+    std::fclose(f);
+    if (!ok) return MOE_EIO;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(demand, host.data(), n * sizeof(uint64_t), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ECUDA;
+    return MOE_OK;
+}

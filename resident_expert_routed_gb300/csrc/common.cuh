@@ -310,6 +310,7 @@ int route_splits(int T, int E, int d);
 
 cudaError_t launch_demand(const int32_t* want_e, const float* want_s, const int32_t* slot_of, int T, int k,
                           int layer, int E, unsigned long long* demand, float* miss_max, cudaStream_t s);
+cudaError_t launch_demand_decay(unsigned long long* demand, long n, unsigned long long q, cudaStream_t s);
 cudaError_t launch_hot_miss(float* miss_max, int n, float threshold, int cap, int32_t* out_flat, float* out_share,
                             int32_t* n_out, cudaStream_t s);
 

@@ -128,7 +128,26 @@ __global__ void __launch_bounds__(1024) hot_miss_select(float* __restrict__ M, i
     for (int f = threadIdx.x; f < n; f += blockDim.x) M[f] = 0.0f;
 }
 
+// demand[i] = floor(demand[i] * q / 2^32) with q <= 2^32 (the product is < 2^96, its high word < 2^32).
+__global__ void __launch_bounds__(256) demand_decay(unsigned long long* __restrict__ D, long n,
+                                                    unsigned long long q) {
+    pdl_trigger();
+    pdl_wait();
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const unsigned long long d = D[i];
+        D[i] = (__umul64hi(d, q) << 32) | ((d * q) >> 32);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_demand_decay(unsigned long long* demand, long n, unsigned long long q, cudaStream_t s) {
+    long blocks = (n + 255) / 256;
+    if (blocks > 4L * moe_sm_count()) blocks = 4L * moe_sm_count();
+    const cudaError_t e = moe_launch(demand_decay, dim3((unsigned)blocks), dim3(256), 0, s, demand, n, q);
+    moe_count_launches(1);
+    return e;
+}
 
 cudaError_t launch_demand(const int32_t* want_e, const float* want_s, const int32_t* slot_of, int T, int k,
                           int layer, int E, unsigned long long* demand, float* miss_max, cudaStream_t s) {

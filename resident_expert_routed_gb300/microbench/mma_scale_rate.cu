@@ -110,18 +110,20 @@ __global__ void __launch_bounds__(160, 1) rate(int n_mma, unsigned long long* ns
 }
 
 template <int MODE>
-void run(const char* name, double flop, int sms, unsigned long long* d_ns) {
+double run(const char* name, double flop, int sms, unsigned long long* d_ns) {
     const int n = 8192;
     cudaFuncSetAttribute(rate<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     for (int w = 0; w < 2; ++w) rate<MODE><<<sms, 160, SMEM>>>(n, d_ns);
-    if (cudaDeviceSynchronize() != cudaSuccess) { printf("%s: launch failed\n", name); return; }
+    if (cudaDeviceSynchronize() != cudaSuccess) { printf("%s: launch failed\n", name); return 0.0; }
     unsigned long long h[1024];
     cudaMemcpy(h, d_ns, sizeof(unsigned long long) * sms, cudaMemcpyDeviceToHost);
     unsigned long long tmax = 0;
     bool timed_out = false;
     for (int b = 0; b < sms; ++b) { tmax = h[b] > tmax ? h[b] : tmax; timed_out |= h[b] == 0; }
-    printf("%-44s %7.1f ns per MMA  %8.1f TFLOP/s over %d SMs%s\n", name, (double)tmax / n,
-           flop * n * sms / (tmax * 1e-9) / 1e12, sms, timed_out ? "  (a wait timed out)" : "");
+    const double tflops = timed_out ? 0.0 : flop * n * sms / (tmax * 1e-9) / 1e12;
+    printf("%-44s %7.1f ns per MMA  %8.1f TFLOP/s over %d SMs%s\n", name, (double)tmax / n, tflops, sms,
+           timed_out ? "  (a wait timed out)" : "");
+    return tflops;
 }
 
 }  // namespace
@@ -133,9 +135,11 @@ int main() {
     unsigned long long* d_ns;
     cudaMalloc(&d_ns, sizeof(unsigned long long) * 1024);
     const double f4 = 128.0 * 256 * 64 * 2, f16 = 128.0 * 256 * 16 * 2;
-    run<0>("mxf4 128x256x64", f4, sms, d_ns);
-    run<1>("mxf4 + 6 tcgen05.cp 32x128b.warpx4 / 4 MMAs", f4, sms, d_ns);
-    run<2>("mxf4 + 4 warps tcgen05.st (24 columns / 4)", f4, sms, d_ns);
-    run<3>("bf16 128x256x16", f16, sms, d_ns);
+    const double a = run<0>("mxf4 128x256x64", f4, sms, d_ns);
+    const double b = run<1>("mxf4 + 6 tcgen05.cp 32x128b.warpx4 / 4 MMAs", f4, sms, d_ns);
+    const double c = run<2>("mxf4 + 4 warps tcgen05.st (24 columns / 4)", f4, sms, d_ns);
+    const double e = run<3>("bf16 128x256x16", f16, sms, d_ns);
+    printf("{\"mxf4_tflops\": %.1f, \"mxf4_with_scale_copies_tflops\": %.1f, \"mxf4_with_scale_stores_tflops\": %.1f, "
+           "\"bf16_tflops\": %.1f, \"sms\": %d}\n", a, b, c, e, sms);
     return 0;
 }

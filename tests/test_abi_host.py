@@ -137,3 +137,23 @@ def test_package_has_no_cpu_fallback():
     x = torch.zeros((2, 64), dtype=torch.int16)
     with pytest.raises(ValueError):
         moe._ptr(x)
+
+
+def test_demand_history_calls_reject_bad_arguments(tmp_path):
+    L = moe.load()
+    assert L.moe_demand_decay(FAKE, 16, ctypes.c_float(1.5), NULL) == moe.MOE_EINVAL     # factor above 1
+    assert L.moe_demand_decay(FAKE, 16, ctypes.c_float(-0.1), NULL) == moe.MOE_EINVAL
+    assert L.moe_demand_decay(FAKE, -1, ctypes.c_float(0.5), NULL) == moe.MOE_EINVAL
+    assert L.moe_demand_decay(NULL, 0, ctypes.c_float(0.5), NULL) == moe.MOE_OK          # nothing to do
+    missing = str(tmp_path / "none.bin").encode()
+    assert L.moe_demand_load(FAKE, 2, 8, missing, NULL) == moe.MOE_EIO
+    # a file whose header names another shape, or a bad magic, is refused before the device is touched
+    p = tmp_path / "d.bin"
+    import struct
+    p.write_bytes(b"MOEDEMD1" + struct.pack("<iiii", 3, 8, 40, 0) + bytes(3 * 8 * 8))
+    assert L.moe_demand_load(FAKE, 2, 8, str(p).encode(), NULL) == moe.MOE_EINVAL
+    p.write_bytes(b"MOEDEMDX" + struct.pack("<iiii", 2, 8, 40, 0) + bytes(2 * 8 * 8))
+    assert L.moe_demand_load(FAKE, 2, 8, str(p).encode(), NULL) == moe.MOE_EINVAL
+    p.write_bytes(b"MOEDEMD1" + struct.pack("<iiii", 2, 8, 40, 0) + bytes(10))          # truncated
+    assert L.moe_demand_load(FAKE, 2, 8, str(p).encode(), NULL) == moe.MOE_EIO
+    assert L.moe_demand_save(NULL, 2, 8, str(p).encode(), NULL) == moe.MOE_EINVAL
