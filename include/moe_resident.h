@@ -232,6 +232,44 @@ moe_status moe_arena_replan(const uint64_t* demand, int L, int E, int n_main, in
 moe_status moe_ring_install(int32_t* slot_of, int32_t* owner, int ring_slot, int flat_id,
                             int n_flat, int n_slots, void* stream);
 
+/*
+ * Asynchronous hot-read ring (README item 3, DeepSeek: "after each step, the
+ * heaviest misses are read into a ring of slots of their own ... while the
+ * next step runs, and are routable from the step after until the ring
+ * wraps"; "Settings worth knowing": the ring's slots are on top of the main
+ * budget). A HOST object; one thread drives it, once per step boundary.
+ *
+ * create: ring slots are arena slots [ring_first, ring_first + n_ring).
+ *   host_records: host array [n_flat] of HOST pointers, one expert record
+ *   (arena->slot_bytes bytes, the arena record layout) per flat id, or NULL
+ *   when the store has no copy (the stand-in for the drive the pages read
+ *   from). The pointer array is copied; the records must stay valid and
+ *   unchanged until destroy, and should be pinned (cudaHostAlloc) so that the
+ *   copies overlap compute. cap: the heavy-miss list's capacity (1..32). The
+ *   arena struct is copied.
+ * step: call after step s has been enqueued on `stream`, including the
+ *   moe_hot_miss_select that wrote heavy_flat [cap] / n_heavy (device).
+ *   1. experts copied by the previous call are installed (the stream waits
+ *      for their copies): routable from step s + 1;
+ *   2. the host waits for step s to finish and reads its heavy-miss list;
+ *   3. each listed flat id with a record and not already in the ring takes
+ *      the next ring slot in FIFO order: the slot's owner leaves the routing
+ *      tables on `stream`, then the record is copied in on `copy_stream`; it
+ *      is installed by the next call (routable from step s + 2).
+ *   *n_fetched (host, may be NULL) = experts whose copies were issued.
+ *   slot_of int32 [n_flat], owner int32 [n_slots] (device). An install of an
+ *   expert that became resident in the meantime is refused and sets
+ *   MOE_DEV_RESIDENT.
+ * destroy: waits for copies in flight, frees the object.
+ */
+typedef struct moe_hot_ring moe_hot_ring;
+moe_status moe_hot_ring_create(const moe_arena* arena, int ring_first, int n_ring, int n_flat,
+                               const void* const* host_records, int cap, moe_hot_ring** ring);
+moe_status moe_hot_ring_step(moe_hot_ring* ring, const int32_t* heavy_flat, const int32_t* n_heavy,
+                             int32_t* slot_of, int32_t* owner, void* stream, void* copy_stream,
+                             int32_t* n_fetched);
+moe_status moe_hot_ring_destroy(moe_hot_ring* ring);
+
 /* Workspace sizes (bytes) for the calls above. */
 size_t moe_workspace_bytes(int T, int k, int d, int ffn, int E, int n_slots);
 size_t moe_replan_workspace_bytes(int L, int E);

@@ -31,7 +31,7 @@ EXPORTS = ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accum
            "moe_arena_replan", "moe_ring_install", "moe_workspace_bytes", "moe_replan_workspace_bytes",
            "moe_device_status", "moe_status_str", "moe_kernel_launches", "moe_profile_enable",
            "moe_profile_kernel_count", "moe_profile_read", "moe_profile_reset", "moe_demand_decay",
-           "moe_demand_save", "moe_demand_load")
+           "moe_demand_save", "moe_demand_load", "moe_hot_ring_create", "moe_hot_ring_step", "moe_hot_ring_destroy")
 
 
 class MoeError(RuntimeError):
@@ -84,12 +84,17 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.moe_profile_reset.restype = None
     L.moe_profile_reset.argtypes = []
     L.moe_demand_decay.argtypes = [_P, ctypes.c_int64, _F, _P]
+    L.moe_hot_ring_create.argtypes = [ctypes.POINTER(MoeArena), _I, _I, _I, ctypes.POINTER(ctypes.c_void_p), _I,
+                                      ctypes.POINTER(ctypes.c_void_p)]
+    L.moe_hot_ring_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_int32)]
+    L.moe_hot_ring_destroy.argtypes = [_P]
     L.moe_demand_save.argtypes = [_P, _I, _I, ctypes.c_char_p, _P]
     L.moe_demand_load.argtypes = [_P, _I, _I, ctypes.c_char_p, _P]
     for name in ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accumulate", "moe_hot_miss_select",
                  "moe_expert_ffn_mxfp4",
                  "moe_arena_replan", "moe_ring_install", "moe_device_status", "moe_profile_enable",
-                 "moe_profile_read", "moe_demand_decay", "moe_demand_save", "moe_demand_load"):
+                 "moe_profile_read", "moe_demand_decay", "moe_demand_save", "moe_demand_load", "moe_hot_ring_create",
+                 "moe_hot_ring_step", "moe_hot_ring_destroy"):
         L[name].restype = _I
     _lib = L
     return L
@@ -252,3 +257,38 @@ def moe_demand_load(demand: torch.Tensor, path: str, stream=None) -> None:
     """Read an [L, E] demand history written by moe_demand_save into `demand`."""
     L, E = demand.shape
     _check("moe_demand_load", load().moe_demand_load(_ptr(demand), L, E, os.fsencode(path), _stream(stream)))
+
+
+class HotRing:
+    """The asynchronous hot-read ring (moe_hot_ring_*): ring slots [ring_first, ring_first + n_ring) of
+    `arena`, filled from `records`, a sequence of n_flat host addresses (int) of expert records or None."""
+
+    def __init__(self, arena: Arena, ring_first: int, n_ring: int, records, cap: int = 16):
+        self._keep = arena
+        n_flat = len(records)
+        self._ptrs = (ctypes.c_void_p * n_flat)(*[r if r else None for r in records])
+        self._st = arena.struct()
+        h = ctypes.c_void_p()
+        _check("moe_hot_ring_create", load().moe_hot_ring_create(
+            ctypes.byref(self._st), ring_first, n_ring, n_flat, self._ptrs, cap, ctypes.byref(h)))
+        self._h = h
+        self.copy_stream = torch.cuda.Stream()
+
+    def step(self, heavy_flat, n_heavy, slot_of, owner, stream=None) -> int:
+        """Install last call's copies, read this step's heavy misses, issue their copies; returns how many."""
+        n = ctypes.c_int32(0)
+        _check("moe_hot_ring_step", load().moe_hot_ring_step(
+            self._h, _ptr(heavy_flat), _ptr(n_heavy), _ptr(slot_of), _ptr(owner), _stream(stream),
+            ctypes.c_void_p(self.copy_stream.cuda_stream), ctypes.byref(n)))
+        return int(n.value)
+
+    def close(self) -> None:
+        if self._h:
+            _check("moe_hot_ring_destroy", load().moe_hot_ring_destroy(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

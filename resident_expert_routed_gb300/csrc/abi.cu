@@ -122,6 +122,9 @@ cudaEvent_t prof_event() {
 
 }  // namespace
 
+// The device error word of the current device, for other translation units.
+uint32_t* moe_err_word() { return err_word(); }
+
 void moe_prof_begin(int kind, cudaStream_t s) {
     (void)kind;
     if (!g_prof_on.load(std::memory_order_relaxed)) return;

@@ -368,6 +368,9 @@ cudaError_t moe_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// The device error word of the current device (abi.cu); null if it cannot be found.
+uint32_t* moe_err_word();
+
 // Kernel launch counter kept by abi.cu.
 void moe_count_launches(int n);
 int moe_sm_count();

@@ -1,0 +1,181 @@
+// The asynchronous hot-read ring (TideLM README, "How adaptive expert loading
+// works", item 3, DeepSeek: after each step the heaviest misses are read into
+// a ring of slots of their own while the next step runs, and are routable from
+// the step after until the ring wraps; "Settings worth knowing": the ring's
+// slots sit on top of the main budget).
+//
+// A host object drives it at step boundaries. One call, made after step s
+// has been enqueued (including its heavy-miss list):
+//   1. installs the experts whose copies the previous call issued (the
+//      compute stream waits for those copies): routable from step s + 1;
+//   2. reads step s's heavy-miss list (the host waits for step s to finish,
+//      as a decode loop does to read its sampled token);
+//   3. for each heavy miss with a record in the host store (the stand-in for
+//      the drive) that is not already in the ring, takes the next ring slot in
+//      FIFO order, removes the slot's current owner from the routing tables on
+//      the compute stream (so nothing from step s + 1 on reads the slot), and
+//      copies the record into the slot on the copy stream once that removal
+//      is done. Those experts are installed by the next call: routable from
+//      step s + 2, while step s + 1 ran beside the copies.
+// Table updates are small kernels on the compute stream; an install of an
+// expert that became resident meanwhile is refused (MOE_DEV_RESIDENT), as for
+// moe_ring_install.
+#include <vector>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int RING_BATCH = 32;
+
+struct RingBatch {
+    int n;
+    int slot[RING_BATCH];
+    int flat[RING_BATCH];
+};
+
+// owner[slot] = -1 and slot_of[old owner] = -1 for every slot of the batch.
+__global__ void ring_evict_batch(int32_t* slot_of, int32_t* owner, RingBatch b) {
+    pdl_trigger();
+    pdl_wait();
+    if (threadIdx.x != 0) return;
+    for (int i = 0; i < b.n; ++i) {
+        const int old = owner[b.slot[i]];
+        if (old >= 0 && slot_of[old] == b.slot[i]) slot_of[old] = -1;
+        owner[b.slot[i]] = -1;
+    }
+}
+
+// Make each flat id resident in its slot (slots were emptied by ring_evict_batch).
+__global__ void ring_install_batch(int32_t* slot_of, int32_t* owner, RingBatch b, uint32_t* err) {
+    pdl_trigger();
+    pdl_wait();
+    if (threadIdx.x != 0) return;
+    for (int i = 0; i < b.n; ++i) {
+        const int f = b.flat[i], s = b.slot[i];
+        if (slot_of[f] >= 0) { record_error(err, MOE_DEV_RESIDENT); continue; }
+        const int old = owner[s];
+        if (old >= 0 && slot_of[old] == s) slot_of[old] = -1;
+        owner[s] = f;
+        slot_of[f] = s;
+    }
+}
+
+}  // namespace
+
+struct moe_hot_ring {
+    moe_arena arena;
+    int ring_first = 0, n_ring = 0, n_flat = 0, cap = 0;
+    std::vector<const void*> records;     // host record of each flat id (or null)
+    std::vector<int> ring_flat;           // last flat id copied into each ring slot (host view), -1 = none
+    int next = 0;                         // FIFO position in the ring
+    RingBatch pending{};                  // copies issued by the previous call, installed by the next
+    int32_t* list = nullptr;              // pinned: [0] = count, [1..cap] = flat ids
+    cudaEvent_t list_ready = nullptr, evicted = nullptr, copied = nullptr;
+    bool copies_in_flight = false;
+};
+
+namespace {
+
+cudaError_t launch_batch(bool install, moe_hot_ring* r, const RingBatch& b, int32_t* slot_of, int32_t* owner,
+                         cudaStream_t s) {
+    if (b.n == 0) return cudaSuccess;
+    cudaError_t e;
+    if (install) {
+        uint32_t* err = moe_err_word();
+        if (!err) return cudaErrorUnknown;
+        e = moe_launch(ring_install_batch, dim3(1), dim3(32), 0, s, slot_of, owner, b, err);
+    } else {
+        e = moe_launch(ring_evict_batch, dim3(1), dim3(32), 0, s, slot_of, owner, b);
+    }
+    moe_count_launches(1);
+    return e;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_hot_ring_create(const moe_arena* arena, int ring_first, int n_ring, int n_flat,
+                                          const void* const* host_records, int cap, moe_hot_ring** ring) {
+    if (!arena || !host_records || !ring || !arena->base || n_flat < 1 || n_ring < 1 || ring_first < 0 ||
+        ring_first + n_ring > arena->n_slots || cap < 1 || cap > RING_BATCH || arena->slot_bytes <= 0)
+        return MOE_EINVAL;
+    *ring = nullptr;
+    auto* r = new moe_hot_ring();
+    r->arena = *arena;
+    r->ring_first = ring_first;
+    r->n_ring = n_ring;
+    r->n_flat = n_flat;
+    r->cap = cap;
+    r->records.assign(host_records, host_records + n_flat);
+    r->ring_flat.assign(n_ring, -1);
+    if (cudaMallocHost(&r->list, sizeof(int32_t) * (1 + cap)) != cudaSuccess ||
+        cudaEventCreateWithFlags(&r->list_ready, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&r->evicted, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&r->copied, cudaEventDisableTiming) != cudaSuccess) {
+        moe_hot_ring_destroy(r);
+        return MOE_ECUDA;
+    }
+    *ring = r;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_hot_ring_step(moe_hot_ring* r, const int32_t* heavy_flat, const int32_t* n_heavy,
+                                        int32_t* slot_of, int32_t* owner, void* stream, void* copy_stream,
+                                        int32_t* n_fetched) {
+    if (!r || !heavy_flat || !n_heavy || !slot_of || !owner) return MOE_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
+    if (n_fetched) *n_fetched = 0;
+    // 1. install what the previous call copied
+    if (r->pending.n > 0) {
+        if (cudaStreamWaitEvent(s, r->copied, 0) != cudaSuccess) return MOE_ECUDA;
+        if (launch_batch(true, r, r->pending, slot_of, owner, s) != cudaSuccess) return MOE_ECUDA;
+        r->pending.n = 0;
+    }
+    // 2. this step's heavy-miss list
+    if (cudaMemcpyAsync(r->list, n_heavy, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(r->list + 1, heavy_flat, sizeof(int32_t) * r->cap, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaEventRecord(r->list_ready, s) != cudaSuccess || cudaEventSynchronize(r->list_ready) != cudaSuccess)
+        return MOE_ECUDA;
+    // 3. choose ring slots in FIFO order for the misses the store can serve
+    RingBatch b{};
+    const int n = r->list[0] < r->cap ? r->list[0] : r->cap;
+    for (int i = 0; i < n && b.n < r->n_ring; ++i) {
+        const int f = r->list[1 + i];
+        if (f < 0 || f >= r->n_flat || !r->records[f]) continue;
+        bool in_ring = false;
+        for (int q = 0; q < r->n_ring && !in_ring; ++q) in_ring = r->ring_flat[q] == f;
+        if (in_ring) continue;
+        b.slot[b.n] = r->ring_first + r->next;
+        b.flat[b.n] = f;
+        r->ring_flat[r->next] = f;
+        r->next = (r->next + 1) % r->n_ring;
+        ++b.n;
+    }
+    if (b.n == 0) return MOE_OK;
+    if (launch_batch(false, r, b, slot_of, owner, s) != cudaSuccess || cudaEventRecord(r->evicted, s) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, r->evicted, 0) != cudaSuccess)
+        return MOE_ECUDA;
+    uint8_t* base = static_cast<uint8_t*>(r->arena.base);
+    for (int i = 0; i < b.n; ++i)
+        if (cudaMemcpyAsync(base + (size_t)b.slot[i] * r->arena.slot_bytes, r->records[b.flat[i]],
+                            (size_t)r->arena.slot_bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+            return MOE_ECUDA;
+    if (cudaEventRecord(r->copied, cs) != cudaSuccess) return MOE_ECUDA;
+    r->pending = b;
+    r->copies_in_flight = true;
+    if (n_fetched) *n_fetched = b.n;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_hot_ring_destroy(moe_hot_ring* r) {
+    if (!r) return MOE_OK;
+    moe_status st = MOE_OK;
+    if (r->copies_in_flight && r->copied && cudaEventSynchronize(r->copied) != cudaSuccess) st = MOE_ECUDA;
+    if (r->list) cudaFreeHost(r->list);
+    if (r->list_ready) cudaEventDestroy(r->list_ready);
+    if (r->evicted) cudaEventDestroy(r->evicted);
+    if (r->copied) cudaEventDestroy(r->copied);
+    delete r;
+    return st;
+}
