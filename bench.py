@@ -53,7 +53,7 @@ def peaks():
 class Layer:
     """Device-resident inputs of one layer workload (weights, tables, arena, hidden-state pool)."""
 
-    def __init__(self, cfg: synth.LayerConfig, T: int, pool: int, drift: bool = False):
+    def __init__(self, cfg: synth.LayerConfig, T: int, pool: int, drift: bool = False, ring: int = 0):
         import torch
         import resident_expert_routed_gb300 as moe
         from resident_expert_routed_gb300.layer import LayerBuffers
@@ -61,8 +61,9 @@ class Layer:
         W = synth.router_weights(cfg.seed, cfg.E, cfg.d)
         b = synth.router_bias(cfg.seed, cfg.E, cfg.sigma)
         res = synth.resident_set(cfg, b)
-        self.n_slots = cfg.resident + cfg.n_ring
-        self.slot_of_np = synth.slot_table(cfg, res, self.n_slots)
+        self.n_slots = cfg.resident + cfg.n_ring + ring
+        # with a hot-read ring the residents keep the main slots and the ring follows them
+        self.slot_of_np = synth.slot_table(cfg, res, cfg.resident if ring else self.n_slots)
         owner = np.full(self.n_slots, -1, np.int32)
         owner[self.slot_of_np[res]] = res
         self.owner_np = owner
@@ -304,6 +305,61 @@ def e2e_steps(layer: Layer, K: int, scratch):
     return total / K, h2d, d2h
 
 
+# ------------------------------------------------------------------ hot-read ring, on and off
+
+def ring_on_off(T: int, steps: int, n_ring: int = 64):
+    """Decode steps (drifted bias, so misses happen) with the asynchronous hot-read ring on and off.
+
+    A pinned host store of every absent expert stands in for the drive. Both modes synchronise the host
+    once per step (a decode loop reads its sampled token); the ring's copies run on their own stream.
+    """
+    import torch
+    import resident_expert_routed_gb300 as moe
+    cfg = synth.DECODE
+    lay = Layer(cfg, T, pool=8, drift=True, ring=n_ring)
+    sb = lay.rec["slot_bytes"]
+    absent = np.flatnonzero(lay.slot_of_np < 0).astype(np.int32)
+    store = torch.empty(len(absent) * sb, dtype=torch.uint8, pin_memory=True)
+    tmp = torch.empty(16 * sb, dtype=torch.uint8, device="cuda")
+    for i0 in range(0, len(absent), 16):
+        part = absent[i0:i0 + 16]
+        synth.fill_slots_device(tmp, cfg.d, cfg.ffn, cfg.seed, cfg.E, torch.from_numpy(part).cuda())
+        store[i0 * sb:(i0 + len(part)) * sb].copy_(tmp[:len(part) * sb])
+    records = [None] * cfg.E
+    for i, f in enumerate(absent):
+        records[int(f)] = store.data_ptr() + i * sb
+    res = {}
+    for mode in ("off", "on"):
+        lay.slot_of.copy_(torch.from_numpy(lay.slot_of_np))
+        owner = torch.from_numpy(lay.owner_np).cuda()
+        lay.demand.zero_()
+        lay.miss.zero_()
+        ring = moe.HotRing(lay.arena, cfg.resident, n_ring, records) if mode == "on" else None
+        fetched, t0 = 0, 0.0
+        for i in range(3 + steps):
+            if i == 3:
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                fetched = 0
+            lay.hidden.copy_(lay.pool[i % len(lay.pool)])
+            lay.step()
+            if ring is not None:
+                fetched += ring.step(lay.buf.hot_flat, lay.buf.hot_n, lay.slot_of, owner)
+            else:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        dt = (time.perf_counter() - t0) / steps
+        if ring is not None:
+            ring.close()
+        res[f"ring_{mode}"] = {"tokens_per_s": T / dt, "ms_per_step": 1000.0 * dt}
+        if mode == "on":
+            res["ring_on"]["experts_fetched_per_step"] = fetched / steps
+            res["ring_on"]["h2d_gb_per_step"] = fetched / steps * sb / 1e9
+    res["workload"] = (f"{cfg.name} with the bias drifted after the resident set was fixed, T={T}, "
+                       f"{n_ring} ring slots on top, {len(absent)} absent experts in a pinned host store")
+    return res
+
+
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
 
 def oracle_sample_run(cfg: synth.LayerConfig, x_bits, W, bias, slot_of, owner, n_tok: int) -> float:
@@ -422,6 +478,7 @@ def run_ours(args, rank, ws, local):
         sweep[f"decode_T{T}"] = {"tokens_per_s": T / (step_ms / 1000.0), "ms_per_step": step_ms,
                                  "distinct_experts": u_mean,
                                  "step_hbm_frac": step_bytes / (step_ms / 1000.0) / 1e9 / pk["hbm_gbs"]}
+        sweep["hot_ring"] = ring_on_off(T, 30)
         if not args.no_prefill:
             lp = Layer(synth.PREFILL, 8192, pool=2)
             m, _, su, _ = timed_graph_steps(lp, 5, 2, scratch, 1)
