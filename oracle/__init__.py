@@ -59,6 +59,7 @@ def _declare(L):
     L.or_demand.argtypes = [_P, _P, _P, _I, _I, _I, _I, _P, _P]
     L.or_hot_miss_select.argtypes = [_P, _I, _I, _D, _I, _P, _P, _P]
     L.or_demand_decay_fixed.argtypes = [_P, ctypes.c_int64, _D]
+    L.or_hot_read_choose.argtypes = [_P, _P, _P, _P, _I, _D, _I, _P]
     L.or_expert_pair.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
     L.or_ffn.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]
     L.or_replan.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P]
@@ -154,6 +155,16 @@ def demand_decay_fixed(D: np.ndarray, factor: float) -> np.ndarray:
     out = np.ascontiguousarray(D, dtype=np.uint64).copy()
     lib().or_demand_decay_fixed(_ptr(out), out.size, float(factor))
     return out
+
+
+def hot_read_choose(M, D, slot_of, in_store, threshold: float = 0.2, budget: int = 1) -> tuple[int, int]:
+    """(expert read, coldest resident it replaces) for one layer's synchronous hot read, or (-1, -1)."""
+    Mc, Dc = _c(M, np.float64), _c(D, np.float64)
+    so = _c(slot_of, np.int32)
+    st = _c(np.asarray(in_store).astype(np.uint8), np.uint8)
+    out = np.zeros(2, np.int32)
+    lib().or_hot_read_choose(_ptr(Mc), _ptr(Dc), _ptr(so), _ptr(st), Mc.size, float(threshold), int(budget), _ptr(out))
+    return int(out[0]), int(out[1])
 
 
 def hot_miss_select(M: np.ndarray, threshold: float = 0.2, cap: int = 16):

@@ -201,6 +201,28 @@ void or_demand_decay_fixed(uint64_t* D, int64_t n, double factor) {
     for (int64_t i = 0; i < n; ++i) D[i] = (uint64_t)(((unsigned __int128)D[i] * q) >> 32);
 }
 
+// Synchronous hot read of one layer (README item 3, GLM-5.3: a layer's
+// heaviest miss is "read before that layer's MoE runs, computed exactly, and
+// kept resident in place of the coldest expert"). Reading: the read expert
+// is the non-resident expert of the layer with the largest miss share this
+// step (>= threshold, ties to the lower index) that the store holds; the
+// coldest expert is the resident one with the lowest demand (ties to the
+// lower index); nothing happens when the step's read budget is spent or
+// either is missing. out = (read expert, victim expert), or (-1, -1).
+void or_hot_read_choose(const double* M, const double* D, const int32_t* slot_of, const uint8_t* in_store,
+                        int E, double threshold, int budget, int32_t* out) {
+    out[0] = out[1] = -1;
+    if (budget <= 0) return;
+    int best = -1, cold = -1;
+    for (int e = 0; e < E; ++e) {
+        if (slot_of[e] < 0 && in_store[e] && M[e] >= threshold && (best < 0 || M[e] > M[best])) best = e;
+        if (slot_of[e] >= 0 && (cold < 0 || D[e] < D[cold])) cold = e;
+    }
+    if (best < 0 || cold < 0) return;
+    out[0] = best;
+    out[1] = cold;
+}
+
 // Heavy misses (README item 3: "the heaviest misses"; ">= 0.2 of the routing
 // weight, at most 16 a step"). Candidates are the (layer, expert) with
 // M >= threshold, ordered by M descending then flat index ascending; the first

@@ -443,3 +443,40 @@ def test_demand_decay_tracks_the_real_product():
             assert abs(g - exact) <= 1 + d * 2.0 ** -33 + exact * 1e-15
         assert np.all(got >= prev)                                                # monotone in the factor
         prev = got
+
+
+# ------------------------------------------------------------------ synchronous hot read (one layer)
+
+def test_hot_read_choose_hand_case():
+    # experts 0..5: 1, 3, 4 resident; 2 and 5 missed with shares 0.25 and 0.6; 5 has no record
+    M = np.array([0, 0, 0.25, 0, 0, 0.6])
+    D = np.array([0, 7.0, 0, 2.0, 2.0, 0])
+    slot_of = np.array([-1, 4, -1, 0, 9, -1], np.int32)
+    store = [1, 1, 1, 1, 1, 0]
+    # 5 is the heaviest miss but the store cannot serve it; 2 is read; 3 and 4 tie at the lowest
+    # demand and the lower index is the coldest
+    assert oracle.hot_read_choose(M, D, slot_of, store, 0.2, 1) == (2, 3)
+    assert oracle.hot_read_choose(M, D, slot_of, [1] * 6, 0.2, 1) == (5, 3)
+    assert oracle.hot_read_choose(M, D, slot_of, store, 0.3, 1) == (-1, -1)     # under the threshold
+    assert oracle.hot_read_choose(M, D, slot_of, store, 0.25, 1) == (2, 3)      # the threshold is included
+    assert oracle.hot_read_choose(M, D, slot_of, store, 0.2, 0) == (-1, -1)     # the step's budget is spent
+    assert oracle.hot_read_choose(M, D, np.full(6, -1, np.int32), store, 0.2, 1) == (-1, -1)   # nothing resident
+
+
+def test_hot_read_choose_brute_force():
+    rng = np.random.default_rng(9)
+    for _ in range(300):
+        E = int(rng.integers(1, 12))
+        M = np.round(rng.random(E), 1) * (rng.random(E) < 0.6)
+        D = np.round(rng.random(E) * 4, 0)
+        slot_of = np.where(rng.random(E) < 0.5, rng.integers(0, 20, E), -1).astype(np.int32)
+        store = (rng.random(E) < 0.8).astype(np.uint8)
+        got = oracle.hot_read_choose(M, D, slot_of, store, 0.2, 1)
+        cand = [e for e in range(E) if slot_of[e] < 0 and store[e] and M[e] >= 0.2]
+        res = [e for e in range(E) if slot_of[e] >= 0]
+        if not cand or not res:
+            assert got == (-1, -1)
+            continue
+        best = sorted(cand, key=lambda e: (-M[e], e))[0]
+        cold = sorted(res, key=lambda e: (D[e], e))[0]
+        assert got == (best, cold)
