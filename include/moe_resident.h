@@ -270,6 +270,34 @@ moe_status moe_hot_ring_step(moe_hot_ring* ring, const int32_t* heavy_flat, cons
                              int32_t* n_fetched);
 moe_status moe_hot_ring_destroy(moe_hot_ring* ring);
 
+/*
+ * Synchronous hot read of one layer (README item 3, GLM-5.3: "a layer's
+ * heaviest miss (>= 0.2 of the routing weight, at most 16 a step, paced over
+ * the layers) is read before that layer's MoE runs, computed exactly, and
+ * kept resident in place of the coldest expert"). Call after
+ * moe_demand_accumulate of `layer` and before its FFN; then route the layer
+ * again with the updated slot_of, so that the tokens that wanted the expert
+ * get it (the wanted picks and the demand are unchanged).
+ *   read   = the non-resident expert of the layer with the largest miss share
+ *            this step (miss_max >= threshold, ties to the lower index) that
+ *            the store holds;
+ *   victim = the resident expert of the layer with the lowest demand (ties to
+ *            the lower index);
+ *   if *budget > 0 and both exist: *budget -= 1; victim leaves the tables,
+ *   read takes its slot, and the record store[read] is copied into the slot.
+ * store: device array [L*E] of uint64 addresses of expert records (slot_bytes
+ *   each, the arena record layout, 16-byte aligned) that the device can read,
+ *   e.g. pinned host memory; 0 = not in the store. The addresses are trusted.
+ * demand uint64 [L,E]; miss_max fp32 [L,E] (this step's shares, before
+ *   moe_hot_miss_select resets them); slot_of int32 [L*E]; owner int32
+ *   [n_slots]; budget: device int32, reads left this step (the caller sets
+ *   it, e.g. to 16, when a step starts); swap: device int32 [3] out =
+ *   (flat read, slot, flat victim), or (-1, -1, -1) when nothing was read.
+ */
+moe_status moe_hot_read_sync(const uint64_t* store, const uint64_t* demand, const float* miss_max,
+                             int32_t* slot_of, int32_t* owner, const moe_arena* arena, int layer, int L, int E,
+                             float threshold, int32_t* budget, int32_t* swap, void* stream);
+
 /* Workspace sizes (bytes) for the calls above. */
 size_t moe_workspace_bytes(int T, int k, int d, int ffn, int E, int n_slots);
 size_t moe_replan_workspace_bytes(int L, int E);

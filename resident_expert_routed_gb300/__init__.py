@@ -31,7 +31,8 @@ EXPORTS = ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accum
            "moe_arena_replan", "moe_ring_install", "moe_workspace_bytes", "moe_replan_workspace_bytes",
            "moe_device_status", "moe_status_str", "moe_kernel_launches", "moe_profile_enable",
            "moe_profile_kernel_count", "moe_profile_read", "moe_profile_reset", "moe_demand_decay",
-           "moe_demand_save", "moe_demand_load", "moe_hot_ring_create", "moe_hot_ring_step", "moe_hot_ring_destroy")
+           "moe_demand_save", "moe_demand_load", "moe_hot_ring_create", "moe_hot_ring_step", "moe_hot_ring_destroy",
+           "moe_hot_read_sync")
 
 
 class MoeError(RuntimeError):
@@ -88,13 +89,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                       ctypes.POINTER(ctypes.c_void_p)]
     L.moe_hot_ring_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_int32)]
     L.moe_hot_ring_destroy.argtypes = [_P]
+    L.moe_hot_read_sync.argtypes = [_P, _P, _P, _P, _P, ctypes.POINTER(MoeArena), _I, _I, _I, _F, _P, _P, _P]
     L.moe_demand_save.argtypes = [_P, _I, _I, ctypes.c_char_p, _P]
     L.moe_demand_load.argtypes = [_P, _I, _I, ctypes.c_char_p, _P]
     for name in ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accumulate", "moe_hot_miss_select",
                  "moe_expert_ffn_mxfp4",
                  "moe_arena_replan", "moe_ring_install", "moe_device_status", "moe_profile_enable",
                  "moe_profile_read", "moe_demand_decay", "moe_demand_save", "moe_demand_load", "moe_hot_ring_create",
-                 "moe_hot_ring_step", "moe_hot_ring_destroy"):
+                 "moe_hot_ring_step", "moe_hot_ring_destroy", "moe_hot_read_sync"):
         L[name].restype = _I
     _lib = L
     return L
@@ -292,3 +294,14 @@ class HotRing:
             self.close()
         except Exception:
             pass
+
+
+def moe_hot_read_sync(store, demand, miss_max, slot_of, owner, arena: Arena, layer: int, threshold: float,
+                      budget, swap, stream=None) -> None:
+    """One layer's synchronous hot read (see the header): store int64 [L*E] device-readable record
+    addresses (0 = none); budget int32 [1] and swap int32 [3] on the device."""
+    L, E = demand.shape
+    st = arena.struct()
+    _check("moe_hot_read_sync", load().moe_hot_read_sync(
+        _ptr(store), _ptr(demand), _ptr(miss_max), _ptr(slot_of), _ptr(owner), ctypes.byref(st), layer, L, E,
+        float(threshold), _ptr(budget), _ptr(swap), _stream(stream)))

@@ -19,7 +19,8 @@
 //      step s + 2, while step s + 1 ran beside the copies.
 // Table updates are small kernels on the compute stream; an install of an
 // expert that became resident meanwhile is refused (MOE_DEV_RESIDENT), as for
-// moe_ring_install.
+// moe_ring_install. The GLM-5.3 variant, a synchronous read of a layer's
+// heaviest miss into the coldest expert's slot, is moe_hot_read_sync below.
 #include <vector>
 
 #include "common.cuh"
@@ -61,7 +62,108 @@ __global__ void ring_install_batch(int32_t* slot_of, int32_t* owner, RingBatch b
     }
 }
 
+// ------------------------------------------------------------------ synchronous hot read (GLM-5.3)
+//
+// README item 3, GLM-5.3: a layer's heaviest miss (>= 0.2 of the routing
+// weight, at most 16 a step, paced over the layers) is read before that
+// layer's MoE runs, computed exactly, and kept resident in place of the
+// coldest expert. One CTA picks the expert and the victim and updates the
+// tables; a grid-wide copy then streams the record from the store (host
+// memory the device can address) into the victim's slot. The caller routes
+// the layer again before its FFN.
+
+// Block-wide max of a 64-bit key (256 threads).
+__device__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, v, off);
+        v = o > v ? o : v;
+    }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    unsigned long long r = red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = red[w] > r ? red[w] : r;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(256) hot_read_choose(const unsigned long long* __restrict__ store,
+                                                       const unsigned long long* __restrict__ D,
+                                                       const float* __restrict__ M, int32_t* slot_of,
+                                                       int32_t* owner, int layer, int E, float thr,
+                                                       int32_t* budget, int32_t* swap) {
+    __shared__ unsigned long long red[8];
+    pdl_trigger();
+    pdl_wait();
+    const size_t base = (size_t)layer * E;
+    // heaviest servable miss: key (share bits, ~e), larger wins; shares are >= 0 so bits order like values
+    unsigned long long best = 0;
+    // coldest resident: the lowest demand, then the lowest index: max of ~(demand) then of ~e
+    unsigned long long cold = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const float m = M[base + e];
+        if (slot_of[base + e] < 0 && store[base + e] != 0ull && m >= thr)
+            best = max(best, ((unsigned long long)__float_as_uint(m) << 32) | (0xFFFFFFFFull - (unsigned)e));
+        if (slot_of[base + e] >= 0) cold = max(cold, ~D[base + e]);
+    }
+    best = block_max_u64(best, red);
+    const unsigned long long cold_key = block_max_u64(cold, red);      // ~(lowest demand), 0 if none resident
+    unsigned long long cold_e = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (slot_of[base + e] >= 0 && ~D[base + e] == cold_key) cold_e = max(cold_e, 0xFFFFFFFFull - (unsigned)e);
+    cold_e = block_max_u64(cold_e, red);
+    if (threadIdx.x != 0) return;
+    swap[0] = swap[1] = swap[2] = -1;
+    if (best == 0ull || cold_e == 0ull || *budget <= 0) return;
+    const int e_read = (int)(0xFFFFFFFFull - (best & 0xFFFFFFFFull));
+    const int e_cold = (int)(0xFFFFFFFFull - cold_e);
+    const int slot = slot_of[base + e_cold];
+    *budget -= 1;
+    slot_of[base + e_cold] = -1;
+    slot_of[base + e_read] = slot;
+    owner[slot] = (int)(base + e_read);
+    swap[0] = (int)(base + e_read);
+    swap[1] = slot;
+    swap[2] = (int)(base + e_cold);
+}
+
+__global__ void __launch_bounds__(256) hot_read_copy(const unsigned long long* __restrict__ store,
+                                                     const int32_t* __restrict__ swap, uint8_t* arena,
+                                                     long long slot_bytes) {
+    pdl_trigger();
+    pdl_wait();
+    const int f = swap[0];
+    if (f < 0) return;
+    const uint4* src = reinterpret_cast<const uint4*>(store[f]);
+    uint4* dst = reinterpret_cast<uint4*>(arena + (size_t)swap[1] * (size_t)slot_bytes);
+    const long long n = slot_bytes / 16;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
 }  // namespace
+
+extern "C" moe_status moe_hot_read_sync(const uint64_t* store, const uint64_t* demand, const float* miss_max,
+                                        int32_t* slot_of, int32_t* owner, const moe_arena* arena, int layer,
+                                        int L, int E, float threshold, int32_t* budget, int32_t* swap,
+                                        void* stream) {
+    if (!store || !demand || !miss_max || !slot_of || !owner || !arena || !arena->base || !budget || !swap)
+        return MOE_EINVAL;
+    if (L < 1 || E < 1 || layer < 0 || layer >= L || arena->slot_bytes <= 0 || arena->slot_bytes % 16 ||
+        !(threshold >= 0.0f))
+        return MOE_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const unsigned long long* st = reinterpret_cast<const unsigned long long*>(store);
+    cudaError_t e = moe_launch(hot_read_choose, dim3(1), dim3(256), 0, s, st,
+                               reinterpret_cast<const unsigned long long*>(demand), miss_max, slot_of, owner, layer,
+                               E, threshold, budget, swap);
+    if (e == cudaSuccess)
+        e = moe_launch(hot_read_copy, dim3((unsigned)(4 * moe_sm_count())), dim3(256), 0, s, st,
+                       static_cast<const int32_t*>(swap), static_cast<uint8_t*>(arena->base),
+                       (long long)arena->slot_bytes);
+    moe_count_launches(2);
+    return e == cudaSuccess ? MOE_OK : MOE_ECUDA;
+}
 
 struct moe_hot_ring {
     moe_arena arena;

@@ -105,3 +105,31 @@ def near_tie_tokens(scores: np.ndarray, mask: np.ndarray, k: int, rel: float = 1
         if len(s) > k and abs(s[k - 1] - s[k]) <= rel * s[k - 1]:
             out[t] = True
     return out
+
+
+def ring_case(cfg: synth.LayerConfig, n_ring: int, T: int = 8, stream: int = 0):
+    """A drifted case with cfg.resident main slots + n_ring ring slots (device arena), its tables, and a
+    pinned host store of every absent expert's record (the stand-in for the drive): returns
+    (case, arena, slot_of, owner, absent ids, store tensor, per-expert record addresses or None)."""
+    import resident_expert_routed_gb300 as moe
+    c = make_case(cfg, T, stream=stream, drift=True)
+    res = np.flatnonzero(c.slot_of >= 0)
+    n_slots = cfg.resident + n_ring
+    slot_of = synth.slot_table(cfg, res, cfg.resident)
+    owner = np.full(n_slots, -1, np.int32)
+    owner[slot_of[res]] = res
+    rec = synth.slot_record(cfg.d, cfg.ffn)
+    sb = rec["slot_bytes"]
+    buf = torch.zeros(n_slots * sb, dtype=torch.uint8, device="cuda")
+    synth.fill_slots_device(buf, cfg.d, cfg.ffn, cfg.seed, cfg.E, to_dev(owner))
+    arena = moe.Arena(buf, sb, n_slots, cfg.d, cfg.ffn, rec["off_gu_codes"], rec["off_gu_scales"],
+                      rec["off_dn_codes"], rec["off_dn_scales"])
+    absent = np.flatnonzero(slot_of < 0).astype(np.int32)
+    tmp = torch.zeros(len(absent) * sb, dtype=torch.uint8, device="cuda")
+    synth.fill_slots_device(tmp, cfg.d, cfg.ffn, cfg.seed, cfg.E, to_dev(absent))
+    store = torch.empty(len(absent) * sb, dtype=torch.uint8, pin_memory=True)
+    store.copy_(tmp)
+    records = [None] * cfg.E
+    for i, f in enumerate(absent):
+        records[f] = store.data_ptr() + i * sb
+    return c, arena, slot_of, owner, absent, store, records

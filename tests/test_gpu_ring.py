@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import synth
-from tests.cases import ffn_within_tolerance, hidden_dev, make_case, to_dev
+from tests.cases import ffn_within_tolerance, hidden_dev, ring_case, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -22,31 +22,6 @@ moe = pytest.importorskip("resident_expert_routed_gb300")
 from resident_expert_routed_gb300.layer import LayerBuffers, layer_step, step_end  # noqa: E402
 
 N_RING = 2
-
-
-def _setup(cfg, n_ring=N_RING, T=8, stream=0):
-    """Arena of cfg.resident main slots + n_ring ring slots, the tables, and a pinned store of the others."""
-    c = make_case(cfg, T, stream=stream, drift=True)
-    res = np.flatnonzero(c.slot_of >= 0)
-    n_slots = cfg.resident + n_ring
-    slot_of = synth.slot_table(cfg, res, cfg.resident)
-    owner = np.full(n_slots, -1, np.int32)
-    owner[slot_of[res]] = res
-    rec = synth.slot_record(cfg.d, cfg.ffn)
-    sb = rec["slot_bytes"]
-    buf = torch.zeros(n_slots * sb, dtype=torch.uint8, device="cuda")
-    synth.fill_slots_device(buf, cfg.d, cfg.ffn, cfg.seed, cfg.E, to_dev(owner))
-    arena = moe.Arena(buf, sb, n_slots, cfg.d, cfg.ffn, rec["off_gu_codes"], rec["off_gu_scales"],
-                      rec["off_dn_codes"], rec["off_dn_scales"])
-    absent = np.flatnonzero(slot_of < 0).astype(np.int32)
-    tmp = torch.zeros(len(absent) * sb, dtype=torch.uint8, device="cuda")
-    synth.fill_slots_device(tmp, cfg.d, cfg.ffn, cfg.seed, cfg.E, to_dev(absent))
-    store = torch.empty(len(absent) * sb, dtype=torch.uint8, pin_memory=True)
-    store.copy_(tmp)
-    records = [None] * cfg.E
-    for i, f in enumerate(absent):
-        records[f] = store.data_ptr() + i * sb
-    return c, arena, slot_of, owner, absent, store, records
 
 
 def _heavy(ids, cap=16):
@@ -58,7 +33,7 @@ def _heavy(ids, cap=16):
 
 def test_ring_fifo_fetch_install_and_evict():
     cfg = synth.TINY
-    c, arena, slot_of, owner, absent, store, records = _setup(cfg)
+    c, arena, slot_of, owner, absent, store, records = ring_case(cfg, N_RING)
     so_d, ow_d = to_dev(slot_of), to_dev(owner)
     ring = moe.HotRing(arena, cfg.resident, N_RING, records)
     a, b, cc = (int(f) for f in absent[:3])
@@ -95,7 +70,7 @@ def test_ring_experts_are_routed_two_steps_later():
     # 64 tokens of hidden stream 3 leave three heavy misses (found with the oracle); a ring with room
     # for every absent expert, so nothing wraps
     cfg, T, n_ring = synth.TINY, 64, 8
-    c, arena, slot_of, owner, absent, store, records = _setup(cfg, n_ring, T, stream=3)
+    c, arena, slot_of, owner, absent, store, records = ring_case(cfg, n_ring, T, stream=3)
     so_d, ow_d = to_dev(slot_of), to_dev(owner)
     Wd, bd = to_dev(c.W), to_dev(c.bias)
     buf = LayerBuffers(T, cfg.k, cfg.E, cfg.d, cfg.ffn, arena.n_slots)
