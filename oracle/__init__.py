@@ -60,6 +60,7 @@ def _declare(L):
     L.or_hot_miss_select.argtypes = [_P, _I, _I, _D, _I, _P, _P, _P]
     L.or_demand_decay_fixed.argtypes = [_P, ctypes.c_int64, _D]
     L.or_hot_read_choose.argtypes = [_P, _P, _P, _P, _I, _D, _I, _P]
+    L.or_renormalise.argtypes = [_P, _P, _I, _I]
     L.or_expert_pair.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
     L.or_ffn.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]
     L.or_replan.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P]
@@ -155,6 +156,15 @@ def demand_decay_fixed(D: np.ndarray, factor: float) -> np.ndarray:
     out = np.ascontiguousarray(D, dtype=np.uint64).copy()
     lib().or_demand_decay_fixed(_ptr(out), out.size, float(factor))
     return out
+
+
+def renormalise(sel_slot, sel_w) -> np.ndarray:
+    """Combine weights renormalised over each token's valid picks (a new float64 [T, k] array)."""
+    so = _c(sel_slot, np.int32)
+    w = np.ascontiguousarray(sel_w, dtype=np.float64).copy()
+    T, k = so.shape
+    lib().or_renormalise(_ptr(so), _ptr(w), T, k)
+    return w
 
 
 def hot_read_choose(M, D, slot_of, in_store, threshold: float = 0.2, budget: int = 1) -> tuple[int, int]:

@@ -201,6 +201,22 @@ void or_demand_decay_fixed(uint64_t* D, int64_t n, double factor) {
     for (int64_t i = 0; i < n; ++i) D[i] = (uint64_t)(((unsigned __int128)D[i] * q) >> 32);
 }
 
+// Optional renormalisation of the combine weights over a token's k picks
+// (reading R2 keeps the raw scores; this is the alternative): w_j / sum_j w_j
+// over the valid picks (sel_slot >= 0), in pick order; a token without a
+// valid pick keeps zeros.
+void or_renormalise(const int32_t* sel_slot, double* sel_w, int T, int k) {
+    for (int t = 0; t < T; ++t) {
+        double z = 0.0;
+        for (int j = 0; j < k; ++j)
+            if (sel_slot[(size_t)t * k + j] >= 0) z += sel_w[(size_t)t * k + j];
+        for (int j = 0; j < k; ++j) {
+            double& w = sel_w[(size_t)t * k + j];
+            w = (sel_slot[(size_t)t * k + j] >= 0 && z > 0.0) ? w / z : 0.0;
+        }
+    }
+}
+
 // Synchronous hot read of one layer (README item 3, GLM-5.3: a layer's
 // heaviest miss is "read before that layer's MoE runs, computed exactly, and
 // kept resident in place of the coldest expert"). Reading: the read expert

@@ -480,3 +480,22 @@ def test_hot_read_choose_brute_force():
         best = sorted(cand, key=lambda e: (-M[e], e))[0]
         cold = sorted(res, key=lambda e: (D[e], e))[0]
         assert got == (best, cold)
+
+
+# ------------------------------------------------------------------ optional weight renormalisation
+
+def test_renormalise_sums_to_one_and_keeps_ratios():
+    so = np.array([[3, 1, -1], [-1, -1, -1], [0, 2, 5]], np.int32)
+    w = np.array([[0.3, 0.1, 0.0], [0.0, 0.0, 0.0], [0.5, 0.25, 0.25]])
+    r = oracle.renormalise(so, w)
+    assert np.allclose(r[0], [0.75, 0.25, 0.0]) and np.all(r[1] == 0) and np.allclose(r[2], [0.5, 0.25, 0.25])
+    rng = np.random.default_rng(3)
+    so = np.where(rng.random((50, 8)) < 0.8, 1, -1).astype(np.int32)
+    w = rng.random((50, 8)) * (so >= 0)
+    r = oracle.renormalise(so, w)
+    valid = (so >= 0).any(1)
+    assert np.allclose(r[valid].sum(1), 1.0) and np.all(r[~valid] == 0)
+    ratio = np.divide(r, w, out=np.zeros_like(r), where=w > 0)               # one scale per token
+    for t in np.flatnonzero(valid):
+        x = ratio[t][w[t] > 0]
+        assert np.allclose(x, x[0])
