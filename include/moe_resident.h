@@ -128,6 +128,17 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
                               void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Optional renormalisation of the combine weights (the pages say only
+ * "score-weighted"; moe_route_resident keeps each pick's own softmax score so
+ * that a substitute is not inflated). For callers that want weights summing
+ * to one over a token's picks: sel_w[t,j] /= sum of sel_w[t,*] over the picks
+ * with sel_slot >= 0 (fp32, summed in pick order); padding picks and tokens
+ * without a valid pick get 0. sel_slot int32 [T,k], sel_w fp32 [T,k] in place.
+ * Limits: T >= 1, 1 <= k <= 32.
+ */
+moe_status moe_renormalise_weights(const int32_t* sel_slot, float* sel_w, int T, int k, void* stream);
+
+/*
  * moe_route_resident without a caller workspace (the paper has no counterpart:
  * this exists for callers of this library that cannot allocate device memory
  * when they route -- e.g. a serving loop whose memory budget was fixed at

@@ -32,7 +32,7 @@ EXPORTS = ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accum
            "moe_device_status", "moe_status_str", "moe_kernel_launches", "moe_profile_enable",
            "moe_profile_kernel_count", "moe_profile_read", "moe_profile_reset", "moe_demand_decay",
            "moe_demand_save", "moe_demand_load", "moe_hot_ring_create", "moe_hot_ring_step", "moe_hot_ring_destroy",
-           "moe_hot_read_sync")
+           "moe_hot_read_sync", "moe_renormalise_weights")
 
 
 class MoeError(RuntimeError):
@@ -89,6 +89,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                       ctypes.POINTER(ctypes.c_void_p)]
     L.moe_hot_ring_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_int32)]
     L.moe_hot_ring_destroy.argtypes = [_P]
+    L.moe_renormalise_weights.argtypes = [_P, _P, _I, _I, _P]
     L.moe_hot_read_sync.argtypes = [_P, _P, _P, _P, _P, ctypes.POINTER(MoeArena), _I, _I, _I, _F, _P, _P, _P]
     L.moe_demand_save.argtypes = [_P, _I, _I, ctypes.c_char_p, _P]
     L.moe_demand_load.argtypes = [_P, _I, _I, ctypes.c_char_p, _P]
@@ -96,7 +97,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "moe_expert_ffn_mxfp4",
                  "moe_arena_replan", "moe_ring_install", "moe_device_status", "moe_profile_enable",
                  "moe_profile_read", "moe_demand_decay", "moe_demand_save", "moe_demand_load", "moe_hot_ring_create",
-                 "moe_hot_ring_step", "moe_hot_ring_destroy", "moe_hot_read_sync"):
+                 "moe_hot_ring_step", "moe_hot_ring_destroy", "moe_hot_read_sync", "moe_renormalise_weights"):
         L[name].restype = _I
     _lib = L
     return L
@@ -305,3 +306,10 @@ def moe_hot_read_sync(store, demand, miss_max, slot_of, owner, arena: Arena, lay
     _check("moe_hot_read_sync", load().moe_hot_read_sync(
         _ptr(store), _ptr(demand), _ptr(miss_max), _ptr(slot_of), _ptr(owner), ctypes.byref(st), layer, L, E,
         float(threshold), _ptr(budget), _ptr(swap), _stream(stream)))
+
+
+def moe_renormalise_weights(sel_slot, sel_w, stream=None) -> None:
+    """In place: each token's valid combine weights divided by their sum (see the header)."""
+    T, k = sel_w.shape
+    _check("moe_renormalise_weights", load().moe_renormalise_weights(_ptr(sel_slot), _ptr(sel_w), T, k,
+                                                                     _stream(stream)))

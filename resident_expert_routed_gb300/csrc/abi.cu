@@ -4,6 +4,7 @@
 // the launch sequence of each entry point. Every step of the computation runs
 // in the kernels of route.cu, demand.cu, ffn_plan.cu, ffn_gemm.cu and
 // replan.cu; nothing here computes on the host.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -55,9 +56,12 @@ int bn_for(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128; }
 // Positions are slot-sorted with every slot's segment padded to a multiple of
 // the tile height bn, so at most work_max tiles and pad_max = work_max * bn rows.
 struct FfnCarve {
-    size_t pos_of_pair, pair_of_pos, seg, tile_off, work, n_work, xp, xsp, hq, hsp, Y, total;
-    int work_max, pad_max, bn;
+    size_t pos_of_pair, pair_of_pos, seg, tile_off, work, n_work, xp, xsp, hq, hsp, Y, cta_counts, total;
+    int work_max, pad_max, bn, plan_ctas;
 };
+
+// Batches of at least this many picks plan with several CTAs (2048 picks each, at most 64).
+constexpr size_t kPlanMultiPicks = 8192;
 
 FfnCarve ffn_carve(int T, int k, int d, int F, int S) {
     FfnCarve c{};
@@ -79,6 +83,8 @@ FfnCarve ffn_carve(int T, int k, int d, int F, int S) {
     c.hq = take((size_t)c.pad_max * F / 2);
     c.hsp = take((size_t)c.work_max * (F / 128) * 512);
     c.Y = take(P * d * 4);
+    c.plan_ctas = P >= kPlanMultiPicks ? (int)std::min<size_t>(64, (P + 2047) / 2048) : 0;
+    c.cta_counts = take((size_t)c.plan_ctas * S * 4);
     c.total = o;
     return c;
 }
@@ -316,6 +322,8 @@ moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot
     a.hq = w + c.hq;
     a.hsp = w + c.hsp;
     a.Y = reinterpret_cast<float*>(w + c.Y);
+    a.cta_counts = reinterpret_cast<int32_t*>(w + c.cta_counts);
+    a.plan_ctas = c.plan_ctas;
     a.work_max = c.work_max;
     a.pad_max = c.pad_max;
     a.err = err;

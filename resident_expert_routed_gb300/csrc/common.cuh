@@ -330,6 +330,8 @@ struct FfnLaunch {
     uint8_t* hq;            // [pad_max, F/2]   down activation operand
     uint8_t* hsp;           // [work_max * F/128 * 512]
     float* Y;               // [T*k, d] one fp32 row per pick
+    int32_t* cta_counts;    // [plan_ctas, S] per-CTA pick counts, then offsets (large batches)
+    int plan_ctas;          // 0: one-CTA plan
     int work_max, pad_max;
     uint32_t* err;
 };

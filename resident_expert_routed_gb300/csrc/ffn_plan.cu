@@ -11,6 +11,8 @@
 //   each slot a segment of positions padded to a multiple of the tile height
 //   BN, gives every pick a position in its slot's segment, and writes the GEMM
 //   work list: (slot, first position, rows) per tile of at most BN rows.
+//   Large batches split it: plan_count (per-CTA histograms), plan_scan (one
+//   CTA: per-CTA offsets within each slot, segments, work list), plan_place.
 // ffn_pack: quantises every token row of x to MXFP4 once (OCP MX v1.0:
 //   exponent floor(log2 amax) - 2, round to nearest even, saturate at 6; two
 //   codes per byte, even element low) and writes it into row `position` of
@@ -24,25 +26,13 @@ namespace {
 
 constexpr int PLAN_THREADS = 1024;
 
-__global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restrict__ sel_slot, int P, int S, int bn,
-                                                         int32_t* __restrict__ pos_of_pair,
-                                                         int32_t* __restrict__ pair_of_pos,
-                                                         int32_t* __restrict__ seg, int32_t* __restrict__ tile_off,
-                                                         int4* __restrict__ work, int32_t* __restrict__ n_work,
-                                                         uint32_t* err) {
-    extern __shared__ int32_t cnt[];
-    __shared__ unsigned long long scan_scratch[32];
+// From per-slot pick counts cnt[S] (shared memory): each slot's segment of
+// positions padded to a multiple of bn (seg), its first work entry (tile_off),
+// the work list (slot, first position, rows) and its length. Whole block.
+__device__ void plan_slots(const int32_t* cnt, int S, int bn, int32_t* __restrict__ seg,
+                           int32_t* __restrict__ tile_off, int4* __restrict__ work, int32_t* __restrict__ n_work,
+                           unsigned long long* scan_scratch) {
     const int tid = threadIdx.x;
-    pdl_trigger();
-    for (int i = tid; i < S; i += PLAN_THREADS) cnt[i] = 0;
-    pdl_wait();
-    __syncthreads();
-    for (int p = tid; p < P; p += PLAN_THREADS) {
-        int s = sel_slot[p];
-        if (s >= S) { record_error(err, MOE_DEV_BAD_SLOT); s = -1; }
-        pos_of_pair[p] = s >= 0 ? atomicAdd(&cnt[s], 1) : -1;          // rank within the slot for now
-    }
-    __syncthreads();
     // exclusive scan of (padded rows, tiles) per slot; each thread owns a contiguous chunk
     const int chunk = (S + PLAN_THREADS - 1) / PLAN_THREADS;
     const int b0 = tid * chunk, b1 = min(S, b0 + chunk);
@@ -62,6 +52,34 @@ __global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restri
     }
     if (tid == 0) *n_work = (int32_t)(total >> 32);
     __syncthreads();
+    for (int i = tid; i < S; i += PLAN_THREADS) {
+        const int c = cnt[i];
+        const int nt = (c + bn - 1) / bn;
+        for (int q = 0; q < nt; ++q) work[tile_off[i] + q] = make_int4(i, seg[i] + q * bn, min(bn, c - q * bn), 0);
+    }
+}
+
+// Small batches: one CTA counts, scans and places every pick.
+__global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restrict__ sel_slot, int P, int S, int bn,
+                                                         int32_t* __restrict__ pos_of_pair,
+                                                         int32_t* __restrict__ pair_of_pos,
+                                                         int32_t* __restrict__ seg, int32_t* __restrict__ tile_off,
+                                                         int4* __restrict__ work, int32_t* __restrict__ n_work,
+                                                         uint32_t* err) {
+    extern __shared__ int32_t cnt[];
+    __shared__ unsigned long long scan_scratch[32];
+    const int tid = threadIdx.x;
+    pdl_trigger();
+    for (int i = tid; i < S; i += PLAN_THREADS) cnt[i] = 0;
+    pdl_wait();
+    __syncthreads();
+    for (int p = tid; p < P; p += PLAN_THREADS) {
+        int s = sel_slot[p];
+        if (s >= S) { record_error(err, MOE_DEV_BAD_SLOT); s = -1; }
+        pos_of_pair[p] = s >= 0 ? atomicAdd(&cnt[s], 1) : -1;          // rank within the slot for now
+    }
+    __syncthreads();
+    plan_slots(cnt, S, bn, seg, tile_off, work, n_work, scan_scratch);
     for (int p = tid; p < P; p += PLAN_THREADS) {
         const int s = sel_slot[p];
         if (s < 0 || s >= S) continue;
@@ -69,10 +87,65 @@ __global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restri
         pos_of_pair[p] = pos;
         pair_of_pos[pos] = p;
     }
-    for (int i = tid; i < S; i += PLAN_THREADS) {
-        const int c = cnt[i];
-        const int nt = (c + bn - 1) / bn;
-        for (int q = 0; q < nt; ++q) work[tile_off[i] + q] = make_int4(i, seg[i] + q * bn, min(bn, c - q * bn), 0);
+}
+
+// Large batches, in three kernels. 1: each CTA counts the picks of its chunk
+// per slot (shared-memory histogram) and notes each pick's rank among them.
+__global__ void __launch_bounds__(PLAN_THREADS) plan_count(const int32_t* __restrict__ sel_slot, int P, int S,
+                                                           int chunk, int32_t* __restrict__ rank,
+                                                           int32_t* __restrict__ cta_counts, uint32_t* err) {
+    extern __shared__ int32_t cnt[];
+    pdl_trigger();
+    for (int i = threadIdx.x; i < S; i += PLAN_THREADS) cnt[i] = 0;
+    pdl_wait();
+    __syncthreads();
+    const int p1 = min(P, (blockIdx.x + 1) * chunk);
+    for (int p = blockIdx.x * chunk + threadIdx.x; p < p1; p += PLAN_THREADS) {
+        int s = sel_slot[p];
+        if (s >= S) { record_error(err, MOE_DEV_BAD_SLOT); s = -1; }
+        rank[p] = s >= 0 ? atomicAdd(&cnt[s], 1) : -1;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < S; i += PLAN_THREADS) cta_counts[(size_t)blockIdx.x * S + i] = cnt[i];
+}
+
+// 2 (one CTA): per slot, each CTA's offset within the slot (CTA order) and the
+// slot's total; then the segments and the work list.
+__global__ void __launch_bounds__(PLAN_THREADS) plan_scan(int G, int S, int bn, int32_t* __restrict__ cta_counts,
+                                                          int32_t* __restrict__ seg, int32_t* __restrict__ tile_off,
+                                                          int4* __restrict__ work, int32_t* __restrict__ n_work) {
+    extern __shared__ int32_t cnt[];
+    __shared__ unsigned long long scan_scratch[32];
+    pdl_trigger();
+    pdl_wait();
+    for (int i = threadIdx.x; i < S; i += PLAN_THREADS) {
+        int run = 0;
+        for (int g = 0; g < G; ++g) {
+            const int c = cta_counts[(size_t)g * S + i];
+            cta_counts[(size_t)g * S + i] = run;
+            run += c;
+        }
+        cnt[i] = run;
+    }
+    __syncthreads();
+    plan_slots(cnt, S, bn, seg, tile_off, work, n_work, scan_scratch);
+}
+
+// 3: each pick's position = its slot's segment + its CTA's offset + its rank.
+__global__ void __launch_bounds__(256) plan_place(const int32_t* __restrict__ sel_slot, int P, int S, int chunk,
+                                                  const int32_t* __restrict__ cta_offsets,
+                                                  const int32_t* __restrict__ seg, int32_t* __restrict__ pos_of_pair,
+                                                  int32_t* __restrict__ pair_of_pos) {
+    pdl_trigger();
+    pdl_wait();
+    const int g = blockIdx.y;
+    const int p1 = min(P, (g + 1) * chunk);
+    for (int p = g * chunk + blockIdx.x * blockDim.x + threadIdx.x; p < p1; p += gridDim.x * blockDim.x) {
+        const int s = sel_slot[p];
+        if (s < 0 || s >= S) continue;
+        const int pos = seg[s] + cta_offsets[(size_t)g * S + s] + pos_of_pair[p];
+        pos_of_pair[p] = pos;
+        pair_of_pos[pos] = p;
     }
 }
 
@@ -140,6 +213,7 @@ cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
     const int P = a.T * a.k;
     const size_t smem = (size_t)a.S * sizeof(int32_t);
     static bool attr_set[64] = {};
+    static bool attr_set_multi[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
@@ -148,8 +222,30 @@ cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
         attr_set[dev] = true;
     }
     moe_prof_begin(MK_PLAN, s);
-    cudaError_t e = moe_launch(ffn_plan, dim3(1), dim3(PLAN_THREADS), smem, s, a.sel_slot, P, a.S, a.bn,
-                               a.pos_of_pair, a.pair_of_pos, a.seg, a.tile_off, a.work, a.n_work, a.err);
+    cudaError_t e;
+    if (a.plan_ctas > 0) {
+        if (dev < 64 && !attr_set_multi[dev]) {
+            e = cudaFuncSetAttribute(plan_count, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 4);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(plan_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 4);
+            if (e != cudaSuccess) return e;
+            attr_set_multi[dev] = true;
+        }
+        const int G = a.plan_ctas, chunk = (P + G - 1) / G;
+        e = moe_launch(plan_count, dim3(G), dim3(PLAN_THREADS), smem, s, a.sel_slot, P, a.S, chunk, a.pos_of_pair,
+                       a.cta_counts, a.err);
+        if (e == cudaSuccess)
+            e = moe_launch(plan_scan, dim3(1), dim3(PLAN_THREADS), smem, s, G, a.S, a.bn, a.cta_counts, a.seg,
+                           a.tile_off, a.work, a.n_work);
+        if (e == cudaSuccess)
+            e = moe_launch(plan_place, dim3((chunk + 255) / 256, G), dim3(256), 0, s, a.sel_slot, P, a.S, chunk,
+                           static_cast<const int32_t*>(a.cta_counts), static_cast<const int32_t*>(a.seg),
+                           a.pos_of_pair, a.pair_of_pos);
+        moe_count_launches(2);
+    } else {
+        e = moe_launch(ffn_plan, dim3(1), dim3(PLAN_THREADS), smem, s, a.sel_slot, P, a.S, a.bn, a.pos_of_pair,
+                       a.pair_of_pos, a.seg, a.tile_off, a.work, a.n_work, a.err);
+    }
     moe_prof_end(MK_PLAN, s);
     if (e != cudaSuccess) return e;
     const long tasks = (long)a.T * (a.d / 32);

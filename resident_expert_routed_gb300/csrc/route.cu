@@ -295,6 +295,36 @@ cudaError_t launch_route(const RouteLaunch& a, cudaStream_t s) {
     return e;
 }
 
+// ------------------------------------------------------------------ optional weight renormalisation
+namespace {
+
+// w_j / sum of the token's valid weights, summed in pick order; no valid pick: zeros.
+__global__ void __launch_bounds__(256) renormalise_weights(const int32_t* __restrict__ sel_slot,
+                                                           float* __restrict__ sel_w, int T, int k) {
+    pdl_trigger();
+    pdl_wait();
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    float z = 0.0f;
+    for (int j = 0; j < k; ++j)
+        if (sel_slot[(size_t)t * k + j] >= 0) z += sel_w[(size_t)t * k + j];
+    const float inv = z > 0.0f ? 1.0f / z : 0.0f;
+    for (int j = 0; j < k; ++j) {
+        const size_t o = (size_t)t * k + j;
+        sel_w[o] = sel_slot[o] >= 0 ? sel_w[o] * inv : 0.0f;
+    }
+}
+
+}  // namespace
+
+extern "C" moe_status moe_renormalise_weights(const int32_t* sel_slot, float* sel_w, int T, int k, void* stream) {
+    if (!sel_slot || !sel_w || T < 1 || k < 1 || k > 32) return MOE_EINVAL;
+    const cudaError_t e = moe_launch(renormalise_weights, dim3((T + 255) / 256), dim3(256), 0,
+                                     static_cast<cudaStream_t>(stream), sel_slot, sel_w, T, k);
+    moe_count_launches(1);
+    return e == cudaSuccess ? MOE_OK : MOE_ECUDA;
+}
+
 // ------------------------------------------------------------------ routing without a caller workspace
 //
 // Some callers cannot allocate device memory at the point where they route:

@@ -50,3 +50,18 @@ def test_demand_save_load_round_trip(tmp_path):
         moe.moe_demand_load(wrong, path)
     assert ei.value.status == moe.MOE_EINVAL
     assert not wrong.any()
+
+
+def test_renormalise_weights_matches_oracle():
+    from tests.cases import make_case
+    from tests.test_gpu_parity import gpu_route
+    import synth
+    for cfg, T in ((synth.DECODE, 64), (synth.TINY, 8)):
+        c = make_case(cfg, T, drift=True)
+        g = gpu_route(c)
+        so = torch.from_numpy(g["sel_slot"]).cuda()
+        w = torch.from_numpy(g["sel_w"]).cuda()
+        moe.moe_renormalise_weights(so, w)
+        torch.cuda.synchronize()
+        ref = oracle.renormalise(g["sel_slot"], g["sel_w"].astype(np.float64))
+        assert np.allclose(w.cpu().numpy(), ref, rtol=2e-6, atol=0)

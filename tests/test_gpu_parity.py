@@ -202,7 +202,9 @@ def gpu_ffn(c, arena, sel_slot, sel_w):
 FFN_CASES = [(synth.TINY, 8, None), (RAGGED, 37, None), (SPARSE, 5, None), (synth.DECODE, 1, None),
              (synth.DECODE, 8, None), (synth.DECODE, 64, 6), (synth.GLM, 16, 4), (synth.PREFILL, 8192, 3),
              # batches above 64 tokens: 128-row tiles, token-major gate/up, then down rows and the ordered combine
-             (synth.TINY, 80, None), (RAGGED, 100, None), (synth.DECODE, 200, 4)]
+             (synth.TINY, 80, None), (RAGGED, 100, None), (synth.DECODE, 200, 4),
+             # 8192 picks and more: the plan runs in several CTAs
+             (synth.TINY, 2048, None), (RAGGED, 2731, None)]
 
 
 @pytest.mark.parametrize("cfg,T,sample", FFN_CASES, ids=[f"{c.name.split()[0]}-T{T}" for c, T, _ in FFN_CASES])
