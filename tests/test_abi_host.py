@@ -118,6 +118,16 @@ def test_ffn_rejects_bad_arguments(kw, status):
     assert st == status
 
 
+def test_ffn_rejects_picks_past_the_limit():
+    L = moe.load()
+    ar = _arena()
+    # T * k = 2^20 is the largest call; one token more is refused before anything is touched
+    assert L.moe_expert_ffn_mxfp4(FAKE, FAKE, FAKE, ctypes.byref(ar), (1 << 18) + 1, 4, FAKE, FAKE, 1 << 40,
+                                  NULL) == moe.MOE_EUNSUPPORTED
+    assert L.moe_expert_ffn_mxfp4(FAKE, FAKE, FAKE, ctypes.byref(ar), 1 << 18, 4, FAKE, FAKE, 64,
+                                  NULL) == moe.MOE_ENOMEM
+
+
 def test_other_entry_points_reject_bad_arguments():
     L = moe.load()
     assert L.moe_demand_accumulate(FAKE, FAKE, FAKE, 4, 4, 3, 2, 16, FAKE, FAKE, NULL) == moe.MOE_EINVAL  # layer >= L
