@@ -151,36 +151,52 @@ __global__ void __launch_bounds__(256) plan_place(const int32_t* __restrict__ se
 
 // One thread per (token, 32-element block): the token's 64 bytes of bf16 are
 // quantised once (not once per pick), then the 16 bytes of codes go to the
-// operand row of each of the token's picks and the block's scale byte to its
-// place in the tile's scale atom.
+// operand row of each of the token's picks. The four scale bytes of a
+// 128-element group sit side by side in the tile's scale atom; d is a multiple
+// of 128, so lanes 4g..4g+3 of a warp hold one group of one token and lane 4g
+// stores the four bytes as one word. Whole warps iterate together (the
+// shuffles need every lane), each lane predicated on its own element.
 __global__ void __launch_bounds__(256) ffn_pack(const uint16_t* __restrict__ x, const int32_t* __restrict__ pos_of_pair,
                                                 int T, int k, int d, int bn, uint8_t* __restrict__ xp,
                                                 uint8_t* __restrict__ xsp) {
     pdl_trigger();
     pdl_wait();
+    const int lane = threadIdx.x & 31;
     const int nb = d / 32;
     const long total = (long)T * nb;
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
-        const long t = i / nb;
-        const int b = (int)(i % nb);
-        const uint4* src = reinterpret_cast<const uint4*>(x + t * d + b * 32);
-        uint4 v[4];
+    const long stride = (long)gridDim.x * blockDim.x;              // a multiple of 32
+    for (long i0 = (long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); i0 < total; i0 += stride) {
+        const long i = i0 + lane;
+        const bool active = i < total;
+        const long t = active ? i / nb : 0;
+        const int b = active ? (int)(i % nb) : 0;
+        uint4 codes = make_uint4(0u, 0u, 0u, 0u);
+        uint32_t byte = 0;
+        if (active) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + t * d + b * 32);
+            uint4 v[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = src[q];
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(v);
-        float f[32];
-        float amax = 0.0f;
+            for (int q = 0; q < 4; ++q) v[q] = src[q];
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(v);
+            float f[32];
+            float amax = 0.0f;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) { f[q] = bf16_bits_to_float(h[q]); amax = fmaxf(amax, fabsf(f[q])); }
-        const int X = mx_shared_exp(amax);
-        const float inv = exp2_int(-X);
-        const uint4 codes = make_uint4(e2m1x8(f, inv), e2m1x8(f + 8, inv), e2m1x8(f + 16, inv), e2m1x8(f + 24, inv));
-        const uint8_t scale = (uint8_t)(X + 127);
+            for (int q = 0; q < 32; ++q) { f[q] = bf16_bits_to_float(h[q]); amax = fmaxf(amax, fabsf(f[q])); }
+            const int X = mx_shared_exp(amax);
+            const float inv = exp2_int(-X);
+            codes = make_uint4(e2m1x8(f, inv), e2m1x8(f + 8, inv), e2m1x8(f + 16, inv), e2m1x8(f + 24, inv));
+            byte = (uint32_t)(X + 127);
+        }
+        uint32_t word = byte;
+        word |= __shfl_down_sync(0xFFFFFFFFu, byte, 1) << 8;
+        word |= __shfl_down_sync(0xFFFFFFFFu, byte, 2) << 16;
+        word |= __shfl_down_sync(0xFFFFFFFFu, byte, 3) << 24;
+        if (!active) continue;
         for (int j = 0; j < k; ++j) {
             const int pos = pos_of_pair[t * k + j];
             if (pos < 0) continue;
             *reinterpret_cast<uint4*>(xp + (size_t)pos * (d / 2) + b * 16) = codes;
-            xsp[operand_scale_offset(pos, b, bn, d)] = scale;
+            if ((b & 3) == 0) *reinterpret_cast<uint32_t*>(xsp + operand_scale_offset(pos, b, bn, d)) = word;
         }
     }
 }

@@ -134,7 +134,11 @@ __device__ __forceinline__ void select_token(float (&lg)[VPL], int t, const floa
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
     const float inv_z = 1.0f / z;
 
+    // pass 0: wanted top-k over all experts; pass 1: resident top-k, skipped when every wanted pick
+    // is resident (then the two lists are the same)
+    bool all_resident = true;
     for (int pass = 0; pass < 2; ++pass) {
+        if (pass == 1 && all_resident) break;
         uint32_t taken = 0;
         for (int j = 0; j < k; ++j) {
             float bv = NEG;
@@ -152,16 +156,19 @@ __device__ __forceinline__ void select_token(float (&lg)[VPL], int t, const floa
                 continue;
             }
             const float s = expf(bv - mx) * inv_z;
+            int sl = -1;
             if ((bi & 31) == lane) {
                 const int i = bi >> 5;
                 taken |= 1u << i;
-                if (pass == 0) { want_e[o] = bi; want_s[o] = s; }
-                else {
-                    int sl = 0;
 #pragma unroll
-                    for (int q = 0; q < VPL; ++q) if (q == i) sl = slot[q];
-                    sel_e[o] = bi; sel_slot[o] = sl; sel_w[o] = s;
-                }
+                for (int q = 0; q < VPL; ++q) if (q == i) sl = slot[q];
+                if (pass == 0) { want_e[o] = bi; want_s[o] = s; }
+                else { sel_e[o] = bi; sel_slot[o] = sl; sel_w[o] = s; }
+            }
+            if (pass == 0) {
+                sl = __shfl_sync(0xFFFFFFFFu, sl, bi & 31);
+                all_resident = all_resident && sl >= 0;
+                if (lane == 0) { sel_e[o] = bi; sel_slot[o] = sl; sel_w[o] = s; }   // final if all are resident
             }
         }
     }
