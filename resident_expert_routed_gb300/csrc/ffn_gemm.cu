@@ -74,7 +74,7 @@ struct GemmArgs {
 // runs beside the MMAs; they signal the MMA thread through sfull[stage]. Lane
 // i of every quadrant holds row i (16 bytes) of each 512-byte atom, the layout
 // the 32x128b.warpx4 copy produces. load(g, v) fills the NV atoms of stage g
-// (zeros past the end of K) and returns false past the last stage.
+// (zeros past the end of K).
 template <int NV, int PF, int NS, typename Load>
 __device__ __forceinline__ void scale_writer(int n_stages, const Load& load, uint64_t* empty, uint64_t* sfull,
                                              uint32_t sf_base, int sf_cols, volatile int* abort_flag) {
@@ -212,20 +212,30 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t it = 0, j = 0;
+            // One thread feeds the tensor pipe, which queues few MMAs, so the loop
+            // keeps its per-stage work small: descriptors offset from per-kernel
+            // bases (a K step of 32 bytes adds 2 to the address field, which cannot
+            // carry below 256 KB of shared memory), stage and phase counters, the
+            // row count of the next item loaded one item ahead.
+            int s = 0;
+            uint32_t ph = 0, j = 0;
             bool ok_run = true;
+            const uint64_t a_base = smem_desc_sw128(smem_u32(smem + C::OFF_A));
+            const uint64_t b_base = smem_desc_sw128(smem_u32(smem + C::OFF_B));
+            const uint32_t sf_base = tmem + NBUF * C::ACC_COLS;
+            int nv_next = blockIdx.x < n_items ? a.work[blockIdx.x / a.m_tiles].z : 0;
             for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x, ++j) {
-                const int nv = a.work[item / a.m_tiles].z;
+                const int nv = nv_next;
+                if (item + (int)gridDim.x < n_items) nv_next = a.work[(item + gridDim.x) / a.m_tiles].z;
                 const int N = (nv + 15) & ~15;
+                const uint32_t id0 = idesc_mxf4(N, 0, 0), id1 = idesc_mxf4(N, 2, 2);
                 const int b = (int)(j % NBUF);
                 const uint32_t u = j / NBUF;
                 if (!mbar_wait(&acce[b], (u & 1) ^ 1, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t dt = tmem + b * C::ACC_COLS;
-                for (int st = 0; st < nst; ++st, ++it) {
-                    const int s = (int)(it % NS);
-                    const uint32_t r = it / NS;
-                    if (!mbar_wait(&full[s], r & 1, abort_flag) || !mbar_wait(&sfull[s], r & 1, abort_flag)) {
+                for (int st = 0; st < nst; ++st) {
+                    if (!mbar_wait(&full[s], ph, abort_flag) || !mbar_wait(&sfull[s], ph, abort_flag)) {
                         ok_run = false;
                         break;
                     }
@@ -233,20 +243,33 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     const int rem = (a.K - st * 256 * KCH) / 64;
                     const int ksteps = rem < 4 * KCH ? rem : 4 * KCH;      // MMAs of K = 64
                     // scale columns: weight matrices m < NMAT, then activations, 8 KCH columns each
-                    const uint32_t sfc = tmem + NBUF * C::ACC_COLS + s * C::SF_COLS;
-                    const uint32_t as = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
-                    const uint32_t bs = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
+                    const uint32_t sfc = sf_base + s * C::SF_COLS;
                     const uint32_t sfb = sfc + 8 * KCH * C::NMAT;
-                    for (int kk = 0; kk < ksteps; ++kk) {
-                        const int q = kk >> 2, kq = kk & 3;
-                        const uint32_t idesc = idesc_mxf4(N, (kk & 1) * 2, (kk & 1) * 2);
-                        const uint64_t bdesc = smem_desc_sw128(bs + q * C::B_CHUNK + kq * 32);
-                        const uint32_t acc = (st | kk) != 0 ? 1u : 0u;
-                        for (int m = 0; m < C::NMAT; ++m)
-                            tc_mma_mxf4(dt + m * BN, smem_desc_sw128(as + (m * KCH + q) * C::BLK + kq * 32), bdesc,
-                                        idesc, sfc + 8 * KCH * m + (kk >> 1) * 4, sfb + (kk >> 1) * 4, acc);
+                    const uint64_t ad = a_base + (uint32_t)(s * C::A_BYTES >> 4);
+                    const uint64_t bd = b_base + (uint32_t)(s * C::B_BYTES >> 4);
+                    if (ksteps == 4 * KCH) {
+#pragma unroll
+                        for (int kk = 0; kk < 4 * KCH; ++kk) {
+                            const int q = kk >> 2, kq = kk & 3;
+#pragma unroll
+                            for (int m = 0; m < C::NMAT; ++m)
+                                tc_mma_mxf4(dt + m * BN, ad + (((m * KCH + q) * C::BLK + kq * 32) >> 4),
+                                            bd + ((q * C::B_CHUNK + kq * 32) >> 4), (kk & 1) ? id1 : id0,
+                                            sfc + 8 * KCH * m + (kk >> 1) * 4, sfb + (kk >> 1) * 4,
+                                            (st | kk) != 0 ? 1u : 0u);
+                        }
+                    } else {
+                        for (int kk = 0; kk < ksteps; ++kk) {
+                            const int q = kk >> 2, kq = kk & 3;
+                            for (int m = 0; m < C::NMAT; ++m)
+                                tc_mma_mxf4(dt + m * BN, ad + (((m * KCH + q) * C::BLK + kq * 32) >> 4),
+                                            bd + ((q * C::B_CHUNK + kq * 32) >> 4), (kk & 1) ? id1 : id0,
+                                            sfc + 8 * KCH * m + (kk >> 1) * 4, sfb + (kk >> 1) * 4,
+                                            (st | kk) != 0 ? 1u : 0u);
+                        }
                     }
                     tc_commit(&empty[s]);
+                    if (++s == NS) { s = 0; ph ^= 1; }
                 }
                 if (ok_run) tc_commit(&accf[b]);
             }
@@ -469,29 +492,39 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t it = 0, j = 0;
+            // the same lean feed loop as the weight-major kernel's
+            int s = 0;
+            uint32_t ph = 0, j = 0;
             bool ok_run = true;
+            const uint64_t a_base = smem_desc_sw128(smem_u32(smem + C::OFF_A));
+            const uint64_t b_base = smem_desc_sw128(smem_u32(smem + C::OFF_B));
+            constexpr uint32_t id0 = idesc_mxf4(256, 0, 0), id1 = idesc_mxf4(256, 2, 2);
             for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x, ++j) {
                 if (!mbar_wait(acce, (j & 1) ^ 1, abort_flag)) break;
                 tc_fence_after();
-                for (int kc = 0; kc < nc; ++kc, ++it) {
-                    const int s = (int)(it % NS);
-                    const uint32_t r = it / NS;
-                    if (!mbar_wait(&full[s], r & 1, abort_flag) || !mbar_wait(&sfull[s], r & 1, abort_flag)) {
+                for (int kc = 0; kc < nc; ++kc) {
+                    if (!mbar_wait(&full[s], ph, abort_flag) || !mbar_wait(&sfull[s], ph, abort_flag)) {
                         ok_run = false;
                         break;
                     }
                     tc_fence_after();
                     const int rem = (a.K - kc * 256) / 64;
-                    const int ksteps = rem < 4 ? rem : 4;
                     const uint32_t sfc = tmem + 256 + s * C::SF_COLS;
-                    const uint32_t as = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
-                    const uint32_t bs = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
-                    for (int kk = 0; kk < ksteps; ++kk)
-                        tc_mma_mxf4(tmem, smem_desc_sw128(as + kk * 32), smem_desc_sw128(bs + kk * 32),
-                                    idesc_mxf4(256, (kk & 1) * 2, (kk & 1) * 2), sfc + (kk >> 1) * 4,
-                                    sfc + 8 + (kk >> 1) * 8, (kc | kk) != 0 ? 1u : 0u);
+                    const uint64_t ad = a_base + (uint32_t)(s * C::A_BYTES >> 4);
+                    const uint64_t bd = b_base + (uint32_t)(s * C::B_BYTES >> 4);
+                    const uint32_t acc0 = kc != 0 ? 1u : 0u;
+                    if (rem >= 4) {
+                        tc_mma_mxf4(tmem, ad, bd, id0, sfc, sfc + 8, acc0);
+                        tc_mma_mxf4(tmem, ad + 2, bd + 2, id1, sfc, sfc + 8, 1u);
+                        tc_mma_mxf4(tmem, ad + 4, bd + 4, id0, sfc + 4, sfc + 16, 1u);
+                        tc_mma_mxf4(tmem, ad + 6, bd + 6, id1, sfc + 4, sfc + 16, 1u);
+                    } else {
+                        for (int kk = 0; kk < rem; ++kk)
+                            tc_mma_mxf4(tmem, ad + 2 * kk, bd + 2 * kk, (kk & 1) ? id1 : id0, sfc + (kk >> 1) * 4,
+                                        sfc + 8 + (kk >> 1) * 8, (kc | kk) != 0 ? 1u : 0u);
+                    }
                     tc_commit(&empty[s]);
+                    if (++s == NS) { s = 0; ph ^= 1; }
                 }
                 if (ok_run) tc_commit(accf);
             }
