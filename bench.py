@@ -86,11 +86,15 @@ class Layer:
         self.demand = torch.zeros((1, cfg.E), dtype=torch.int64, device="cuda")
         self.miss = torch.zeros((1, cfg.E), dtype=torch.float32, device="cuda")
 
-    def step(self, stream=None):
-        from resident_expert_routed_gb300.layer import layer_step, step_end
+    def step(self, stream=None, side=None):
+        """One layer step; with `side`, the demand update and heavy-miss list run on that second stream,
+        beside the expert FFN, and are joined back before the step ends."""
+        from resident_expert_routed_gb300.layer import join, layer_step, step_end
         layer_step(self.hidden, self.W, self.bias, self.slot_of, self.arena, self.demand, self.miss, 0, self.buf,
-                   stream)
-        step_end(self.miss, self.buf, 0.2, stream)
+                   stream, side)
+        step_end(self.miss, self.buf, 0.2, stream if side is None else side)
+        if side is not None:
+            join(stream, side)
 
 
 class ClockSampler:
@@ -225,17 +229,17 @@ def timed_graph_steps(layer: Layer, K: int, W: int, scratch, ws: int):
     """Returns (per-step ms list, launches per step, distinct slots per step)."""
     import torch
     import resident_expert_routed_gb300 as moe
-    stream = torch.cuda.Stream()
+    stream, side = torch.cuda.Stream(), torch.cuda.Stream()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for i in range(max(W, 1)):
             layer.hidden.copy_(layer.pool[i % len(layer.pool)])
-            layer.step(stream)
+            layer.step(stream, side)
     stream.synchronize()
     graph = torch.cuda.CUDAGraph()
     n0 = moe.moe_kernel_launches()
     with torch.cuda.graph(graph, stream=stream):
-        layer.step(stream)
+        layer.step(stream, side)
     launches = moe.moe_kernel_launches() - n0
     torch.cuda.synchronize()
     for i in range(3):                     # graph warm-up
@@ -288,14 +292,14 @@ def e2e_steps(layer: Layer, K: int, scratch):
     import torch
     host_in = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in layer.pool_np]
     host_out = torch.empty((layer.T, layer.cfg.d), dtype=torch.float32).pin_memory()
-    stream = torch.cuda.current_stream()
+    stream, side = torch.cuda.current_stream(), torch.cuda.Stream()
     total = 0.0
     for i in range(K):
         flush_l2(scratch)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         layer.hidden.copy_(host_in[i % len(host_in)], non_blocking=True)
-        layer.step(stream)
+        layer.step(stream, side)
         host_out.copy_(layer.buf.out, non_blocking=True)
         b.record(stream)
         b.synchronize()

@@ -572,35 +572,43 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
             const int pos = pos0 + row;
             const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
             const int fb0 = warp < 4 ? 0 : 2;
-            for (int fb = fb0; fb < fb0 + 2; ++fb) {                // 2 of the 4 blocks of 32 features
+            // 2 of the 4 blocks of 32 features: SwiGLU of both into registers, then the
+            // accumulator is released to the next item's MMAs before the MXFP4 blocks are
+            // formed and stored
+            float h[2][32];
+            float amax[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int fb = fb0 + q2;
                 uint32_t g0[16], g1[16], u0[16], u1[16];
                 tc_ld_x16(trow + 32 * fb, g0);
                 tc_ld_x16(trow + 32 * fb + 16, g1);
                 tc_ld_x16(trow + 128 + 32 * fb, u0);
                 tc_ld_x16(trow + 128 + 32 * fb + 16, u1);
                 tc_wait_ld();
-                float h[32];
-                float amax = 0.0f;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    h[i] = silu_mul(__uint_as_float(i < 16 ? g0[i] : g1[i - 16]),
-                                    __uint_as_float(i < 16 ? u0[i] : u1[i - 16]));
-                    amax = fmaxf(amax, fabsf(h[i]));
-                }
-                const int X = mx_shared_exp(amax);
-                const float inv = exp2_int(-X);
-                uint32_t wd[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) wd[q] = e2m1x8(h + q * 8, inv);
-                if (row < nv) {
-                    const int f = mt * 128 + 32 * fb;
-                    *reinterpret_cast<uint4*>(a.hq + (size_t)pos * (a.F / 2) + f / 2) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-                    a.hsp[operand_scale_offset(pos, f / 32, BN, a.F)] = (uint8_t)(X + 127);
+                    h[q2][i] = silu_mul(__uint_as_float(i < 16 ? g0[i] : g1[i - 16]),
+                                        __uint_as_float(i < 16 ? u0[i] : u1[i - 16]));
+                    amax[q2] = fmaxf(amax[q2], fabsf(h[q2][i]));
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce);
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int X = mx_shared_exp(amax[q2]);
+                const float inv = exp2_int(-X);
+                uint32_t wd[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) wd[q] = e2m1x8(h[q2] + q * 8, inv);
+                if (row < nv) {
+                    const int f = mt * 128 + 32 * (fb0 + q2);
+                    *reinterpret_cast<uint4*>(a.hq + (size_t)pos * (a.F / 2) + f / 2) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                    a.hsp[operand_scale_offset(pos, f / 32, BN, a.F)] = (uint8_t)(X + 127);
+                }
+            }
         }
     }
 

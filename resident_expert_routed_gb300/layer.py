@@ -1,4 +1,4 @@
-"""One routed-MoE layer step as a sequence of C-ABI calls on one stream.
+"""One routed-MoE layer step as a sequence of C-ABI calls on one stream (or two).
 
 TideLM README, "How adaptive expert loading works", items 1-3, per layer:
 route to resident experts (with substitution), record demand and miss shares,
@@ -34,13 +34,30 @@ class LayerBuffers:
 
 
 def layer_step(hidden: torch.Tensor, w_router: torch.Tensor, bias, slot_of: torch.Tensor, arena: Arena,
-               demand: torch.Tensor, miss_max: torch.Tensor, layer: int, buf: LayerBuffers, stream=None) -> torch.Tensor:
-    """route -> demand -> expert FFN; returns buf.out (fp32 [T, d])."""
+               demand: torch.Tensor, miss_max: torch.Tensor, layer: int, buf: LayerBuffers, stream=None,
+               side=None) -> torch.Tensor:
+    """route -> demand -> expert FFN; returns buf.out (fp32 [T, d]).
+
+    With a second stream `side`, the demand update runs there, beside the
+    expert FFN (it reads only the routing outputs). The caller then runs
+    ``step_end`` on `side` too and calls ``join(stream, side)`` before the next
+    step's routing rewrites want_e / want_s, or before it reads the tables.
+    """
+    main = torch.cuda.current_stream() if stream is None else stream
     moe_route_resident(hidden, w_router, bias, slot_of, buf.k, buf.want_e, buf.want_s, buf.sel_e, buf.sel_slot,
-                       buf.sel_w, buf.workspace, stream)
-    moe_demand_accumulate(buf.want_e, buf.want_s, slot_of, layer, demand, miss_max, stream)
-    moe_expert_ffn_mxfp4(hidden, buf.sel_slot, buf.sel_w, arena, buf.out, buf.workspace, stream)
+                       buf.sel_w, buf.workspace, main)
+    if side is None:
+        moe_demand_accumulate(buf.want_e, buf.want_s, slot_of, layer, demand, miss_max, main)
+    else:
+        side.wait_stream(main)
+        moe_demand_accumulate(buf.want_e, buf.want_s, slot_of, layer, demand, miss_max, side)
+    moe_expert_ffn_mxfp4(hidden, buf.sel_slot, buf.sel_w, arena, buf.out, buf.workspace, main)
     return buf.out
+
+
+def join(stream, side) -> None:
+    """The main stream waits for the side stream's demand and heavy-miss work."""
+    (torch.cuda.current_stream() if stream is None else stream).wait_stream(side)
 
 
 def step_end(miss_max: torch.Tensor, buf: LayerBuffers, threshold: float = 0.2, stream=None):

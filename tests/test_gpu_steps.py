@@ -197,3 +197,69 @@ def test_full_decode_step_shared_arena_replan():
     assert ok, (fro, mx)
     del arena
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T", [8, 130])
+def test_side_stream_step_matches_one_stream(T):
+    # the demand update and heavy-miss list on a second stream, forked after routing and joined at the
+    # end of the step, eagerly and under CUDA graph capture: every output equals the one-stream step's
+    from resident_expert_routed_gb300.layer import join
+    cfg = synth.TINY
+    x = [hidden_dev(synth.hidden_bf16(cfg.seed, T, cfg.d, stream=s)) for s in range(3)]
+    W, b = to_dev(synth.router_weights(cfg.seed, cfg.E, cfg.d)), to_dev(synth.router_bias(cfg.seed, cfg.E, cfg.sigma))
+    res = synth.resident_set(cfg, synth.router_bias(cfg.seed, cfg.E, cfg.sigma))
+    n_slots = cfg.resident
+    slot_of = synth.slot_table(cfg, res, n_slots)
+    owner = np.full(n_slots, -1, np.int32)
+    owner[slot_of[res]] = res
+    arena = _arena(cfg, n_slots, owner)
+    so = to_dev(slot_of)
+
+    def run(side, graph):
+        buf = LayerBuffers(T, cfg.k, cfg.E, cfg.d, cfg.ffn, n_slots)
+        demand = torch.zeros((1, cfg.E), dtype=torch.int64, device="cuda")
+        miss = torch.zeros((1, cfg.E), dtype=torch.float32, device="cuda")
+        hidden = torch.empty_like(x[0])
+        main = torch.cuda.Stream()
+        outs = []
+
+        def step():
+            layer_step(hidden, W, b, so, arena, demand, miss, 0, buf, main, side)
+            step_end(miss, buf, 0.2, main if side is None else side)
+            if side is not None:
+                join(main, side)
+
+        g = None
+        if graph:
+            hidden.copy_(x[0])
+            torch.cuda.synchronize()
+            with torch.cuda.stream(main):
+                step()                                    # warm-up outside the capture
+            main.synchronize()
+            demand.zero_()
+            miss.zero_()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=main):
+                step()
+        for i in range(3):
+            torch.cuda.synchronize()
+            hidden.copy_(x[i])
+            torch.cuda.synchronize()
+            if g is not None:
+                g.replay()
+            else:
+                with torch.cuda.stream(main):
+                    step()
+            torch.cuda.synchronize()
+            n = int(buf.hot_n.item())
+            outs.append((buf.out.cpu().clone(), buf.sel_slot.cpu().clone(), demand.cpu().clone(), miss.cpu().clone(),
+                         buf.hot_flat.cpu()[:n].clone()))
+        return outs
+
+    ref = run(None, False)
+    for side, graph in ((torch.cuda.Stream(), False), (torch.cuda.Stream(), True)):
+        got = run(side, graph)
+        for r, g in zip(ref, got):
+            for a, c in zip(r, g):
+                assert torch.equal(a, c)
+    assert moe.moe_device_status() == (moe.MOE_OK, 0)
