@@ -238,13 +238,24 @@ __global__ void __launch_bounds__(256) route_select_cta(const float* __restrict_
     float acc[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) acc[i] = 0.0f;
-    for (int z = warp; z < splits; z += 8) {
-        const float* pz = partial + ((size_t)z * T + t) * E;
+    // slices warp, warp + 8, ...: up to four rounds' loads are issued before they are summed (in order)
+    for (int z0 = warp; z0 < splits; z0 += 32) {
+        float v[4][VPL];
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E) acc[i] += pz[e];
+        for (int q = 0; q < 4; ++q) {
+            const int z = z0 + 8 * q;
+            const float* pz = partial + ((size_t)z * T + t) * E;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                const int e = lane + 32 * i;
+                v[q][i] = (z < splits && e < E) ? pz[e] : 0.0f;
+            }
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (z0 + 8 * q < splits)
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) acc[i] += v[q][i];
     }
 #pragma unroll
     for (int i = 0; i < VPL; ++i) part[warp][lane + 32 * i] = acc[i];
