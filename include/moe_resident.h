@@ -115,10 +115,14 @@ typedef struct {
  * when fewer than k experts are resident the tail is (-1, -1, 0).
  * workspace: >= moe_workspace_bytes(T, k, d, ffn, E, S) bytes (any ffn, S).
  * hidden_bf16, w_router and workspace must be 16-byte aligned (MOE_EINVAL).
- * Batches of more than 64 tokens with d % 64 == 0 and E % 16 == 0 are scored
- * on the tensor cores: W_r is split exactly into three bf16 parts in the
- * workspace and the products are accumulated in fp32, so the logits match
- * the CUDA-core path up to fp32 rounding order.
+ * hidden_bf16 may be device memory or page-locked host memory (cudaHostAlloc,
+ * cudaHostRegister), which the kernels read directly; pageable host memory is
+ * refused (MOE_EINVAL).
+ * Batches of more than 64 tokens with d % 64 == 0 and E % 16 == 0 in device
+ * memory are scored on the tensor cores: W_r is split exactly into three bf16
+ * parts in the workspace and the products are accumulated in fp32, so the
+ * logits match the CUDA-core path up to fp32 rounding order. A batch in host
+ * memory is always scored on the CUDA cores.
  * Limits: 1 <= k <= 32, k <= E <= 1024, d % 32 == 0, T >= 1.
  */
 moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, const float* bias,
@@ -202,7 +206,10 @@ moe_status moe_hot_miss_select(float* miss_max, int L, int E, float threshold, i
  *   out[t] = sum_j sel_w[t,j] * y(t, j)   (j = 0..k-1 in order: deterministic)
  * hidden_bf16 [T,d]; sel_slot, sel_w [T,k] (as from moe_route_resident);
  * arena: HOST pointer, see moe_arena; out fp32 [T,d] (fully overwritten;
- * a token with no pick gets zeros).
+ * a token with no pick gets zeros). hidden_bf16 and out may be device memory
+ * or page-locked host memory, which the kernels read and write directly (the
+ * batch is read once, the output written once); pageable host memory is
+ * refused (MOE_EINVAL).
  * workspace: >= moe_workspace_bytes(T, k, d, ffn, E, arena->n_slots).
  * Limits: 1 <= k <= 32, T*k <= 2^20, n_slots <= 16384, d and ffn multiples of
  * 128, d <= 16384, ffn <= 16384.

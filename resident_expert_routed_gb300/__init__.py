@@ -108,11 +108,12 @@ def _check(fn: str, st: int) -> None:
         raise MoeError(fn, st, load().moe_status_str(st).decode())
 
 
-def _ptr(t):
+def _ptr(t, host_ok: bool = False):
+    """Pointer of a contiguous CUDA tensor (or, with host_ok, of a pinned host tensor the kernels read directly)."""
     if t is None:
         return None
-    if not t.is_cuda:
-        raise ValueError("expected a CUDA tensor")
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError("expected a CUDA tensor" + (" or a pinned host tensor" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError("expected a contiguous tensor")
     return ctypes.c_void_p(t.data_ptr())
@@ -156,7 +157,7 @@ def moe_route_resident(hidden_bf16, w_router, bias, slot_of, k, want_e, want_s, 
     T, d = hidden_bf16.shape
     E = w_router.shape[0]
     _check("moe_route_resident", load().moe_route_resident(
-        _ptr(hidden_bf16), _ptr(w_router), _ptr(bias), _ptr(slot_of), T, d, E, k, _ptr(want_e), _ptr(want_s),
+        _ptr(hidden_bf16, True), _ptr(w_router), _ptr(bias), _ptr(slot_of), T, d, E, k, _ptr(want_e), _ptr(want_s),
         _ptr(sel_e), _ptr(sel_slot), _ptr(sel_w), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
 
@@ -172,7 +173,7 @@ def moe_route_resident_noalloc(hidden_bf16, w_router, bias, slot_of, k, want_e, 
     T, d = hidden_bf16.shape
     E = w_router.shape[0]
     _check("moe_route_resident_noalloc", load().moe_route_resident_noalloc(
-        _ptr(hidden_bf16), _ptr(w_router), _ptr(bias), _ptr(slot_of), T, d, E, k, _ptr(want_e), _ptr(want_s),
+        _ptr(hidden_bf16, True), _ptr(w_router), _ptr(bias), _ptr(slot_of), T, d, E, k, _ptr(want_e), _ptr(want_s),
         _ptr(sel_e), _ptr(sel_slot), _ptr(sel_w), _stream(stream)))
 
 
@@ -196,7 +197,7 @@ def moe_expert_ffn_mxfp4(hidden_bf16, sel_slot, sel_w, arena: Arena, out, worksp
     k = sel_slot.shape[1]
     st = arena.struct()
     _check("moe_expert_ffn_mxfp4", load().moe_expert_ffn_mxfp4(
-        _ptr(hidden_bf16), _ptr(sel_slot), _ptr(sel_w), ctypes.byref(st), T, k, _ptr(out), _ptr(workspace),
+        _ptr(hidden_bf16, True), _ptr(sel_slot), _ptr(sel_w), ctypes.byref(st), T, k, _ptr(out, True), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 

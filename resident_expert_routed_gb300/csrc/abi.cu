@@ -90,12 +90,33 @@ FfnCarve ffn_carve(int T, int k, int d, int F, int S) {
 }
 
 // Routing workspace: the split-K partial logits of the CUDA-core router, or,
-// for batches the tensor-core router takes, its three bf16 parts of W_r
-// followed by its partials.
+// for batches the tensor-core router can take, the larger of that and its
+// three bf16 parts of W_r followed by its partials (a batch in host memory is
+// always scored by the CUDA-core router).
 size_t route_bytes(int T, int E, int d) {
-    if (!router_tc_eligible(T, E, d)) return align_up((size_t)route_splits(T, E, d) * T * E * 4, 256);
-    return router_tc_split_bytes(E, d) + align_up((size_t)router_tc_splits(T, E, d) * T * E * 4, 256);
+    const size_t simt = align_up((size_t)route_splits(T, E, d) * T * E * 4, 256);
+    if (!router_tc_eligible(T, E, d)) return simt;
+    return std::max(simt, router_tc_split_bytes(E, d) + align_up((size_t)router_tc_splits(T, E, d) * T * E * 4, 256));
 }
+
+}  // namespace
+
+// Where a caller's buffer lives: 0 device memory (or a pointer the runtime does
+// not know, e.g. without a device), 1 page-locked host memory that the kernels
+// read and write directly (over the chip-to-chip link on this platform), -1
+// pageable host memory, which they cannot touch.
+int pointer_kind(const void* p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (at.type == cudaMemoryTypeHost) return 1;
+    if (at.type == cudaMemoryTypeUnregistered) return -1;
+    return 0;
+}
+
+namespace {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ECUDA; }
 
@@ -242,6 +263,8 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
     if (E > 1024) return MOE_EUNSUPPORTED;
     if ((size_t)T * E > ((size_t)1 << 31)) return MOE_EUNSUPPORTED;
     if (ws_bytes < route_bytes(T, E, d)) return MOE_ENOMEM;
+    const int hk = pointer_kind(hidden_bf16);
+    if (hk < 0) return MOE_EINVAL;
     RouteLaunch a{};
     a.x = static_cast<const uint16_t*>(hidden_bf16);
     a.w = w_router;
@@ -253,7 +276,7 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
     a.partial = static_cast<float*>(workspace);
     a.err = err_word();
     if (!a.err) return MOE_ECUDA;
-    if (router_tc_eligible(T, E, d)) {
+    if (hk == 0 && router_tc_eligible(T, E, d)) {     // the tensor maps need device memory
         a.wsplit = workspace;
         a.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + router_tc_split_bytes(E, d));
         a.splits = router_tc_splits(T, E, d);
@@ -300,6 +323,7 @@ moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot
     if (S > 16384 || d > 16384 || F > 16384 || (long)T * k > (1L << 20)) return MOE_EUNSUPPORTED;
     const FfnCarve c = ffn_carve(T, k, d, F, S);
     if (ws_bytes < c.total) return MOE_ENOMEM;
+    if (pointer_kind(hidden_bf16) < 0 || pointer_kind(out) < 0) return MOE_EINVAL;
     uint32_t* err = err_word();
     if (!err) return MOE_ECUDA;
     uint8_t* w = static_cast<uint8_t*>(workspace);

@@ -301,6 +301,7 @@ struct RouteLaunch {
     uint32_t* err;          // device error word (tensor-core router's bounded waits)
 };
 bool router_tc_eligible(int T, int E, int d);
+int pointer_kind(const void* p);      // 0 device, 1 page-locked host, -1 pageable host
 int router_tc_splits(int T, int E, int d);
 size_t router_tc_split_bytes(int E, int d);
 cudaError_t launch_router_tc(const uint16_t* x, const float* W, int T, int d, int E, int splits, void* wsplit,

@@ -390,6 +390,7 @@ extern "C" moe_status moe_route_resident_noalloc(const void* hidden_bf16, const 
     if (E > 1024) return MOE_EUNSUPPORTED;
     const int splits = route_splits(T, E, d);
     if ((size_t)splits * T * E > kNoAllocPartials) return MOE_EUNSUPPORTED;   // beyond the fixed array
+    if (pointer_kind(hidden_bf16) < 0) return MOE_EINVAL;
     float* partials = nullptr;
     if (noalloc_partials(&partials) != cudaSuccess) return MOE_ECUDA;
     RouteLaunch a{};

@@ -35,8 +35,11 @@ class LayerBuffers:
 
 def layer_step(hidden: torch.Tensor, w_router: torch.Tensor, bias, slot_of: torch.Tensor, arena: Arena,
                demand: torch.Tensor, miss_max: torch.Tensor, layer: int, buf: LayerBuffers, stream=None,
-               side=None) -> torch.Tensor:
-    """route -> demand -> expert FFN; returns buf.out (fp32 [T, d]).
+               side=None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """route -> demand -> expert FFN; returns the output (fp32 [T, d]): buf.out, or `out` when given.
+
+    `hidden` and `out` may be pinned host tensors: the kernels then read the
+    batch and write the output in host memory directly.
 
     With a second stream `side`, the demand update runs there, beside the
     expert FFN (it reads only the routing outputs). The caller then runs
@@ -51,8 +54,9 @@ def layer_step(hidden: torch.Tensor, w_router: torch.Tensor, bias, slot_of: torc
     else:
         side.wait_stream(main)
         moe_demand_accumulate(buf.want_e, buf.want_s, slot_of, layer, demand, miss_max, side)
-    moe_expert_ffn_mxfp4(hidden, buf.sel_slot, buf.sel_w, arena, buf.out, buf.workspace, main)
-    return buf.out
+    dst = buf.out if out is None else out
+    moe_expert_ffn_mxfp4(hidden, buf.sel_slot, buf.sel_w, arena, dst, buf.workspace, main)
+    return dst
 
 
 def join(stream, side) -> None:
@@ -64,3 +68,61 @@ def step_end(miss_max: torch.Tensor, buf: LayerBuffers, threshold: float = 0.2, 
     """Heavy-miss list of the step (README item 3); resets miss_max."""
     moe_hot_miss_select(miss_max, threshold, buf.cap, buf.hot_flat, buf.hot_share, buf.hot_n, stream)
     return buf.hot_flat, buf.hot_share, buf.hot_n
+
+
+class CapturedStep:
+    """A layer step captured once in a CUDA graph and replayed.
+
+    Each replay takes a batch from a pinned host buffer, runs the step (the
+    demand update and heavy-miss list on a side stream), and leaves the fp32
+    output in the pinned ``host_out``: one graph launch per step instead of one
+    host call per kernel. With ``zero_copy`` (the default) the kernels read the
+    batch and write the output in host memory directly; otherwise the graph
+    copies the batch in and the output out with the copy engines around a
+    device-resident step. Everything the step touches is fixed at
+    capture (weights, tables, arena, demand and miss tables, ``buf``, the host
+    buffers); ``run(i)`` replays the graph of ``host_inputs[i]``, whose contents
+    the caller may rewrite between replays. Construction runs one eager step
+    (it updates the demand and miss tables like any step) before capturing.
+    """
+
+    def __init__(self, host_inputs, w_router: torch.Tensor, bias, slot_of: torch.Tensor, arena: Arena,
+                 demand: torch.Tensor, miss_max: torch.Tensor, layer: int, buf: LayerBuffers,
+                 host_out: torch.Tensor | None = None, threshold: float = 0.2, zero_copy: bool = True):
+        T, d = host_inputs[0].shape
+        for h in host_inputs:
+            if not h.is_pinned() or h.shape != (T, d) or h.dtype != torch.bfloat16:
+                raise ValueError("host inputs must be pinned bf16 [T, d] tensors of one shape")
+        self.main, self.side = torch.cuda.Stream(), torch.cuda.Stream()
+        self.hidden = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+        self.host_out = host_out if host_out is not None else torch.empty((T, d), dtype=torch.float32).pin_memory()
+        self.buf = buf
+
+        def body(h_in):
+            if zero_copy:
+                layer_step(h_in, w_router, bias, slot_of, arena, demand, miss_max, layer, buf, self.main, self.side,
+                           out=self.host_out)
+            else:
+                self.hidden.copy_(h_in, non_blocking=True)
+                layer_step(self.hidden, w_router, bias, slot_of, arena, demand, miss_max, layer, buf, self.main,
+                           self.side)
+            step_end(miss_max, buf, threshold, self.side)
+            join(self.main, self.side)
+            if not zero_copy:
+                self.host_out.copy_(buf.out, non_blocking=True)
+
+        self.main.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(self.main):
+            body(host_inputs[0])
+        self.main.synchronize()
+        self.graphs = []
+        for h in host_inputs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.main):
+                body(h)
+            self.graphs.append(g)
+
+    def run(self, i: int = 0) -> torch.Tensor:
+        """Replay the step for host_inputs[i] on the current stream; host_out is valid after a sync."""
+        self.graphs[i].replay()
+        return self.host_out

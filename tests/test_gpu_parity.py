@@ -326,3 +326,59 @@ def test_bad_slot_id_sets_error_word_and_is_skipped():
     exp = oracle.ffn(c.x, sel_u, w.astype(np.float32).astype(np.float64), experts, c.cfg.d, c.cfg.ffn)
     ok, fro, mx = ffn_within_tolerance(out.cpu().numpy().astype(np.float64), exp)
     assert ok, (fro, mx)
+
+
+def test_route_and_ffn_read_a_pinned_host_batch():
+    # a batch in page-locked host memory: the kernels read it directly (routing on the CUDA cores even above
+    # 64 tokens, where a device batch takes the tensor-core router); the FFN output, also written to pinned host
+    # memory, equals the device-buffer call's bit for bit
+    cfg, T = synth.TINY, 130
+    c = make_case(cfg, T)
+    arena = device_arena(cfg, c.owner, c.n_slots)
+    host_x = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    k = cfg.k
+    ws = torch.empty(moe.moe_workspace_bytes(T, k, cfg.d, cfg.ffn, cfg.E, c.n_slots), dtype=torch.uint8,
+                     device="cuda")
+    outs = {}
+    for name, x in (("device", hidden_dev(c.x)), ("host", host_x)):
+        want_e = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        want_s = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        sel_e = torch.empty_like(want_e)
+        sel_slot = torch.empty_like(want_e)
+        sel_w = torch.empty_like(want_s)
+        moe.moe_route_resident(x, to_dev(c.W), to_dev(c.bias), to_dev(c.slot_of), k, want_e, want_s, sel_e,
+                               sel_slot, sel_w, ws)
+        torch.cuda.synchronize()
+        g = dict(want_e=want_e.cpu().numpy(), want_s=want_s.cpu().numpy(), sel_e=sel_e.cpu().numpy(),
+                 sel_slot=sel_slot.cpu().numpy(), sel_w=sel_w.cpu().numpy())
+        check_route(c, g, np.arange(T))
+        outs[name] = g
+    # the FFN on the same picks (the device routing's) from both buffers
+    sel_slot = to_dev(outs["device"]["sel_slot"])
+    sel_w = to_dev(outs["device"]["sel_w"])
+    out_dev = torch.empty((T, cfg.d), dtype=torch.float32, device="cuda")
+    out_host = torch.empty((T, cfg.d), dtype=torch.float32).pin_memory()
+    moe.moe_expert_ffn_mxfp4(hidden_dev(c.x), sel_slot, sel_w, arena, out_dev, ws)
+    moe.moe_expert_ffn_mxfp4(host_x, sel_slot, sel_w, arena, out_host, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_dev.cpu(), out_host)
+    assert moe.moe_device_status() == (moe.MOE_OK, 0)
+
+
+def test_pageable_host_batch_is_refused():
+    # the C ABI refuses a batch in pageable host memory before launching anything
+    import ctypes
+    cfg, T = synth.TINY, 8
+    c = make_case(cfg, T)
+    x_pageable = np.ascontiguousarray(c.x)
+    k = cfg.k
+    ws = torch.empty(moe.moe_workspace_bytes(T, k, cfg.d, cfg.ffn, cfg.E, c.n_slots), dtype=torch.uint8,
+                     device="cuda")
+    outs = [torch.empty((T, k), dtype=dt, device="cuda") for dt in (torch.int32, torch.float32, torch.int32,
+                                                                     torch.int32, torch.float32)]
+    W, bias, so = to_dev(c.W), to_dev(c.bias), to_dev(c.slot_of)
+    P = ctypes.c_void_p
+    st = moe.load().moe_route_resident(
+        P(x_pageable.ctypes.data), P(W.data_ptr()), P(bias.data_ptr()), P(so.data_ptr()), T, cfg.d, cfg.E, k,
+        *[P(o.data_ptr()) for o in outs], P(ws.data_ptr()), ws.numel(), P(torch.cuda.current_stream().cuda_stream))
+    assert st == moe.MOE_EINVAL

@@ -263,3 +263,53 @@ def test_side_stream_step_matches_one_stream(T):
             for a, c in zip(r, g):
                 assert torch.equal(a, c)
     assert moe.moe_device_status() == (moe.MOE_OK, 0)
+
+
+@pytest.mark.parametrize("zero_copy", [True, False], ids=["zero-copy", "copies"])
+def test_captured_step_matches_eager_steps(zero_copy):
+    # CapturedStep (the batch read from pinned host memory by the kernels, or copied in and out by the graph,
+    # around the two-stream step, one CUDA graph per host buffer): its host output, demand and miss tables and
+    # heavy-miss list equal those of eager one-stream steps on device copies of the same batches
+    from resident_expert_routed_gb300.layer import CapturedStep
+    cfg, T = synth.TINY, 40
+    xs = [synth.hidden_bf16(cfg.seed, T, cfg.d, stream=s) for s in range(3)]
+    host = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs]
+    W, b = to_dev(synth.router_weights(cfg.seed, cfg.E, cfg.d)), to_dev(synth.router_bias(cfg.seed, cfg.E, cfg.sigma))
+    res = synth.resident_set(cfg, synth.router_bias(cfg.seed, cfg.E, cfg.sigma))
+    slot_of = synth.slot_table(cfg, res, cfg.resident)
+    owner = np.full(cfg.resident, -1, np.int32)
+    owner[slot_of[res]] = res
+    arena = _arena(cfg, cfg.resident, owner)
+    so = to_dev(slot_of)
+
+    def tables():
+        return (torch.zeros((1, cfg.E), dtype=torch.int64, device="cuda"),
+                torch.zeros((1, cfg.E), dtype=torch.float32, device="cuda"))
+
+    # eager: the capture's own warm-up step (batch 0), then batches 1, 2, 0
+    buf_e = LayerBuffers(T, cfg.k, cfg.E, cfg.d, cfg.ffn, cfg.resident)
+    dem_e, miss_e = tables()
+    ref = []
+    for i in (0, 1, 2, 0):
+        layer_step(hidden_dev(xs[i]), W, b, so, arena, dem_e, miss_e, 0, buf_e)
+        step_end(miss_e, buf_e, 0.2)
+        torch.cuda.synchronize()
+        n = int(buf_e.hot_n.item())
+        ref.append((buf_e.out.cpu().clone(), dem_e.cpu().clone(), miss_e.cpu().clone(), buf_e.hot_flat.cpu()[:n].clone()))
+
+    buf_c = LayerBuffers(T, cfg.k, cfg.E, cfg.d, cfg.ffn, cfg.resident)
+    dem_c, miss_c = tables()
+    cap = CapturedStep(host, W, b, so, arena, dem_c, miss_c, 0, buf_c, zero_copy=zero_copy)
+    got = []
+    torch.cuda.synchronize()
+    n = int(buf_c.hot_n.item())
+    got.append((cap.host_out.clone(), dem_c.cpu().clone(), miss_c.cpu().clone(), buf_c.hot_flat.cpu()[:n].clone()))
+    for i in (1, 2, 0):
+        out = cap.run(i)
+        torch.cuda.synchronize()
+        n = int(buf_c.hot_n.item())
+        got.append((out.clone(), dem_c.cpu().clone(), miss_c.cpu().clone(), buf_c.hot_flat.cpu()[:n].clone()))
+    for r, g in zip(ref, got):
+        for a, c in zip(r, g):
+            assert torch.equal(a, c)
+    assert moe.moe_device_status() == (moe.MOE_OK, 0)
