@@ -119,7 +119,7 @@ struct Cfg {
     static constexpr int B_CHUNK = BN * 128;
     static constexpr int B_BYTES = KCH * B_CHUNK;
     static constexpr int NV = (NMAT + 1) * 2 * KCH;        // scale atoms per stage (weights, then activations)
-    static constexpr int PF = 4 / KCH;                     // stages of scales loaded ahead
+    static constexpr int PF = 4;                           // stages of scales loaded ahead (registers: 4 NV uint4)
     static constexpr int SF_COLS = 4 * NV;                 // TMEM columns of one stage's scales
     static constexpr int ACC_COLS = NMAT * BN;    // one accumulator buffer (gate, then up)
     static constexpr int OFF_A = 0;
