@@ -65,13 +65,14 @@ __global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restri
                                                          int32_t* __restrict__ pair_of_pos,
                                                          int32_t* __restrict__ seg, int32_t* __restrict__ tile_off,
                                                          int4* __restrict__ work, int32_t* __restrict__ n_work,
-                                                         uint32_t* err) {
+                                                         int late_trigger, uint32_t* err) {
     extern __shared__ int32_t cnt[];
     __shared__ unsigned long long scan_scratch[32];
     const int tid = threadIdx.x;
-    pdl_trigger();
+    if (!late_trigger) pdl_trigger();
     for (int i = tid; i < S; i += PLAN_THREADS) cnt[i] = 0;
     pdl_wait();
+    if (late_trigger) pdl_trigger();    // after the wait: the pack, launched now, may read x before its own wait
     __syncthreads();
     for (int p = tid; p < P; p += PLAN_THREADS) {
         int s = sel_slot[p];
@@ -136,8 +137,8 @@ __global__ void __launch_bounds__(256) plan_place(const int32_t* __restrict__ se
                                                   const int32_t* __restrict__ cta_offsets,
                                                   const int32_t* __restrict__ seg, int32_t* __restrict__ pos_of_pair,
                                                   int32_t* __restrict__ pair_of_pos) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();          // after the wait: the pack, launched now, reads x before its own wait
     const int g = blockIdx.y;
     const int p1 = min(P, (g + 1) * chunk);
     for (int p = g * chunk + blockIdx.x * blockDim.x + threadIdx.x; p < p1; p += gridDim.x * blockDim.x) {
@@ -154,50 +155,51 @@ __global__ void __launch_bounds__(256) plan_place(const int32_t* __restrict__ se
 // operand row of each of the token's picks. The four scale bytes of a
 // 128-element group sit side by side in the tile's scale atom; d is a multiple
 // of 128, so lanes 4g..4g+3 of a warp hold one group of one token and lane 4g
-// stores the four bytes as one word. Whole warps iterate together (the
-// shuffles need every lane), each lane predicated on its own element.
+// stores the four bytes as one word.
+// With `early` the quantisation runs before the wait for the plan: the plan
+// kernel before this one then signals its dependents only after its own wait,
+// so this kernel starts once every kernel before the plan, including whatever
+// wrote x, has finished; only the positions need the plan. Small batches (too
+// little to quantise to hide the later launch) wait first.
 __global__ void __launch_bounds__(256) ffn_pack(const uint16_t* __restrict__ x, const int32_t* __restrict__ pos_of_pair,
-                                                int T, int k, int d, int bn, uint8_t* __restrict__ xp,
+                                                int T, int k, int d, int bn, int early, uint8_t* __restrict__ xp,
                                                 uint8_t* __restrict__ xsp) {
     pdl_trigger();
-    pdl_wait();
-    const int lane = threadIdx.x & 31;
+    if (!early) pdl_wait();
     const int nb = d / 32;
     const long total = (long)T * nb;
-    const long stride = (long)gridDim.x * blockDim.x;              // a multiple of 32
-    for (long i0 = (long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); i0 < total; i0 += stride) {
-        const long i = i0 + lane;
-        const bool active = i < total;
-        const long t = active ? i / nb : 0;
-        const int b = active ? (int)(i % nb) : 0;
-        uint4 codes = make_uint4(0u, 0u, 0u, 0u);
-        uint32_t byte = 0;
-        if (active) {
-            const uint4* src = reinterpret_cast<const uint4*>(x + t * d + b * 32);
-            uint4 v[4];
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;     // whole warps: the grid covers every task
+    const bool active = i < total;
+    const long t = active ? i / nb : 0;
+    const int b = active ? (int)(i % nb) : 0;
+    uint4 codes = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t byte = 0;
+    if (active) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + t * d + b * 32);
+        uint4 v[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) v[q] = src[q];
-            const uint16_t* h = reinterpret_cast<const uint16_t*>(v);
-            float f[32];
-            float amax = 0.0f;
+        for (int q = 0; q < 4; ++q) v[q] = src[q];
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(v);
+        float f[32];
+        float amax = 0.0f;
 #pragma unroll
-            for (int q = 0; q < 32; ++q) { f[q] = bf16_bits_to_float(h[q]); amax = fmaxf(amax, fabsf(f[q])); }
-            const int X = mx_shared_exp(amax);
-            const float inv = exp2_int(-X);
-            codes = make_uint4(e2m1x8(f, inv), e2m1x8(f + 8, inv), e2m1x8(f + 16, inv), e2m1x8(f + 24, inv));
-            byte = (uint32_t)(X + 127);
-        }
-        uint32_t word = byte;
-        word |= __shfl_down_sync(0xFFFFFFFFu, byte, 1) << 8;
-        word |= __shfl_down_sync(0xFFFFFFFFu, byte, 2) << 16;
-        word |= __shfl_down_sync(0xFFFFFFFFu, byte, 3) << 24;
-        if (!active) continue;
-        for (int j = 0; j < k; ++j) {
-            const int pos = pos_of_pair[t * k + j];
-            if (pos < 0) continue;
-            *reinterpret_cast<uint4*>(xp + (size_t)pos * (d / 2) + b * 16) = codes;
-            if ((b & 3) == 0) *reinterpret_cast<uint32_t*>(xsp + operand_scale_offset(pos, b, bn, d)) = word;
-        }
+        for (int q = 0; q < 32; ++q) { f[q] = bf16_bits_to_float(h[q]); amax = fmaxf(amax, fabsf(f[q])); }
+        const int X = mx_shared_exp(amax);
+        const float inv = exp2_int(-X);
+        codes = make_uint4(e2m1x8(f, inv), e2m1x8(f + 8, inv), e2m1x8(f + 16, inv), e2m1x8(f + 24, inv));
+        byte = (uint32_t)(X + 127);
+    }
+    uint32_t word = byte;
+    word |= __shfl_down_sync(0xFFFFFFFFu, byte, 1) << 8;
+    word |= __shfl_down_sync(0xFFFFFFFFu, byte, 2) << 16;
+    word |= __shfl_down_sync(0xFFFFFFFFu, byte, 3) << 24;
+    if (early) pdl_wait();                                          // positions are the plan's output
+    if (!active) return;
+    for (int j = 0; j < k; ++j) {
+        const int pos = pos_of_pair[t * k + j];
+        if (pos < 0) continue;
+        *reinterpret_cast<uint4*>(xp + (size_t)pos * (d / 2) + b * 16) = codes;
+        if ((b & 3) == 0) *reinterpret_cast<uint32_t*>(xsp + operand_scale_offset(pos, b, bn, d)) = word;
     }
 }
 
@@ -227,6 +229,9 @@ __global__ void __launch_bounds__(256) ffn_combine(const float* __restrict__ Y, 
 
 cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
     const int P = a.T * a.k;
+    // batches of 8 tokens or more quantise x while the plan runs (large batches always: their plan ends
+    // with plan_place, which signals after its wait)
+    const int early = a.plan_ctas > 0 || a.T >= 8 ? 1 : 0;
     const size_t smem = (size_t)a.S * sizeof(int32_t);
     static bool attr_set[64] = {};
     static bool attr_set_multi[64] = {};
@@ -260,16 +265,15 @@ cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
         moe_count_launches(2);
     } else {
         e = moe_launch(ffn_plan, dim3(1), dim3(PLAN_THREADS), smem, s, a.sel_slot, P, a.S, a.bn, a.pos_of_pair,
-                       a.pair_of_pos, a.seg, a.tile_off, a.work, a.n_work, a.err);
+                       a.pair_of_pos, a.seg, a.tile_off, a.work, a.n_work, early, a.err);
     }
     moe_prof_end(MK_PLAN, s);
     if (e != cudaSuccess) return e;
     const long tasks = (long)a.T * (a.d / 32);
-    long blocks = (tasks + 255) / 256;
-    if (blocks > 8L * moe_sm_count()) blocks = 8L * moe_sm_count();
+    const long blocks = (tasks + 255) / 256;                // one task per thread (at most 2^20 * 512 / 256)
     moe_prof_begin(MK_PACK, s);
     e = moe_launch(ffn_pack, dim3((unsigned)blocks), dim3(256), 0, s, a.x, a.pos_of_pair, a.T, a.k, a.d, a.bn,
-                   a.xp, a.xsp);
+                   early, a.xp, a.xsp);
     moe_prof_end(MK_PACK, s);
     moe_count_launches(2);
     return e;
