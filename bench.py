@@ -288,8 +288,8 @@ def profiled_steps(layer: Layer, K: int, scratch):
 
 
 def e2e_steps(layer: Layer, K: int, scratch):
-    """Same metric through the public API with host buffers: each step replays a CapturedStep (pinned H2D of
-    the batch, the layer step, D2H of the output, all in one CUDA graph) and waits for the output."""
+    """Same metric through the public API with host buffers: each step replays a CapturedStep (the kernels read
+    the pinned host batch and write the fp32 output into pinned host memory, one CUDA graph) and waits for it."""
     import torch
     from resident_expert_routed_gb300.layer import CapturedStep
     host_in = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in layer.pool_np]
@@ -541,7 +541,7 @@ def run_ours(args, rank, ws, local):
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": T / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                        "path": "pinned host batch -> CapturedStep replay (H2D, layer_step/step_end through the C ABI, D2H in one CUDA graph) -> pinned host output"},
+                        "path": "pinned host batch, read by the kernels -> CapturedStep replay (layer_step/step_end through the C ABI in one CUDA graph) -> fp32 output written into pinned host memory"},
                 "gpu_launches": launches * args.steps, "clocks": clocks, "kernels": kernels, "sweep": sweep,
                 "wall_s": wall}
         print(json.dumps(line), flush=True)
