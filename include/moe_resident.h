@@ -219,6 +219,21 @@ moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot
                                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Optional, for latency: prefetches into L2 the gate/up weights that
+ * moe_expert_ffn_mxfp4 streams first for these picks. Its plan orders the
+ * work by slot and its gate/up GEMM runs one CTA per SM, so the first round
+ * reads one 128-feature tile of gate and up weights (codes and scales) per SM
+ * from the lowest-numbered slots the picks use; this call prefetches exactly
+ * those blocks, one SM each. Issue it on a second stream right after the
+ * routing, so that HBM serves it while the FFN's plan and pack run (they read
+ * little). It reads sel_slot and the arena and writes nothing: results never
+ * depend on it. sel_slot int32 [T,k]; arena and limits as for
+ * moe_expert_ffn_mxfp4; batches of more than 65,536 picks return MOE_OK
+ * without a launch.
+ */
+moe_status moe_expert_ffn_prefetch(const int32_t* sel_slot, const moe_arena* arena, int T, int k, void* stream);
+
+/*
  * Re-plan of the one shared arena from the demand history (README item 1: the
  * arena is filled from the history and re-planned; "a busy layer takes slots
  * from a quiet one").

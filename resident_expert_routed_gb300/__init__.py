@@ -32,7 +32,7 @@ EXPORTS = ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accum
            "moe_device_status", "moe_status_str", "moe_kernel_launches", "moe_profile_enable",
            "moe_profile_kernel_count", "moe_profile_read", "moe_profile_reset", "moe_demand_decay",
            "moe_demand_save", "moe_demand_load", "moe_hot_ring_create", "moe_hot_ring_step", "moe_hot_ring_destroy",
-           "moe_hot_read_sync", "moe_renormalise_weights")
+           "moe_hot_read_sync", "moe_renormalise_weights", "moe_expert_ffn_prefetch")
 
 
 class MoeError(RuntimeError):
@@ -90,6 +90,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.moe_hot_ring_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_int32)]
     L.moe_hot_ring_destroy.argtypes = [_P]
     L.moe_renormalise_weights.argtypes = [_P, _P, _I, _I, _P]
+    L.moe_expert_ffn_prefetch.argtypes = [_P, ctypes.POINTER(MoeArena), _I, _I, _P]
     L.moe_hot_read_sync.argtypes = [_P, _P, _P, _P, _P, ctypes.POINTER(MoeArena), _I, _I, _I, _F, _P, _P, _P]
     L.moe_demand_save.argtypes = [_P, _I, _I, ctypes.c_char_p, _P]
     L.moe_demand_load.argtypes = [_P, _I, _I, ctypes.c_char_p, _P]
@@ -97,7 +98,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "moe_expert_ffn_mxfp4",
                  "moe_arena_replan", "moe_ring_install", "moe_device_status", "moe_profile_enable",
                  "moe_profile_read", "moe_demand_decay", "moe_demand_save", "moe_demand_load", "moe_hot_ring_create",
-                 "moe_hot_ring_step", "moe_hot_ring_destroy", "moe_hot_read_sync", "moe_renormalise_weights"):
+                 "moe_hot_ring_step", "moe_hot_ring_destroy", "moe_hot_read_sync", "moe_renormalise_weights",
+                 "moe_expert_ffn_prefetch"):
         L[name].restype = _I
     _lib = L
     return L
@@ -307,6 +309,14 @@ def moe_hot_read_sync(store, demand, miss_max, slot_of, owner, arena: Arena, lay
     _check("moe_hot_read_sync", load().moe_hot_read_sync(
         _ptr(store), _ptr(demand), _ptr(miss_max), _ptr(slot_of), _ptr(owner), ctypes.byref(st), layer, L, E,
         float(threshold), _ptr(budget), _ptr(swap), _stream(stream)))
+
+
+def moe_expert_ffn_prefetch(sel_slot, arena: Arena, stream=None) -> None:
+    """L2 prefetch of the gate/up weights the expert FFN streams first for these picks (see the header)."""
+    T, k = sel_slot.shape
+    st = arena.struct()
+    _check("moe_expert_ffn_prefetch", load().moe_expert_ffn_prefetch(_ptr(sel_slot), ctypes.byref(st), T, k,
+                                                                     _stream(stream)))
 
 
 def moe_renormalise_weights(sel_slot, sel_w, stream=None) -> None:

@@ -62,6 +62,7 @@ struct FfnCarve {
 
 // Batches of at least this many picks plan with several CTAs (2048 picks each, at most 64).
 constexpr size_t kPlanMultiPicks = 8192;
+constexpr long kPrefetchMaxPicks = 65536;       // moe_expert_ffn_prefetch scans the picks in every CTA
 
 FfnCarve ffn_carve(int T, int k, int d, int F, int S) {
     FfnCarve c{};
@@ -303,10 +304,9 @@ moe_status moe_hot_miss_select(float* miss_max, int L, int E, float threshold, i
                                        static_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot, const float* sel_w,
-                                const moe_arena* arena, int T, int k, float* out, void* workspace, size_t ws_bytes,
-                                void* stream) {
-    if (!hidden_bf16 || !sel_slot || !sel_w || !arena || !out || !workspace || !arena->base) return MOE_EINVAL;
+// The arena record and batch limits that the expert FFN (and its prefetch) rely on.
+static moe_status arena_status(const moe_arena* arena, int T, int k) {
+    if (!arena->base) return MOE_EINVAL;
     const int d = arena->d, F = arena->ffn, S = arena->n_slots;
     if (T < 1 || k < 1 || k > 32 || d < 128 || F < 128 || d % 128 || F % 128 || S < 1) return MOE_EINVAL;
     if (arena->slot_bytes <= 0 || arena->slot_bytes % 256) return MOE_EINVAL;
@@ -321,6 +321,24 @@ moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot
         !inside(arena->off_dn_scales, dns))
         return MOE_EINVAL;
     if (S > 16384 || d > 16384 || F > 16384 || (long)T * k > (1L << 20)) return MOE_EUNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status moe_expert_ffn_prefetch(const int32_t* sel_slot, const moe_arena* arena, int T, int k, void* stream) {
+    if (!sel_slot || !arena) return MOE_EINVAL;
+    const moe_status as = arena_status(arena, T, k);
+    if (as != MOE_OK) return as;
+    if ((long)T * k > kPrefetchMaxPicks) return MOE_OK;        // large batches: nothing to hide it behind
+    return cuda_status(launch_ffn_prefetch(sel_slot, T * k, *arena, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot, const float* sel_w,
+                                const moe_arena* arena, int T, int k, float* out, void* workspace, size_t ws_bytes,
+                                void* stream) {
+    if (!hidden_bf16 || !sel_slot || !sel_w || !arena || !out || !workspace) return MOE_EINVAL;
+    const moe_status as = arena_status(arena, T, k);
+    if (as != MOE_OK) return as;
+    const int d = arena->d, F = arena->ffn, S = arena->n_slots;
     const FfnCarve c = ffn_carve(T, k, d, F, S);
     if (ws_bytes < c.total) return MOE_ENOMEM;
     if (pointer_kind(hidden_bf16) < 0 || pointer_kind(out) < 0) return MOE_EINVAL;

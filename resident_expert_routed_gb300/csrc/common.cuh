@@ -187,6 +187,11 @@ MOE_DEV void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_
                  : "memory");
 }
 
+// Bulk prefetch of global bytes into L2 (16-byte aligned, a multiple of 16 bytes; no completion).
+MOE_DEV void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)
+                 : "memory");
+}
 MOE_DEV void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -308,6 +313,7 @@ struct FfnLaunch {
     uint32_t* err;
 };
 cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s);
+cudaError_t launch_ffn_prefetch(const int32_t* sel_slot, int P, const moe_arena& ar, cudaStream_t s);
 cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches);
 cudaError_t launch_ffn_combine(const FfnLaunch& a, cudaStream_t s);
 

@@ -225,7 +225,69 @@ __global__ void __launch_bounds__(256) ffn_combine(const float* __restrict__ Y, 
     *reinterpret_cast<float4*>(out + (size_t)t * d + c) = acc;
 }
 
+// Used slots in index order head the plan's work list (its tiles follow the
+// slot order), so the gate/up GEMM's persistent grid streams their weights
+// first: its CTA b takes feature tile b % m_tiles of the (b / m_tiles)-th used
+// slot (one token tile per slot assumed). CTA b of this kernel prefetches the
+// same code blocks and scale atoms into L2, so that the prefetches come from
+// every SM's copy engine at once.
+__global__ void __launch_bounds__(128) ffn_prefetch_first(const int32_t* __restrict__ sel_slot, int P, int S,
+                                                          const uint8_t* __restrict__ arena, long long slot_bytes,
+                                                          long long off_codes, long long off_scales, int m_tiles,
+                                                          int nc, int atoms) {
+    extern __shared__ uint32_t used[];                  // one bit per slot
+    __shared__ int slot;
+    pdl_trigger();
+    const int nw = (S + 31) / 32;
+    for (int i = threadIdx.x; i < nw; i += blockDim.x) used[i] = 0;
+    pdl_wait();
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int s = sel_slot[p];
+        if (s >= 0 && s < S) atomicOr(&used[s >> 5], 1u << (s & 31));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int want = (int)blockIdx.x / m_tiles, found = -1;
+        for (int i = 0; i < nw && found < 0; ++i) {
+            const int c = __popc(used[i]);
+            if (want < c) {
+                uint32_t m = used[i];
+                for (int q = 0; q < want; ++q) m &= m - 1;      // drop the lowest set bits
+                found = i * 32 + __ffs(m) - 1;
+            } else {
+                want -= c;
+            }
+        }
+        slot = found;
+    }
+    __syncthreads();
+    if (slot < 0) return;
+    const int mt = (int)blockIdx.x % m_tiles;
+    const uint8_t* rec = arena + (size_t)slot * slot_bytes;
+    for (int r = threadIdx.x; r < 2 * nc + 2; r += blockDim.x) {
+        if (r < 2 * nc) {
+            const int tile = r < nc ? mt : m_tiles + mt;                // up tiles follow the gate tiles
+            bulk_prefetch_l2(rec + off_codes + ((size_t)tile * nc + r % nc) * 16384, 16384);
+        } else {
+            const int tile = r == 2 * nc ? mt : m_tiles + mt;
+            bulk_prefetch_l2(rec + off_scales + (size_t)tile * atoms * 512, (uint32_t)atoms * 512);
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_ffn_prefetch(const int32_t* sel_slot, int P, const moe_arena& ar, cudaStream_t s) {
+    const int nw = (ar.n_slots + 31) / 32;
+    const cudaError_t e = moe_launch(ffn_prefetch_first, dim3((unsigned)moe_sm_count()), dim3(128),
+                                     (size_t)nw * 4, s, sel_slot, P, ar.n_slots,
+                                     static_cast<const uint8_t*>(ar.base), (long long)ar.slot_bytes,
+                                     (long long)ar.off_gu_codes, (long long)ar.off_gu_scales, ar.ffn / 128,
+                                     (ar.d + 255) / 256, ar.d / 128);
+    moe_count_launches(1);
+    return e;
+}
 
 cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
     const int P = a.T * a.k;

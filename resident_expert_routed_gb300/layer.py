@@ -10,8 +10,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (Arena, moe_demand_accumulate, moe_expert_ffn_mxfp4, moe_hot_miss_select, moe_route_resident,
-               moe_workspace_bytes)
+from . import (Arena, moe_demand_accumulate, moe_expert_ffn_mxfp4, moe_expert_ffn_prefetch, moe_hot_miss_select,
+               moe_route_resident, moe_workspace_bytes)
 
 
 class LayerBuffers:
@@ -41,8 +41,9 @@ def layer_step(hidden: torch.Tensor, w_router: torch.Tensor, bias, slot_of: torc
     `hidden` and `out` may be pinned host tensors: the kernels then read the
     batch and write the output in host memory directly.
 
-    With a second stream `side`, the demand update runs there, beside the
-    expert FFN (it reads only the routing outputs). The caller then runs
+    With a second stream `side`, the L2 prefetch of the weights the FFN reads
+    first and the demand update run there, beside the expert FFN (they read
+    only the routing outputs). The caller then runs
     ``step_end`` on `side` too and calls ``join(stream, side)`` before the next
     step's routing rewrites want_e / want_s, or before it reads the tables.
     """
@@ -53,6 +54,7 @@ def layer_step(hidden: torch.Tensor, w_router: torch.Tensor, bias, slot_of: torc
         moe_demand_accumulate(buf.want_e, buf.want_s, slot_of, layer, demand, miss_max, main)
     else:
         side.wait_stream(main)
+        moe_expert_ffn_prefetch(buf.sel_slot, arena, side)
         moe_demand_accumulate(buf.want_e, buf.want_s, slot_of, layer, demand, miss_max, side)
     dst = buf.out if out is None else out
     moe_expert_ffn_mxfp4(hidden, buf.sel_slot, buf.sel_w, arena, dst, buf.workspace, main)

@@ -167,3 +167,24 @@ def test_demand_history_calls_reject_bad_arguments(tmp_path):
     p.write_bytes(b"MOEDEMD1" + struct.pack("<iiii", 2, 8, 40, 0) + bytes(10))          # truncated
     assert L.moe_demand_load(FAKE, 2, 8, str(p).encode(), NULL) == moe.MOE_EIO
     assert L.moe_demand_save(NULL, 2, 8, str(p).encode(), NULL) == moe.MOE_EINVAL
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=200), moe.MOE_EINVAL),
+    (dict(base=0x100010), moe.MOE_EINVAL),
+    (dict(off_dn_scales=68608), moe.MOE_EINVAL),
+    (dict(n_slots=20000), moe.MOE_EUNSUPPORTED),
+])
+def test_ffn_prefetch_checks_the_arena_like_the_ffn(kw, status):
+    L = moe.load()
+    ar = _arena(**kw)
+    assert L.moe_expert_ffn_prefetch(FAKE, ctypes.byref(ar), 8, 4, NULL) == status
+
+
+def test_ffn_prefetch_skips_large_batches_and_rejects_nulls():
+    # more than 65,536 picks: nothing to prefetch behind, returns MOE_OK without a launch (no GPU needed)
+    L = moe.load()
+    ar = _arena()
+    assert L.moe_expert_ffn_prefetch(FAKE, ctypes.byref(ar), 8192 + 1, 8, NULL) == moe.MOE_OK
+    assert L.moe_expert_ffn_prefetch(NULL, ctypes.byref(ar), 8, 4, NULL) == moe.MOE_EINVAL
+    assert L.moe_expert_ffn_prefetch(FAKE, None, 8, 4, NULL) == moe.MOE_EINVAL
