@@ -228,8 +228,9 @@ moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot
  * routing, so that HBM serves it while the FFN's plan and pack run (they read
  * little). It reads sel_slot and the arena and writes nothing: results never
  * depend on it. sel_slot int32 [T,k]; arena and limits as for
- * moe_expert_ffn_mxfp4; batches of more than 65,536 picks return MOE_OK
- * without a launch.
+ * moe_expert_ffn_mxfp4; batches of more than 8,192 picks return MOE_OK
+ * without a launch (there the first round is a small part of the GEMM, and
+ * every CTA of this call would scan all the picks beside the plan and pack).
  */
 moe_status moe_expert_ffn_prefetch(const int32_t* sel_slot, const moe_arena* arena, int T, int k, void* stream);
 

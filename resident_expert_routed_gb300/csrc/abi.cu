@@ -62,7 +62,7 @@ struct FfnCarve {
 
 // Batches of at least this many picks plan with several CTAs (2048 picks each, at most 64).
 constexpr size_t kPlanMultiPicks = 8192;
-constexpr long kPrefetchMaxPicks = 65536;       // moe_expert_ffn_prefetch scans the picks in every CTA
+constexpr long kPrefetchMaxPicks = 8192;        // moe_expert_ffn_prefetch scans the picks in every CTA
 
 FfnCarve ffn_carve(int T, int k, int d, int F, int S) {
     FfnCarve c{};

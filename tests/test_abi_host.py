@@ -182,9 +182,9 @@ def test_ffn_prefetch_checks_the_arena_like_the_ffn(kw, status):
 
 
 def test_ffn_prefetch_skips_large_batches_and_rejects_nulls():
-    # more than 65,536 picks: nothing to prefetch behind, returns MOE_OK without a launch (no GPU needed)
+    # more than 8,192 picks: returns MOE_OK without a launch (no GPU needed)
     L = moe.load()
     ar = _arena()
-    assert L.moe_expert_ffn_prefetch(FAKE, ctypes.byref(ar), 8192 + 1, 8, NULL) == moe.MOE_OK
+    assert L.moe_expert_ffn_prefetch(FAKE, ctypes.byref(ar), 1024 + 1, 8, NULL) == moe.MOE_OK
     assert L.moe_expert_ffn_prefetch(NULL, ctypes.byref(ar), 8, 4, NULL) == moe.MOE_EINVAL
     assert L.moe_expert_ffn_prefetch(FAKE, None, 8, 4, NULL) == moe.MOE_EINVAL
