@@ -313,6 +313,80 @@ def e2e_steps(layer: Layer, K: int, scratch):
     return total / K, h2d, d2h
 
 
+# ------------------------------------------------------------------ full decode step: 60 layers, one arena
+
+def full_decode_step(scratch, hbm_gbs: float, K: int = 10, W: int = 3):
+    """The 60-layer decode step (2 tokens, E256 k8 d4096 F2048, one arena of 10,000 main + 64 ring slots shared
+    by all layers, the main slots a seeded sample of the 15,360 (layer, expert) ids), replayed from one CUDA graph:
+    per layer the step (with the demand work and prefetch on a side stream, joined before the next layer reuses
+    the routing buffers), then the step's heavy-miss list."""
+    import torch
+    import resident_expert_routed_gb300 as moe
+    from resident_expert_routed_gb300.layer import LayerBuffers, join, layer_step, step_end
+    cfg, T = synth.FULL, 2
+    L, E = cfg.L, cfg.E
+    n_slots = cfg.n_main + cfg.n_ring
+    slot_of, owner = synth.full_initial_arena(cfg)
+    rec = synth.slot_record(cfg.d, cfg.ffn)
+    abuf = torch.zeros(n_slots * rec["slot_bytes"], dtype=torch.uint8, device="cuda")
+    synth.fill_slots_device(abuf, cfg.d, cfg.ffn, cfg.seed, E, torch.from_numpy(owner).cuda())
+    arena = moe.Arena(abuf, rec["slot_bytes"], n_slots, cfg.d, cfg.ffn, rec["off_gu_codes"], rec["off_gu_scales"],
+                      rec["off_dn_codes"], rec["off_dn_scales"])
+    Wd = torch.from_numpy(np.stack([synth.router_weights(cfg.seed, E, cfg.d, l) for l in range(L)])).cuda()
+    bd = torch.from_numpy(np.stack([synth.router_bias(cfg.seed, E, cfg.sigma, l) for l in range(L)])).cuda()
+    so = torch.from_numpy(slot_of).cuda()
+    xs = [torch.from_numpy(synth.hidden_bf16(cfg.seed, T, cfg.d, stream=l).view(np.int16)).cuda()
+          .view(torch.bfloat16) for l in range(L)]
+    demand = torch.zeros((L, E), dtype=torch.int64, device="cuda")
+    miss = torch.zeros((L, E), dtype=torch.float32, device="cuda")
+    buf = LayerBuffers(T, cfg.k, E, cfg.d, cfg.ffn, n_slots)
+    stream, side = torch.cuda.Stream(), torch.cuda.Stream()
+    used = []                               # distinct slots each layer reads (for the bytes), from an eager pass
+    with torch.cuda.stream(stream):
+        for l in range(L):
+            layer_step(xs[l], Wd[l], bd[l], so[l * E:(l + 1) * E], arena, demand, miss, l, buf, stream)
+            stream.synchronize()
+            sl = buf.sel_slot.cpu().numpy()
+            used.append(len(np.unique(sl[sl >= 0])))
+
+    def step():
+        for l in range(L):
+            layer_step(xs[l], Wd[l], bd[l], so[l * E:(l + 1) * E], arena, demand, miss, l, buf, stream, side)
+            join(stream, side)
+        step_end(miss, buf, 0.2, side)
+        join(stream, side)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(W, 1)):
+            step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    cur = torch.cuda.current_stream()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(K):
+        flush_l2(scratch)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        graph.replay()
+        b.record(cur)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    step_ms = sum(ms) / len(ms)
+    expert_bytes = 3 * cfg.d * cfg.ffn // 2 + 3 * cfg.d * cfg.ffn // 32
+    step_bytes = sum(used) * expert_bytes + L * E * cfg.d * 4
+    out = {"workload": cfg.name, "tokens_per_s": T / (step_ms / 1000.0), "ms_per_step": step_ms, "layers": L,
+           "distinct_experts_per_layer": float(np.mean(used)), "step_bytes": step_bytes,
+           "step_hbm_frac": step_bytes / (step_ms / 1000.0) / 1e9 / hbm_gbs}
+    del graph, abuf, arena
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ hot-read ring, on and off
 
 def ring_on_off(T: int, steps: int, n_ring: int = 64):
@@ -487,6 +561,19 @@ def run_ours(args, rank, ws, local):
                                  "distinct_experts": u_mean,
                                  "step_hbm_frac": step_bytes / (step_ms / 1000.0) / 1e9 / pk["hbm_gbs"]}
         sweep["hot_ring"] = ring_on_off(T, 30)
+        gcfg = synth.GLM
+        g_bytes = 3 * gcfg.d * gcfg.ffn // 2 + 3 * gcfg.d * gcfg.ffn // 32
+        for Tg in (1, 16, 64):
+            lg = Layer(gcfg, Tg, pool=4)
+            m, _, su, _ = timed_graph_steps(lg, 20, 3, scratch, 1)
+            sm = sum(m) / len(m)
+            sweep[f"glm_T{Tg}"] = {"workload": gcfg.name, "tokens_per_s": Tg / (sm / 1000.0), "ms_per_step": sm,
+                                   "distinct_experts": float(np.mean(su)),
+                                   "step_hbm_frac": (np.mean(su) * g_bytes + gcfg.E * gcfg.d * 4) / (sm / 1000.0)
+                                   / 1e9 / pk["hbm_gbs"]}
+            del lg
+        if not args.no_full:
+            sweep["full_decode_L60_T2"] = full_decode_step(scratch, pk["hbm_gbs"])
         if not args.no_prefill:
             lp = Layer(synth.PREFILL, 8192, pool=2)
             m, _, su, _ = timed_graph_steps(lp, 5, 2, scratch, 1)
@@ -556,6 +643,7 @@ def main():
     ap.add_argument("--T", type=int, default=64)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-full", action="store_true", help="skip the 60-layer decode step of the sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)      # at least three untimed warm-up steps
