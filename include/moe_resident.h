@@ -4,15 +4,15 @@
  *
  * The method is the adaptive expert loading of the TideLM README, section
  * "How adaptive expert loading works":
- *   item 1  demand learned from the router's own picks, per (layer, expert),
- *           weighted by routing score; one arena shared by all layers,
- *           re-planned from that history;
- *   item 2  the router only picks resident experts; a missing pick is
- *           replaced by the next-best resident expert for that token, and
- *           its demand still counts;
- *   item 3  heavy misses (>= 0.2 of the routing weight, at most 16 a step)
- *           feed hot reads into a ring of slots of their own.
- * The experts are "native MXFP4" (README profile table): OCP MX v1.0 e2m1
+ *   item 1  per (layer, expert) demand, learned from the scores of the
+ *           router's picks; a single arena for all layers, planned again
+ *           from that history;
+ *   item 2  routing is restricted to resident experts: an absent expert's
+ *           place goes to the best resident one not yet picked, and the
+ *           absent expert's demand is counted anyway;
+ *   item 3  misses with a large share of the routing weight (>= 0.2, at
+ *           most 16 a step) are fetched by hot reads into extra ring slots.
+ * The experts are stored in MXFP4 (README profile table): OCP MX v1.0 e2m1
  * elements with one e8m0 scale per 32 elements.
  *
  * Conventions for every call
@@ -60,7 +60,7 @@ typedef enum {
 #define MOE_DEV_RESIDENT    0x10u  /* ring install of an expert that is already resident */
 
 /*
- * The shared slot arena (README item 1: "one arena is shared by all layers").
+ * The shared slot arena (README item 1: a single arena serves every layer).
  * Passed by HOST pointer; `base` is a device pointer to n_slots records of
  * slot_bytes each. Slots [0, n_main) form the main arena and the rest the
  * hot-read ring (README item 3); the FFN treats them alike.
@@ -102,8 +102,9 @@ typedef struct {
 /*
  * Router scoring and resident-only top-k with substitution.
  * README items 1-2: the router scores every token against all E experts; the
- * wanted picks are the top-k over all experts; the router only picks resident
- * experts, replacing a missing pick with the next-best resident one.
+ * wanted picks are the top-k over all experts; the routed picks come from the
+ * resident experts only, an absent wanted expert giving its place to the best
+ * resident expert not yet picked.
  *   logit[t,e] = sum_i x[t,i] * W[e,i] + bias[e]   (fp32 accumulation)
  *   score[t,e] = softmax over e of logit[t,e]
  *   want  = top-k of score over all E                (score desc, index asc)
@@ -169,10 +170,10 @@ moe_status moe_route_resident_noalloc(const void* hidden_bf16, const float* w_ro
                                       int32_t* sel_e, int32_t* sel_slot, float* sel_w, void* stream);
 
 /*
- * Demand accumulation (README item 1: every wanted pick, resident or not,
- * recorded per (layer, expert) weighted by its routing score; item 2: the
- * demand of a substituted pick still counts) and the miss share (item 3: a
- * miss "would have carried a large share of a token's routing weight").
+ * Demand accumulation (README item 1: each wanted pick adds its score to the
+ * demand of its (layer, expert), resident or not; item 2: substituted picks
+ * add too) and the miss share (item 3: how much of its token's routing weight
+ * a missing expert would have taken).
  *   demand[layer, e]   += round(s * 2^40)   for each wanted pick (t, j)
  *   miss_max[layer, e]  = max(miss_max, s)  for each wanted pick with slot_of[e] < 0
  * want_e, want_s [T,k] as written by moe_route_resident; slot_of [E] of this
@@ -184,9 +185,9 @@ moe_status moe_demand_accumulate(const int32_t* want_e, const float* want_s, con
                                  uint64_t* demand, float* miss_max, void* stream);
 
 /*
- * Heavy-miss list for one step (README item 3: the heaviest misses, >= 0.2 of
- * the routing weight, at most 16 a step; "every lane's misses feed one
- * plan"). Candidates are (layer, expert) with miss_max >= threshold, ordered
+ * Heavy-miss list for one step (README item 3: the misses with the largest
+ * share, a threshold of 0.2 of a token's routing weight and a cap of 16 per
+ * step; the misses of all lanes of a step go into one list). Candidates are (layer, expert) with miss_max >= threshold, ordered
  * by miss_max descending, then flat index layer*E + e ascending; the first
  * `cap` are written. Afterwards miss_max is reset to zero for the next step.
  * out_flat int32 [cap], out_share fp32 [cap], n_out: device int32 (count).
@@ -197,7 +198,7 @@ moe_status moe_hot_miss_select(float* miss_max, int L, int E, float threshold, i
 
 /*
  * Grouped SwiGLU expert FFN over the MXFP4 arena with weighted combine
- * (README items 1-2 and the "native MXFP4" experts of the profile table).
+ * (README items 1-2 and the MXFP4 experts of the profile table).
  * For every pick (t, j) with sel_slot[t,j] >= 0, with W the expert in that slot:
  *   xq   = MXFP4(x[t])      (OCP MX: exponent floor(log2 amax) - 2, RNE, saturate)
  *   g, u = Wg xq, Wu xq     (tcgen05 block-scaled MXFP4 MMA, fp32 accumulation)
@@ -236,8 +237,8 @@ moe_status moe_expert_ffn_prefetch(const int32_t* sel_slot, const moe_arena* are
 
 /*
  * Re-plan of the one shared arena from the demand history (README item 1: the
- * arena is filled from the history and re-planned; "a busy layer takes slots
- * from a quiet one").
+ * arena's contents follow the history and are planned again; layers with more
+ * demand end up with more of the shared slots).
  *   1. rank every flat id f = layer*E + e by (demand desc, currently in a main
  *      slot first, f asc); the first n_main form the new main set;
  *   2. survivors keep their slots; main-set members that drop out lose theirs;
@@ -255,9 +256,9 @@ moe_status moe_arena_replan(const uint64_t* demand, int L, int E, int n_main, in
                             void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * Ring install (README item 3, DeepSeek: after a step the heaviest misses go
- * into a ring of slots of their own, routable from the step after until the
- * ring wraps). Makes flat id `flat_id` resident in `ring_slot`; the slot's
+ * Ring install (README item 3, DeepSeek: a step's largest misses are fetched
+ * into extra ring slots and become routable one step later, until newer
+ * fetches wrap around the ring). Makes flat id `flat_id` resident in `ring_slot`; the slot's
  * previous owner becomes non-resident. The slot's bytes are written by the
  * caller. An expert that is already resident is left alone and sets
  * MOE_DEV_RESIDENT in the device error word.
@@ -267,11 +268,10 @@ moe_status moe_ring_install(int32_t* slot_of, int32_t* owner, int ring_slot, int
                             int n_flat, int n_slots, void* stream);
 
 /*
- * Asynchronous hot-read ring (README item 3, DeepSeek: "after each step, the
- * heaviest misses are read into a ring of slots of their own ... while the
- * next step runs, and are routable from the step after until the ring
- * wraps"; "Settings worth knowing": the ring's slots are on top of the main
- * budget). A HOST object; one thread drives it, once per step boundary.
+ * Asynchronous hot-read ring (README item 3, DeepSeek: the fetches of a
+ * step's largest misses overlap the following step, and the fetched experts
+ * can be routed to from the step after it until the ring wraps; "Settings
+ * worth knowing": ring slots come in addition to the main budget). A HOST object; one thread drives it, once per step boundary.
  *
  * create: ring slots are arena slots [ring_first, ring_first + n_ring).
  *   host_records: host array [n_flat] of HOST pointers, one expert record
@@ -305,10 +305,10 @@ moe_status moe_hot_ring_step(moe_hot_ring* ring, const int32_t* heavy_flat, cons
 moe_status moe_hot_ring_destroy(moe_hot_ring* ring);
 
 /*
- * Synchronous hot read of one layer (README item 3, GLM-5.3: "a layer's
- * heaviest miss (>= 0.2 of the routing weight, at most 16 a step, paced over
- * the layers) is read before that layer's MoE runs, computed exactly, and
- * kept resident in place of the coldest expert"). Call after
+ * Synchronous hot read of one layer (README item 3, GLM-5.3: before a layer's
+ * MoE runs, its largest miss (share >= 0.2; at most 16 such reads a step,
+ * spread over the layers) is loaded, used with its exact weights, and stays
+ * resident in the slot of the least-demanded expert). Call after
  * moe_demand_accumulate of `layer` and before its FFN; then route the layer
  * again with the updated slot_of, so that the tokens that wanted the expert
  * get it (the wanted picks and the demand are unchanged).
@@ -337,9 +337,9 @@ size_t moe_workspace_bytes(int T, int k, int d, int ffn, int E, int n_slots);
 size_t moe_replan_workspace_bytes(int L, int E);
 
 /*
- * Forgetting in the demand history (README "Settings worth knowing": the
- * adaptation setting decides "how fast the resident set follows new traffic";
- * the pages give no formula). Reading: the caller applies an exponential
+ * Forgetting in the demand history (README "Settings worth knowing": an
+ * adaptation setting controls how quickly the resident set tracks a change in
+ * traffic; the pages give no formula). Reading: the caller applies an exponential
  * decay between re-plans; every entry is scaled exactly in fixed point:
  *   q = round(factor * 2^32)  (factor in [0, 1]; ties to even)
  *   demand[i] = floor(demand[i] * q / 2^32)        (128-bit product)

@@ -5,11 +5,11 @@
 // tests, the bench's CPU-baseline leg and the package smoke check call it.
 //
 // What it computes follows the TideLM README ("How adaptive expert loading
-// works", items 1-3): the router scores every token against all experts, picks
-// only resident experts (a missing pick is replaced by the next-best resident
-// one for that token), records every wanted pick per (layer, expert) weighted
-// by its routing score, lists the heavy misses (>= 0.2 of the routing weight,
-// at most 16 a step), and runs the expert FFN over the resident weights
+// works", items 1-3): the router scores every token against all experts and
+// routes to resident experts only (an absent wanted expert gives its place to
+// the best resident expert not yet picked), adds each wanted pick's score to
+// the demand of its (layer, expert), lists the misses with a large share of
+// the routing weight (>= 0.2, at most 16 a step), and runs the expert FFN over the resident weights
 // ("native MXFP4" experts, profile table) with a score-weighted combine.
 // The number formats follow the OCP Microscaling (MX) Formats v1.0 spec:
 // e2m1 elements, e8m0 shared scales, blocks of 32.
@@ -133,8 +133,8 @@ void or_router(const uint16_t* x_bf16, const float* W, const float* bias,
 }
 
 // Wanted top-k over all experts and resident top-k with substitution
-// (README item 2: "the router only picks resident experts; a missing pick is
-// replaced by the next-best resident one for that token").
+// (README item 2: routing is restricted to resident experts, and an absent
+// wanted expert gives its place to the best resident expert not yet picked).
 // Order: score descending, ties to the lower expert index. The selected list
 // is the top-k of the scores restricted to {e : slot_of[e] >= 0}; when fewer
 // than k experts are resident it is padded with expert -1, slot -1, weight 0.
@@ -172,12 +172,12 @@ void or_topk(const double* scores, const int32_t* slot_of, int T, int E, int k,
     }
 }
 
-// Demand recording (README item 1: "every routed pick the router wants -
-// resident or not - is recorded per (layer, expert), weighted by its routing
-// score"; item 2: "the demand still counts"). D[layer*E + e] += s for each
-// wanted pick. The miss share M[layer*E + e] = max(M, s) over the wanted picks
-// of non-resident experts (item 3: a miss that "would have carried a large
-// share of a token's routing weight"; reading: the share is the softmax score).
+// Demand recording (README item 1: each wanted pick adds its routing score to
+// the demand of its (layer, expert), resident or not; item 2: substituted
+// picks add too). D[layer*E + e] += s for each wanted pick. The miss share
+// M[layer*E + e] = max(M, s) over the wanted picks of non-resident experts
+// (item 3: how much of its token's routing weight a missing expert would have
+// taken; reading: the share is the softmax score).
 void or_demand(const int32_t* want_e, const double* want_s, const int32_t* slot_of,
                int T, int k, int layer, int E, double* D, double* M) {
     for (int t = 0; t < T; ++t)
@@ -190,9 +190,9 @@ void or_demand(const int32_t* want_e, const double* want_s, const int32_t* slot_
         }
 }
 
-// Forgetting in the demand history (README "Settings worth knowing": the
-// adaptation setting sets "how fast the resident set follows new traffic"; no
-// formula is given). Reading: exponential decay applied between re-plans to
+// Forgetting in the demand history (README "Settings worth knowing": an
+// adaptation setting controls how quickly the resident set tracks a change in
+// traffic; no formula is given). Reading: exponential decay applied between re-plans to
 // the stored table, which keeps demand as an integer count of 2^-40 units.
 // The factor is rounded to a multiple of 2^-32 (ties to even) and each entry
 // becomes the floor of its exact product with it.
@@ -217,9 +217,9 @@ void or_renormalise(const int32_t* sel_slot, double* sel_w, int T, int k) {
     }
 }
 
-// Synchronous hot read of one layer (README item 3, GLM-5.3: a layer's
-// heaviest miss is "read before that layer's MoE runs, computed exactly, and
-// kept resident in place of the coldest expert"). Reading: the read expert
+// Synchronous hot read of one layer (README item 3, GLM-5.3: before a layer's
+// MoE runs, its largest miss is loaded, used with its exact weights, and stays
+// resident in the slot of the least-demanded expert). Reading: the read expert
 // is the non-resident expert of the layer with the largest miss share this
 // step (>= threshold, ties to the lower index) that the store holds; the
 // coldest expert is the resident one with the lowest demand (ties to the
@@ -239,8 +239,8 @@ void or_hot_read_choose(const double* M, const double* D, const int32_t* slot_of
     out[1] = cold;
 }
 
-// Heavy misses (README item 3: "the heaviest misses"; ">= 0.2 of the routing
-// weight, at most 16 a step"). Candidates are the (layer, expert) with
+// Heavy misses (README item 3: the misses with the largest share; the share
+// threshold is 0.2 of a token's routing weight and the cap 16 per step). Candidates are the (layer, expert) with
 // M >= threshold, ordered by M descending then flat index ascending; the first
 // `cap` are returned. M is then reset to zero for the next step.
 void or_hot_miss_select(double* M, int L, int E, double threshold, int cap,
@@ -368,9 +368,9 @@ void or_ffn(const uint16_t* x_bf16, const int32_t* sel_u, const double* sel_w,
 
 // ---------------------------------------------------------------- arena re-plan
 
-// Re-plan of the one shared arena (README item 1: "one arena is shared by all
-// layers: a busy layer takes slots from a quiet one"; the arena is "re-planned"
-// from the demand history). Slots [0, n_main) are the main arena, slots
+// Re-plan of the one shared arena (README item 1: a single arena serves every
+// layer, so layers with more demand hold more of its slots; its contents are
+// planned again from the demand history). Slots [0, n_main) are the main arena, slots
 // [n_main, n_slots) the hot-read ring.
 //   1. Rank every (layer, expert) flat id f by (D desc, currently in a main
 //      slot first, f asc); the first n_main form the new main set.
@@ -417,9 +417,9 @@ void or_replan(const double* D, int L, int E, int n_main, int n_slots,
     *n_loads = nl;
 }
 
-// Install expert `flat` in ring slot `ring_slot` (README item 3, DeepSeek:
-// "the heaviest misses are read into a ring of slots of their own ... routable
-// from the step after until the ring wraps"). The slot's previous owner
+// Install expert `flat` in ring slot `ring_slot` (README item 3, DeepSeek: a
+// step's largest misses are fetched into extra ring slots and can be routed to
+// one step later, until newer fetches wrap around the ring). The slot's previous owner
 // becomes non-resident. An expert that is already resident is left alone and
 // the call returns 1; otherwise 0.
 int or_ring_install(int32_t* slot_of, int32_t* owner, int ring_slot, int flat) {

@@ -1,11 +1,12 @@
 // Demand accumulation and the heavy-miss list.
 //
 // TideLM README, "How adaptive expert loading works":
-//   item 1  every routed pick the router wants, resident or not, is recorded
-//           per (layer, expert) weighted by its routing score;
-//   item 2  the demand of a substituted (missing) pick still counts;
-//   item 3  a miss that would have carried a large share of a token's routing
-//           weight (>= 0.2, at most 16 a step) is a candidate for a hot read.
+//   item 1  each pick the router asks for adds its routing score to the
+//           demand of its (layer, expert), whether that expert is resident
+//           or not;
+//   item 2  a pick that had to be substituted adds to the demand as well;
+//   item 3  a miss whose score is a big part of its token's routing weight
+//           (at least 0.2; at most 16 a step) may be fetched by a hot read.
 //
 // demand_accumulate: shared-memory histograms over the E experts of one layer
 // (u64 fixed point in units of 2^-40, and the max miss share as float bits),

@@ -1,8 +1,9 @@
 // The asynchronous hot-read ring (TideLM README, "How adaptive expert loading
-// works", item 3, DeepSeek: after each step the heaviest misses are read into
-// a ring of slots of their own while the next step runs, and are routable from
-// the step after until the ring wraps; "Settings worth knowing": the ring's
-// slots sit on top of the main budget).
+// works", item 3, the DeepSeek variant: once a step ends, its largest misses
+// are fetched into a dedicated set of ring slots during the following step;
+// they can be routed to from the step after that, and stay until newer
+// fetches wrap around the ring. "Settings worth knowing": these slots come in
+// addition to the main slot budget).
 //
 // A host object drives it at step boundaries. One call, made after step s
 // has been enqueued (including its heavy-miss list):
@@ -64,10 +65,11 @@ __global__ void ring_install_batch(int32_t* slot_of, int32_t* owner, RingBatch b
 
 // ------------------------------------------------------------------ synchronous hot read (GLM-5.3)
 //
-// README item 3, GLM-5.3: a layer's heaviest miss (>= 0.2 of the routing
-// weight, at most 16 a step, paced over the layers) is read before that
-// layer's MoE runs, computed exactly, and kept resident in place of the
-// coldest expert. One CTA picks the expert and the victim and updates the
+// README item 3, the GLM-5.3 variant: before a layer's MoE runs, its largest
+// miss (a share of at least 0.2 of a token's routing weight; at most 16 such
+// reads per step, spread over the layers) is loaded, used for this layer with
+// its exact weights, and then stays resident, evicting the expert with the
+// least demand. One CTA picks the expert and the victim and updates the
 // tables; a grid-wide copy then streams the record from the store (host
 // memory the device can address) into the victim's slot. The caller routes
 // the layer again before its FFN.

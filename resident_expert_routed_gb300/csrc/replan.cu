@@ -1,13 +1,13 @@
 // Re-plan of the one shared expert arena, and the hot-read ring install.
 //
 // TideLM README, "How adaptive expert loading works":
-//   item 1  the arena is filled from the learned demand history and re-planned
-//           (after prefill, every few hundred tokens, between requests); one
-//           arena is shared by all layers, so a busy layer takes slots from a
-//           quiet one;
-//   item 3  (DeepSeek) after each step the heaviest misses are read into a
-//           ring of slots of their own, on top of the main budget, routable
-//           from the step after until the ring wraps.
+//   item 1  the arena's contents follow the learned demand history and are
+//           planned again from time to time (after a prefill, every few
+//           hundred tokens, between requests); all layers draw on a single
+//           arena, so layers with more demand hold more of its slots;
+//   item 3  (DeepSeek) the largest misses of a step are fetched into extra
+//           ring slots beyond the main budget, usable from the step after
+//           next, until later fetches wrap around the ring.
 //
 // arena_replan runs in one CTA (it is off the per-token path): a bitonic sort
 // of (demand, currently-main flag, inverted flat id) keys in the workspace,

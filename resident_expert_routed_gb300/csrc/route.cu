@@ -3,7 +3,8 @@
 // TideLM README, "How adaptive expert loading works", items 1-2: the router
 // scores every token against all experts; the wanted picks are the top-k over
 // all of them, and the picks actually routed are the top-k over the resident
-// experts only, so a missing pick is replaced by the next-best resident one.
+// experts only: a wanted expert that is absent gives its place to the best
+// resident expert not yet picked.
 //
 // Two kernels:
 //   router_logits_partial  fp32 register-tiled GEMM over a K slice:

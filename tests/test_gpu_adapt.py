@@ -1,7 +1,7 @@
 """Demand history on the GPU: forgetting (fixed point) and persistence, through the C ABI.
 
-The TideLM README keeps the demand history across restarts and lets a
-setting decide how fast the resident set follows new traffic. Decay is
+The TideLM README keeps the demand history over restarts, and a setting there
+controls how quickly the resident set tracks a change in traffic. Decay is
 checked bit-exact against the oracle's fixed-point restatement; save and load
 round-trip the table through the documented file format.
 """

@@ -1,8 +1,8 @@
 """The synchronous hot read of one layer (moe_hot_read_sync) on the GPU, through the C ABI.
 
-TideLM README, item 3 (GLM-5.3): a layer's heaviest miss is read before that
-layer's MoE runs, computed exactly, and kept resident in place of the coldest
-expert. The choice and the table update are checked bit-exact against the
+TideLM README, item 3 (GLM-5.3): before a layer's MoE runs, its largest miss
+is loaded, used with its exact weights, and stays resident in the slot of the
+least-demanded expert. The choice and the table update are checked bit-exact against the
 oracle fed the GPU's own miss shares and demand; the copied record, the read
 budget, and the layer routed again (routing and FFN against the oracle on the
 updated table) are checked too.

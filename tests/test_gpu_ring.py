@@ -1,8 +1,8 @@
 """The asynchronous hot-read ring (moe_hot_ring_*) on the GPU, through the C ABI.
 
-TideLM README, item 3 (DeepSeek): after each step the heaviest misses are
-read into a ring of slots of their own while the next step runs, and are
-routable from the step after until the ring wraps. A pinned host store of
+TideLM README, item 3 (DeepSeek): a step's largest misses are fetched into
+extra ring slots during the following step and can be routed to from the step
+after it, until newer fetches wrap around the ring. A pinned host store of
 expert records stands in for the drive. Checked: the tables after each call
 against the oracle's ring install (FIFO order, evictions, experts not yet
 routable while their copies are in flight), the copied bytes, and a real
