@@ -43,9 +43,10 @@ def layer_step(hidden: torch.Tensor, w_router: torch.Tensor, bias, slot_of: torc
 
     With a second stream `side`, the L2 prefetch of the weights the FFN reads
     first and the demand update run there, beside the expert FFN (they read
-    only the routing outputs). The caller then runs
-    ``step_end`` on `side` too and calls ``join(stream, side)`` before the next
-    step's routing rewrites want_e / want_s, or before it reads the tables.
+    only the routing outputs). The caller then runs ``step_end`` on `side` too
+    and calls ``join(stream, side)`` before the routing outputs in `buf` are
+    written again (the next layer's step when layers share `buf`, else the next
+    step's) and before it reads the tables.
     """
     main = torch.cuda.current_stream() if stream is None else stream
     moe_route_resident(hidden, w_router, bias, slot_of, buf.k, buf.want_e, buf.want_s, buf.sel_e, buf.sel_slot,
@@ -62,7 +63,7 @@ def layer_step(hidden: torch.Tensor, w_router: torch.Tensor, bias, slot_of: torc
 
 
 def join(stream, side) -> None:
-    """The main stream waits for the side stream's demand and heavy-miss work."""
+    """The main stream waits for the side stream's work (prefetch, demand update, heavy-miss list)."""
     (torch.cuda.current_stream() if stream is None else stream).wait_stream(side)
 
 
@@ -96,7 +97,7 @@ class CapturedStep:
             if not h.is_pinned() or h.shape != (T, d) or h.dtype != torch.bfloat16:
                 raise ValueError("host inputs must be pinned bf16 [T, d] tensors of one shape")
         self.main, self.side = torch.cuda.Stream(), torch.cuda.Stream()
-        self.hidden = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+        self.hidden = None if zero_copy else torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
         self.host_out = host_out if host_out is not None else torch.empty((T, d), dtype=torch.float32).pin_memory()
         self.buf = buf
 
