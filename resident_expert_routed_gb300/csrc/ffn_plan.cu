@@ -90,6 +90,83 @@ __global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restri
     }
 }
 
+// Small batches (at most SMALL_PICKS picks), with work in proportion to the
+// picks rather than the slots: the (slot, pick) keys are sorted in shared
+// memory (bitonic sort of the next power of two >= P), so every used slot is
+// one run of equal slots, runs in slot order and each run's picks in pick
+// order; block scans give each run's padded segment and first work entry.
+// Nothing here visits the S slots one by one, which matters with arenas of
+// thousands of slots and a few picks per layer.
+constexpr int SMALL_PICKS = 1024;
+
+__global__ void __launch_bounds__(SMALL_PICKS) ffn_plan_small(const int32_t* __restrict__ sel_slot, int P, int S,
+                                                              int bn, int32_t* __restrict__ pos_of_pair,
+                                                              int32_t* __restrict__ pair_of_pos,
+                                                              int4* __restrict__ work, int32_t* __restrict__ n_work,
+                                                              int late_trigger, uint32_t* err) {
+    __shared__ uint32_t key[SMALL_PICKS];               // slot << 10 | pick (slot < 2^14), 0xFFFFFFFF = none
+    __shared__ int32_t run_start[SMALL_PICKS + 1];
+    __shared__ int32_t run_seg[SMALL_PICKS];
+    __shared__ unsigned long long scan_scratch[32];
+    const int tid = threadIdx.x;
+    if (!late_trigger) pdl_trigger();
+    pdl_wait();
+    if (late_trigger) pdl_trigger();    // after the wait: the pack, launched now, may read x before its own wait
+    uint32_t kv = 0xFFFFFFFFu;
+    if (tid < P) {
+        int s = sel_slot[tid];
+        if (s >= S) { record_error(err, MOE_DEV_BAD_SLOT); s = -1; }
+        if (s >= 0) kv = ((uint32_t)s << 10) | (uint32_t)tid;
+        else pos_of_pair[tid] = -1;
+    }
+    key[tid] = kv;
+    int n2 = 32;
+    while (n2 < P) n2 <<= 1;                            // keys past P are all 0xFFFFFFFF
+    for (int k = 2; k <= n2; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            __syncthreads();
+            const int ixj = tid ^ j;
+            if (tid < n2 && ixj > tid) {
+                const uint32_t x = key[tid], y = key[ixj];
+                if ((x > y) == ((tid & k) == 0)) { key[tid] = y; key[ixj] = x; }
+            }
+        }
+    __syncthreads();
+    const uint32_t me = key[tid];
+    const bool valid = me != 0xFFFFFFFFu;               // the valid keys come first
+    const bool head = valid && (tid == 0 || (key[tid - 1] >> 10) != (me >> 10));
+    unsigned long long n_runs, n_valid;
+    const int run = (int)block_inclusive_scan_u64(head ? 1ull : 0ull, scan_scratch, &n_runs) - 1;
+    (void)block_inclusive_scan_u64(valid ? 1ull : 0ull, scan_scratch, &n_valid);
+    if (head) run_start[run] = tid;
+    if (tid == 0) run_start[n_runs] = (int)n_valid;
+    __syncthreads();
+    // thread r < n_runs: run r's slot, its padded rows and tiles, scanned in slot order
+    int c = 0, r_slot = 0;
+    if (tid < (int)n_runs) {
+        c = run_start[tid + 1] - run_start[tid];
+        r_slot = (int)(key[run_start[tid]] >> 10);
+    }
+    const unsigned long long nt = (unsigned long long)((c + bn - 1) / bn);
+    const unsigned long long packed = (nt * bn) | (nt << 32);
+    unsigned long long total;
+    const unsigned long long excl = block_inclusive_scan_u64(packed, scan_scratch, &total) - packed;
+    if (tid < (int)n_runs) {
+        const int seg = (int)(excl & 0xFFFFFFFFull), toff = (int)(excl >> 32);
+        run_seg[tid] = seg;
+        for (int q = 0; q < (int)nt; ++q)
+            work[toff + q] = make_int4(r_slot, seg + q * bn, min(bn, c - q * bn), 0);
+    }
+    if (tid == 0) *n_work = (int32_t)(total >> 32);
+    __syncthreads();
+    if (valid) {
+        const int pick = (int)(me & 1023u);
+        const int pos = run_seg[run] + (tid - run_start[run]);
+        pos_of_pair[pick] = pos;
+        pair_of_pos[pos] = pick;
+    }
+}
+
 // Large batches, in three kernels. 1: each CTA counts the picks of its chunk
 // per slot (shared-memory histogram) and notes each pick's rank among them.
 __global__ void __launch_bounds__(PLAN_THREADS) plan_count(const int32_t* __restrict__ sel_slot, int P, int S,
@@ -326,8 +403,12 @@ cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
                            a.pos_of_pair, a.pair_of_pos);
         moe_count_launches(2);
     } else {
-        e = moe_launch(ffn_plan, dim3(1), dim3(PLAN_THREADS), smem, s, a.sel_slot, P, a.S, a.bn, a.pos_of_pair,
-                       a.pair_of_pos, a.seg, a.tile_off, a.work, a.n_work, early, a.err);
+        if (P <= SMALL_PICKS)
+            e = moe_launch(ffn_plan_small, dim3(1), dim3(SMALL_PICKS), 0, s, a.sel_slot, P, a.S, a.bn, a.pos_of_pair,
+                           a.pair_of_pos, a.work, a.n_work, early, a.err);
+        else
+            e = moe_launch(ffn_plan, dim3(1), dim3(PLAN_THREADS), smem, s, a.sel_slot, P, a.S, a.bn, a.pos_of_pair,
+                           a.pair_of_pos, a.seg, a.tile_off, a.work, a.n_work, early, a.err);
     }
     moe_prof_end(MK_PLAN, s);
     if (e != cudaSuccess) return e;
