@@ -90,20 +90,67 @@ __global__ void __launch_bounds__(PLAN_THREADS) ffn_plan(const int32_t* __restri
     }
 }
 
+// MXFP4 of one (token t, 32-element block b) of x: 16 bytes of codes and, on
+// lane 4g of each group of four lanes, the 4-byte scale word of its 128-element
+// group (the four blocks' bytes side by side in the tile's scale atom). Whole
+// warps call it together (the word is assembled with shuffles); inactive lanes
+// contribute nothing.
+__device__ __forceinline__ void pack_quantise(const uint16_t* __restrict__ x, long t, int b, int d, bool active,
+                                              uint4& codes, uint32_t& word) {
+    codes = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t byte = 0;
+    if (active) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + t * d + b * 32);
+        uint4 v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = src[q];
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(v);
+        float f[32];
+        float amax = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) { f[q] = bf16_bits_to_float(h[q]); amax = fmaxf(amax, fabsf(f[q])); }
+        const int X = mx_shared_exp(amax);
+        const float inv = exp2_int(-X);
+        codes = make_uint4(e2m1x8(f, inv), e2m1x8(f + 8, inv), e2m1x8(f + 16, inv), e2m1x8(f + 24, inv));
+        byte = (uint32_t)(X + 127);
+    }
+    word = byte;
+    word |= __shfl_down_sync(0xFFFFFFFFu, byte, 1) << 8;
+    word |= __shfl_down_sync(0xFFFFFFFFu, byte, 2) << 16;
+    word |= __shfl_down_sync(0xFFFFFFFFu, byte, 3) << 24;
+}
+
+// The block's codes and scale word go to the operand row of each of token t's picks.
+__device__ __forceinline__ void pack_scatter(const int32_t* __restrict__ pos_of_pair, long t, int b, int k, int d,
+                                             int bn, const uint4& codes, uint32_t word, uint8_t* __restrict__ xp,
+                                             uint8_t* __restrict__ xsp) {
+    for (int j = 0; j < k; ++j) {
+        const int pos = pos_of_pair[t * k + j];
+        if (pos < 0) continue;
+        *reinterpret_cast<uint4*>(xp + (size_t)pos * (d / 2) + b * 16) = codes;
+        if ((b & 3) == 0) *reinterpret_cast<uint32_t*>(xsp + operand_scale_offset(pos, b, bn, d)) = word;
+    }
+}
+
 // Small batches (at most SMALL_PICKS picks), with work in proportion to the
 // picks rather than the slots: the (slot, pick) keys are sorted in shared
 // memory (bitonic sort of the next power of two >= P), so every used slot is
 // one run of equal slots, runs in slot order and each run's picks in pick
 // order; block scans give each run's padded segment and first work entry.
 // Nothing here visits the S slots one by one, which matters with arenas of
-// thousands of slots and a few picks per layer.
+// thousands of slots and a few picks per layer. With `fuse` (few tokens) the
+// same CTA then quantises x and writes the operand rows, which saves the pack
+// launch: x is complete here, since this kernel runs after its wait.
 constexpr int SMALL_PICKS = 1024;
+constexpr long FUSED_PACK_TASKS = 512;                  // (token, 32-block) tasks: T <= 4 at d = 4096
 
 __global__ void __launch_bounds__(SMALL_PICKS) ffn_plan_small(const int32_t* __restrict__ sel_slot, int P, int S,
                                                               int bn, int32_t* __restrict__ pos_of_pair,
                                                               int32_t* __restrict__ pair_of_pos,
                                                               int4* __restrict__ work, int32_t* __restrict__ n_work,
-                                                              int late_trigger, uint32_t* err) {
+                                                              int late_trigger, int fuse, const uint16_t* __restrict__ x,
+                                                              int T, int k, int d, uint8_t* __restrict__ xp,
+                                                              uint8_t* __restrict__ xsp, uint32_t* err) {
     __shared__ uint32_t key[SMALL_PICKS];               // slot << 10 | pick (slot < 2^14), 0xFFFFFFFF = none
     __shared__ int32_t run_start[SMALL_PICKS + 1];
     __shared__ int32_t run_seg[SMALL_PICKS];
@@ -164,6 +211,20 @@ __global__ void __launch_bounds__(SMALL_PICKS) ffn_plan_small(const int32_t* __r
         const int pos = run_seg[run] + (tid - run_start[run]);
         pos_of_pair[pick] = pos;
         pair_of_pos[pos] = pick;
+    }
+    if (!fuse) return;
+    __syncthreads();                                    // the positions are visible to the whole block
+    const int nb = d / 32;
+    const long tasks = (long)T * nb;
+    for (long i0 = 0; i0 < tasks; i0 += SMALL_PICKS) {  // whole warps iterate together
+        const long i = i0 + tid;
+        const bool active = i < tasks;
+        const long t = active ? i / nb : 0;
+        const int b = active ? (int)(i % nb) : 0;
+        uint4 codes;
+        uint32_t word;
+        pack_quantise(x, t, b, d, active, codes, word);
+        if (active) pack_scatter(pos_of_pair, t, b, k, d, bn, codes, word, xp, xsp);
     }
 }
 
@@ -249,35 +310,12 @@ __global__ void __launch_bounds__(256) ffn_pack(const uint16_t* __restrict__ x, 
     const bool active = i < total;
     const long t = active ? i / nb : 0;
     const int b = active ? (int)(i % nb) : 0;
-    uint4 codes = make_uint4(0u, 0u, 0u, 0u);
-    uint32_t byte = 0;
-    if (active) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + t * d + b * 32);
-        uint4 v[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = src[q];
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(v);
-        float f[32];
-        float amax = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 32; ++q) { f[q] = bf16_bits_to_float(h[q]); amax = fmaxf(amax, fabsf(f[q])); }
-        const int X = mx_shared_exp(amax);
-        const float inv = exp2_int(-X);
-        codes = make_uint4(e2m1x8(f, inv), e2m1x8(f + 8, inv), e2m1x8(f + 16, inv), e2m1x8(f + 24, inv));
-        byte = (uint32_t)(X + 127);
-    }
-    uint32_t word = byte;
-    word |= __shfl_down_sync(0xFFFFFFFFu, byte, 1) << 8;
-    word |= __shfl_down_sync(0xFFFFFFFFu, byte, 2) << 16;
-    word |= __shfl_down_sync(0xFFFFFFFFu, byte, 3) << 24;
+    uint4 codes;
+    uint32_t word;
+    pack_quantise(x, t, b, d, active, codes, word);
     if (early) pdl_wait();                                          // positions are the plan's output
     if (!active) return;
-    for (int j = 0; j < k; ++j) {
-        const int pos = pos_of_pair[t * k + j];
-        if (pos < 0) continue;
-        *reinterpret_cast<uint4*>(xp + (size_t)pos * (d / 2) + b * 16) = codes;
-        if ((b & 3) == 0) *reinterpret_cast<uint32_t*>(xsp + operand_scale_offset(pos, b, bn, d)) = word;
-    }
+    pack_scatter(pos_of_pair, t, b, k, d, bn, codes, word, xp, xsp);
 }
 
 __global__ void __launch_bounds__(256) ffn_combine(const float* __restrict__ Y, const int32_t* __restrict__ sel_slot,
@@ -371,6 +409,8 @@ cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
     // batches of 8 tokens or more quantise x while the plan runs (large batches always: their plan ends
     // with plan_place, which signals after its wait)
     const int early = a.plan_ctas > 0 || a.T >= 8 ? 1 : 0;
+    // few tokens: the small plan also packs x (one launch fewer)
+    const bool fused = a.plan_ctas == 0 && P <= SMALL_PICKS && (long)a.T * (a.d / 32) <= FUSED_PACK_TASKS;
     const size_t smem = (size_t)a.S * sizeof(int32_t);
     static bool attr_set[64] = {};
     static bool attr_set_multi[64] = {};
@@ -405,13 +445,18 @@ cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
     } else {
         if (P <= SMALL_PICKS)
             e = moe_launch(ffn_plan_small, dim3(1), dim3(SMALL_PICKS), 0, s, a.sel_slot, P, a.S, a.bn, a.pos_of_pair,
-                           a.pair_of_pos, a.work, a.n_work, early, a.err);
+                           a.pair_of_pos, a.work, a.n_work, fused ? 0 : early, fused ? 1 : 0, a.x, a.T, a.k, a.d,
+                           a.xp, a.xsp, a.err);
         else
             e = moe_launch(ffn_plan, dim3(1), dim3(PLAN_THREADS), smem, s, a.sel_slot, P, a.S, a.bn, a.pos_of_pair,
                            a.pair_of_pos, a.seg, a.tile_off, a.work, a.n_work, early, a.err);
     }
     moe_prof_end(MK_PLAN, s);
     if (e != cudaSuccess) return e;
+    if (fused) {
+        moe_count_launches(1);
+        return e;
+    }
     const long tasks = (long)a.T * (a.d / 32);
     const long blocks = (tasks + 255) / 256;                // one task per thread (at most 2^20 * 512 / 256)
     moe_prof_begin(MK_PACK, s);
