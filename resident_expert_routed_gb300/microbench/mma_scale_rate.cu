@@ -9,7 +9,9 @@
 // Modes: 0 MMAs only; 1 plus six 32x128b.warpx4 scale copies per four MMAs
 // (what a stage of the gate/up GEMM needs); 2 plus four warps writing the same
 // 24 scale columns per four MMAs with tcgen05.st; 3 bf16 kind::f16 MMAs
-// (M 128, N 256, K 16) for reference.
+// (M 128, N 256, K 16) for reference; 4 the same e2m1 operands and e8m0
+// scales under kind::mxf4nvf4 (scale_vec::2X); 5 kind::mxf4nvf4 with
+// scale_vec::4X and ue4m3 scales (one scale per 16 elements).
 #include <cstdio>
 
 #include "../csrc/common.cuh"
@@ -36,6 +38,23 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+template <bool VEC4>
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, uint32_t acc) {
+    if (VEC4)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+            ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+            ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+            : "memory");
+}
+
 constexpr int SMEM = 120 * 1024;     // forces one CTA per SM
 
 template <int MODE>
@@ -50,7 +69,7 @@ __global__ void __launch_bounds__(160, 1) rate(int n_mma, unsigned long long* ns
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 52244);
     for (int i = threadIdx.x; i < 49152 / 16; i += blockDim.x)
         reinterpret_cast<uint4*>(smem)[i] = make_uint4(0x22222222u, 0x11111111u, 0x22222222u, 0x11111111u);
-    for (int i = threadIdx.x; i < 3072; i += blockDim.x) SF[i] = 127;     // scale 2^0
+    for (int i = threadIdx.x; i < 3072; i += blockDim.x) SF[i] = MODE == 5 ? 0x38 : 127;     // scale 1 (ue4m3 / e8m0)
     if (threadIdx.x == 0) {
         mbar_init(bar, 1);
         *abort_flag = 0;
@@ -92,6 +111,14 @@ __global__ void __launch_bounds__(160, 1) rate(int n_mma, unsigned long long* ns
                 }
             if (MODE == 3)
                 mma_bf16(tmem, smem_desc_sw128(as + kk * 32), smem_desc_sw128(bs + kk * 32), i != 0);
+            else if (MODE == 4)
+                mma_nvf4<false>(tmem, smem_desc_sw128(as + kk * 32), smem_desc_sw128(bs + kk * 32),
+                                idesc_mxf4(256, (kk & 1) * 2, (kk & 1) * 2), sfc + (kk >> 1) * 4,
+                                sfc + 8 + (kk >> 1) * 8, i != 0);
+            else if (MODE == 5)     // ue4m3 scale type: bit 23 clear; one whole scale word per MMA
+                mma_nvf4<true>(tmem, smem_desc_sw128(as + kk * 32), smem_desc_sw128(bs + kk * 32),
+                               idesc_mxf4(256, 0, 0) & ~(1u << 23), sfc + (kk >> 1) * 4, sfc + 8 + (kk >> 1) * 8,
+                               i != 0);
             else
                 tc_mma_mxf4(tmem, smem_desc_sw128(as + kk * 32), smem_desc_sw128(bs + kk * 32),
                             idesc_mxf4(256, (kk & 1) * 2, (kk & 1) * 2), sfc + (kk >> 1) * 4, sfc + 8 + (kk >> 1) * 8,
@@ -139,7 +166,10 @@ int main() {
     const double b = run<1>("mxf4 + 6 tcgen05.cp 32x128b.warpx4 / 4 MMAs", f4, sms, d_ns);
     const double c = run<2>("mxf4 + 4 warps tcgen05.st (24 columns / 4)", f4, sms, d_ns);
     const double e = run<3>("bf16 128x256x16", f16, sms, d_ns);
+    const double g = run<4>("mxf4nvf4 2X (e8m0) 128x256x64", f4, sms, d_ns);
+    const double h = run<5>("mxf4nvf4 4X (ue4m3) 128x256x64", f4, sms, d_ns);
     printf("{\"mxf4_tflops\": %.1f, \"mxf4_with_scale_copies_tflops\": %.1f, \"mxf4_with_scale_stores_tflops\": %.1f, "
-           "\"bf16_tflops\": %.1f, \"sms\": %d}\n", a, b, c, e, sms);
+           "\"bf16_tflops\": %.1f, \"mxf4nvf4_2x_tflops\": %.1f, \"mxf4nvf4_4x_tflops\": %.1f, \"sms\": %d}\n",
+           a, b, c, e, g, h, sms);
     return 0;
 }
