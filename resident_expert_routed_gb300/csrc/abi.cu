@@ -277,6 +277,10 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
     a.partial = static_cast<float*>(workspace);
     a.err = err_word();
     if (!a.err) return MOE_ECUDA;
+    if (hk == 0 && router_rows_eligible(T, d)) {      // few tokens: whole rows, no K slices
+        a.rows = 1;
+        a.splits = 1;
+    }
     if (hk == 0 && router_tc_eligible(T, E, d)) {     // the tensor maps need device memory
         a.wsplit = workspace;
         a.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + router_tc_split_bytes(E, d));

@@ -275,7 +275,9 @@ struct RouteLaunch {
     float* partial;
     void* wsplit;           // non-null: tensor-core router, W split into three bf16 parts here
     uint32_t* err;          // device error word (tensor-core router's bounded waits)
+    int rows;               // 1: one CTA per expert row (few tokens in device memory; splits = 1)
 };
+bool router_rows_eligible(int T, int d);
 bool router_tc_eligible(int T, int E, int d);
 int pointer_kind(const void* p);      // 0 device, 1 page-locked host, -1 pageable host
 int router_tc_splits(int T, int E, int d);

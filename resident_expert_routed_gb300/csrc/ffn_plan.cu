@@ -132,6 +132,64 @@ __device__ __forceinline__ void pack_scatter(const int32_t* __restrict__ pos_of_
     }
 }
 
+// At most 32 picks: the plan of ffn_plan_small in one warp, lane = pick, with
+// shuffles and ballots instead of block barriers: bitonic sort of the keys
+// across the lanes, run heads, and a lane scan of (padded rows, tiles) over
+// the heads. Same outputs as the block version.
+__device__ __forceinline__ void plan_warp(const int32_t* __restrict__ sel_slot, int P, int S, int bn,
+                                          int32_t* __restrict__ pos_of_pair, int32_t* __restrict__ pair_of_pos,
+                                          int4* __restrict__ work, int32_t* __restrict__ n_work, uint32_t* err) {
+    const int lane = threadIdx.x & 31;
+    uint32_t key = 0xFFFFFFFFu;
+    if (lane < P) {
+        int sl = sel_slot[lane];
+        if (sl >= S) { record_error(err, MOE_DEV_BAD_SLOT); sl = -1; }
+        if (sl >= 0) key = ((uint32_t)sl << 10) | (uint32_t)lane;
+        else pos_of_pair[lane] = -1;
+    }
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, key, j);
+            const bool up = (lane & k) == 0, lower = (lane & j) == 0;
+            key = (up == lower) ? min(key, other) : max(key, other);
+        }
+    const bool valid = key != 0xFFFFFFFFu;                          // the valid keys come first
+    const uint32_t prev = __shfl_up_sync(0xFFFFFFFFu, key, 1);
+    const bool head = valid && (lane == 0 || (prev >> 10) != (key >> 10));
+    const uint32_t heads = __ballot_sync(0xFFFFFFFFu, head);
+    const int n_valid = __popc(__ballot_sync(0xFFFFFFFFu, valid));
+    // a head's run ends at the next head (or at the end of the valid keys)
+    const uint32_t later = heads & ~((2u << lane) - 1u);
+    const int c = head ? (later ? __ffs(later) - 1 : n_valid) - lane : 0;
+    const unsigned long long nt = (unsigned long long)((c + bn - 1) / bn);
+    const unsigned long long packed = (nt * bn) | (nt << 32);
+    unsigned long long incl = packed;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    const unsigned long long excl = incl - packed;
+    const int seg = (int)(excl & 0xFFFFFFFFull);
+    if (head) {
+        const int toff = (int)(excl >> 32), r_slot = (int)(key >> 10);
+        for (int q = 0; q < (int)nt; ++q) work[toff + q] = make_int4(r_slot, seg + q * bn, min(bn, c - q * bn), 0);
+    }
+    if (lane == 31) *n_work = (int32_t)(incl >> 32);
+    // each valid key: its run's segment start, from the run's head lane
+    const uint32_t mine = heads & ((2u << lane) - 1u);
+    const int h = mine ? 31 - __clz(mine) : 0;
+    const int seg_h = __shfl_sync(0xFFFFFFFFu, seg, h);
+    if (valid) {
+        const int pick = (int)(key & 1023u);
+        const int pos = seg_h + (lane - h);
+        pos_of_pair[pick] = pos;
+        pair_of_pos[pos] = pick;
+    }
+}
+
 // Small batches (at most SMALL_PICKS picks), with work in proportion to the
 // picks rather than the slots: the (slot, pick) keys are sorted in shared
 // memory (bitonic sort of the next power of two >= P), so every used slot is
@@ -143,6 +201,7 @@ __device__ __forceinline__ void pack_scatter(const int32_t* __restrict__ pos_of_
 // launch: x is complete here, since this kernel runs after its wait.
 constexpr int SMALL_PICKS = 1024;
 constexpr long FUSED_PACK_TASKS = 512;                  // (token, 32-block) tasks: T <= 4 at d = 4096
+static_assert(FUSED_PACK_TASKS <= SMALL_PICKS - 32, "the one-warp plan quantises one task per thread of warps 1..");
 
 __global__ void __launch_bounds__(SMALL_PICKS) ffn_plan_small(const int32_t* __restrict__ sel_slot, int P, int S,
                                                               int bn, int32_t* __restrict__ pos_of_pair,
@@ -159,6 +218,28 @@ __global__ void __launch_bounds__(SMALL_PICKS) ffn_plan_small(const int32_t* __r
     if (!late_trigger) pdl_trigger();
     pdl_wait();
     if (late_trigger) pdl_trigger();    // after the wait: the pack, launched now, may read x before its own wait
+    if (P <= 32) {
+        // warp 0 plans; meanwhile warps 1.. quantise x, one (token, 32-block) task per thread
+        const int nb = d / 32;
+        const long tasks = fuse ? (long)T * nb : 0;
+        if (tid < 32) {
+            plan_warp(sel_slot, P, S, bn, pos_of_pair, pair_of_pos, work, n_work, err);
+            if (!fuse) return;
+        } else if (!fuse) {
+            return;
+        }
+        const long i = tid - 32;                                    // task of this thread (warps 1..)
+        const bool warp_busy = tid >= 32 && (i & ~31L) < tasks;     // whole warps quantise together
+        const bool active = tid >= 32 && i < tasks;
+        const long t = active ? i / nb : 0;
+        const int b = active ? (int)(i % nb) : 0;
+        uint4 codes = make_uint4(0u, 0u, 0u, 0u);
+        uint32_t word = 0;
+        if (warp_busy) pack_quantise(x, t, b, d, active, codes, word);
+        __syncthreads();                                            // the positions are visible to the whole block
+        if (active) pack_scatter(pos_of_pair, t, b, k, d, bn, codes, word, xp, xsp);
+        return;
+    }
     uint32_t kv = 0xFFFFFFFFu;
     if (tid < P) {
         int s = sel_slot[tid];
@@ -345,7 +426,13 @@ __global__ void __launch_bounds__(256) ffn_combine(const float* __restrict__ Y, 
 // first: its CTA b takes feature tile b % m_tiles of the (b / m_tiles)-th used
 // slot (one token tile per slot assumed). CTA b of this kernel prefetches the
 // same code blocks and scale atoms into L2, so that the prefetches come from
-// every SM's copy engine at once.
+// every SM's copy engine at once. Only the first PREFETCH_CHUNKS 256-element K
+// chunks of each tile (the first stages the GEMM streams, 128 KB of codes at
+// four chunks) are prefetched: that covers the GEMM's start, while whole tiles
+// (544 KB each at d = 4096) went on arriving after the GEMM had read them
+// itself and took HBM time from it.
+constexpr int PREFETCH_CHUNKS = 4;
+
 __global__ void __launch_bounds__(128) ffn_prefetch_first(const int32_t* __restrict__ sel_slot, int P, int S,
                                                           const uint8_t* __restrict__ arena, long long slot_bytes,
                                                           long long off_codes, long long off_scales, int m_tiles,
@@ -380,13 +467,15 @@ __global__ void __launch_bounds__(128) ffn_prefetch_first(const int32_t* __restr
     if (slot < 0) return;
     const int mt = (int)blockIdx.x % m_tiles;
     const uint8_t* rec = arena + (size_t)slot * slot_bytes;
-    for (int r = threadIdx.x; r < 2 * nc + 2; r += blockDim.x) {
-        if (r < 2 * nc) {
-            const int tile = r < nc ? mt : m_tiles + mt;                // up tiles follow the gate tiles
-            bulk_prefetch_l2(rec + off_codes + ((size_t)tile * nc + r % nc) * 16384, 16384);
+    const int npf = nc < PREFETCH_CHUNKS ? nc : PREFETCH_CHUNKS;
+    const int apf = 2 * npf < atoms ? 2 * npf : atoms;                  // two scale atoms per chunk
+    for (int r = threadIdx.x; r < 2 * npf + 2; r += blockDim.x) {
+        if (r < 2 * npf) {
+            const int tile = r < npf ? mt : m_tiles + mt;               // up tiles follow the gate tiles
+            bulk_prefetch_l2(rec + off_codes + ((size_t)tile * nc + r % npf) * 16384, 16384);
         } else {
-            const int tile = r == 2 * nc ? mt : m_tiles + mt;
-            bulk_prefetch_l2(rec + off_scales + (size_t)tile * atoms * 512, (uint32_t)atoms * 512);
+            const int tile = r == 2 * npf ? mt : m_tiles + mt;
+            bulk_prefetch_l2(rec + off_scales + (size_t)tile * atoms * 512, (uint32_t)apf * 512);
         }
     }
 }

@@ -9,6 +9,8 @@
 // Two kernels:
 //   router_logits_partial  fp32 register-tiled GEMM over a K slice:
 //                          partial[z, t, e] = sum_{i in slice z} x[t,i] W[e,i]
+//   (router_logits_rows    a few tokens in device memory: one CTA per expert
+//                          row, the whole sum over i, no K slices)
 //   route_select           one warp per token: sum the slices in a fixed order
 //                          (+ bias), softmax, wanted and resident top-k by
 //                          warp-shuffle arg-max rounds.
@@ -87,40 +89,128 @@ __global__ void __launch_bounds__(256) router_logits_partial(const uint16_t* __r
     }
 }
 
-// Arg-max across the warp of (value, index): larger value wins, ties to the
-// lower index. Index INT_MAX marks "nothing left".
-__device__ __forceinline__ void warp_argmax(float& v, int& idx) {
+// A few tokens (T <= ROWS_MAX_T) whose x is in device memory: one CTA per
+// expert e reads its whole W_r row, 8 consecutive elements per thread and
+// chunk, with every load in flight at once, and writes logits[t, e] (the
+// single K slice of the selection's input). W_r is loaded before the wait: no
+// kernel of this library writes it, so those loads overlap the end of the
+// previous kernel; x, which that kernel may have written, after. Each sum runs
+// in a fixed order: a thread's chunks and their elements in K order, the warp's
+// butterfly, then the warps in order.
+constexpr int ROWS_THREADS = 256, ROWS_MAX_T = 4, ROWS_MAX_CH = 4;    // d <= 8 * 4 * 256 = 8192
+
+__global__ void __launch_bounds__(ROWS_THREADS) router_logits_rows(const uint16_t* __restrict__ x,
+                                                                   const float* __restrict__ W, int T, int d,
+                                                                   int E, float* __restrict__ logits) {
+    __shared__ float red[ROWS_THREADS / 32][ROWS_MAX_T];
+    pdl_trigger();
+    const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nch = d / 8;
+    const float4* wr = reinterpret_cast<const float4*>(W + (size_t)e * d);
+    float4 wlo[ROWS_MAX_CH], whi[ROWS_MAX_CH];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        float ov = __shfl_xor_sync(0xFFFFFFFFu, v, off);
-        int oi = __shfl_xor_sync(0xFFFFFFFFu, idx, off);
-        if (ov > v || (ov == v && oi < idx)) { v = ov; idx = oi; }
+    for (int j = 0; j < ROWS_MAX_CH; ++j) {
+        const int c = tid + j * ROWS_THREADS;
+        wlo[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        whi[j] = wlo[j];
+        if (c < nch) { wlo[j] = wr[2 * c]; whi[j] = wr[2 * c + 1]; }
+    }
+    pdl_wait();
+    uint4 xv[ROWS_MAX_T][ROWS_MAX_CH];
+#pragma unroll
+    for (int t = 0; t < ROWS_MAX_T; ++t)
+#pragma unroll
+        for (int j = 0; j < ROWS_MAX_CH; ++j) {
+            const int c = tid + j * ROWS_THREADS;
+            xv[t][j] = make_uint4(0u, 0u, 0u, 0u);
+            if (t < T && c < nch) xv[t][j] = *reinterpret_cast<const uint4*>(x + (size_t)t * d + 8 * c);
+        }
+    float acc[ROWS_MAX_T];
+#pragma unroll
+    for (int t = 0; t < ROWS_MAX_T; ++t) {
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < ROWS_MAX_CH; ++j) {
+            const uint4 h = xv[t][j];
+            s = fmaf(__uint_as_float(h.x << 16), wlo[j].x, s);
+            s = fmaf(__uint_as_float(h.x & 0xFFFF0000u), wlo[j].y, s);
+            s = fmaf(__uint_as_float(h.y << 16), wlo[j].z, s);
+            s = fmaf(__uint_as_float(h.y & 0xFFFF0000u), wlo[j].w, s);
+            s = fmaf(__uint_as_float(h.z << 16), whi[j].x, s);
+            s = fmaf(__uint_as_float(h.z & 0xFFFF0000u), whi[j].y, s);
+            s = fmaf(__uint_as_float(h.w << 16), whi[j].z, s);
+            s = fmaf(__uint_as_float(h.w & 0xFFFF0000u), whi[j].w, s);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+        acc[t] = s;
+    }
+    if (lane == 0)
+#pragma unroll
+        for (int t = 0; t < ROWS_MAX_T; ++t) red[warp][t] = acc[t];
+    __syncthreads();
+    if (tid < T) {
+        float s = red[0][tid];
+#pragma unroll
+        for (int w = 1; w < ROWS_THREADS / 32; ++w) s += red[w][tid];
+        logits[(size_t)tid * E + e] = s;
     }
 }
 
-// Bias, softmax over all E, wanted top-k over all experts and resident top-k,
-// for one token whose summed logits lg[i] (expert lane + 32 i) one warp holds.
-// Order by logit (monotone in the score), ties to the lower expert index.
+// Order-preserving map of a float onto uint32 (-0 and +0 both map to +0's
+// image, so that they tie); 0 is below every float's image and means "none".
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+    const uint32_t u = __float_as_uint(f + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Arg-max across the warp of (value, index): larger value wins, ties to the
+// lower index; two warp reductions (redux.sync) instead of a shuffle tree.
+// `has` false: this lane offers nothing. Returns the winning index, or -1
+// when no lane offers anything.
+__device__ __forceinline__ int warp_argmax(float v, int idx, bool has) {
+    const uint32_t u = has ? ordered_key(v) : 0u;
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, u);
+    const uint32_t w = __reduce_min_sync(0xFFFFFFFFu, (has && u == m) ? (uint32_t)idx : 0xFFFFFFFFu);
+    return m == 0u ? -1 : (int)w;
+}
+
+// The bias and slot of the experts a lane holds (lane + 32 i), padding past E.
+// The bias is read before the kernel's wait (no kernel of this library writes
+// it); the slot table after it (ring installs and re-plans rewrite it).
 template <int VPL>
-__device__ __forceinline__ void select_token(float (&lg)[VPL], int t, const float* __restrict__ bias,
-                                             const int32_t* __restrict__ slot_of, int E, int k,
+__device__ __forceinline__ void load_bias(const float* __restrict__ bias, int E, float (&bv)[VPL]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        bv[i] = (bias && e < E) ? bias[e] : 0.0f;
+    }
+}
+template <int VPL>
+__device__ __forceinline__ void load_slots(const int32_t* __restrict__ slot_of, int E, int (&slot)[VPL]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        slot[i] = e < E ? slot_of[e] : -1;
+    }
+}
+
+// Softmax over all E, wanted top-k over all experts and resident top-k, for
+// one token whose logits (bias added) lg[i] (expert lane + 32 i) one warp
+// holds. Order by logit (monotone in the score), ties to the lower expert
+// index. The winning lane of each round writes the pick.
+template <int VPL>
+__device__ __forceinline__ void select_token(float (&lg)[VPL], const int (&slot)[VPL], int t, int E, int k,
                                              int32_t* __restrict__ want_e, float* __restrict__ want_s,
                                              int32_t* __restrict__ sel_e, int32_t* __restrict__ sel_slot,
                                              float* __restrict__ sel_w) {
     const int lane = threadIdx.x & 31;
     const float NEG = -__int_as_float(0x7F800000);   // -inf
-    int slot[VPL];
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const int e = lane + 32 * i;
-        slot[i] = -1;
-        if (e < E) {
-            lg[i] += bias ? bias[e] : 0.0f;
-            slot[i] = slot_of[e];
-        } else {
-            lg[i] = NEG;
-        }
-    }
+    for (int i = 0; i < VPL; ++i)
+        if (lane + 32 * i >= E) lg[i] = NEG;
     // softmax over all E: max, then sum of exp(l - max)
     float mx = NEG;
 #pragma unroll
@@ -143,34 +233,35 @@ __device__ __forceinline__ void select_token(float (&lg)[VPL], int t, const floa
         uint32_t taken = 0;
         for (int j = 0; j < k; ++j) {
             float bv = NEG;
-            int bi = 0x7FFFFFFF;
+            int bi = 0x7FFFFFFF, bq = 0;
+            bool has = false;
 #pragma unroll
             for (int i = 0; i < VPL; ++i) {
-                int e = lane + 32 * i;
-                bool ok = e < E && !((taken >> i) & 1u) && (pass == 0 || slot[i] >= 0);
-                if (ok && (lg[i] > bv || bi == 0x7FFFFFFF)) { bv = lg[i]; bi = e; }
+                const int e = lane + 32 * i;
+                const bool ok = e < E && !((taken >> i) & 1u) && (pass == 0 || slot[i] >= 0);
+                if (ok && (!has || lg[i] > bv)) { bv = lg[i]; bi = e; bq = i; has = true; }
             }
-            warp_argmax(bv, bi);
+            const int win = warp_argmax(bv, bi, has);
             const size_t o = (size_t)t * k + j;
-            if (bi == 0x7FFFFFFF) {           // fewer resident experts than k
+            if (win < 0) {                    // fewer resident experts than k
                 if (lane == 0) { sel_e[o] = -1; sel_slot[o] = -1; sel_w[o] = 0.0f; }
                 continue;
             }
-            const float s = expf(bv - mx) * inv_z;
+            const bool mine = win == bi && has;
             int sl = -1;
-            if ((bi & 31) == lane) {
-                const int i = bi >> 5;
-                taken |= 1u << i;
+            if (mine) {
+                taken |= 1u << bq;
 #pragma unroll
-                for (int q = 0; q < VPL; ++q) if (q == i) sl = slot[q];
-                if (pass == 0) { want_e[o] = bi; want_s[o] = s; }
-                else { sel_e[o] = bi; sel_slot[o] = sl; sel_w[o] = s; }
+                for (int q = 0; q < VPL; ++q) if (q == bq) sl = slot[q];
+                const float s = expf(bv - mx) * inv_z;
+                if (pass == 0) {
+                    want_e[o] = win; want_s[o] = s;
+                    sel_e[o] = win; sel_slot[o] = sl; sel_w[o] = s;     // final if all are resident
+                } else {
+                    sel_e[o] = win; sel_slot[o] = sl; sel_w[o] = s;
+                }
             }
-            if (pass == 0) {
-                sl = __shfl_sync(0xFFFFFFFFu, sl, bi & 31);
-                all_resident = all_resident && sl >= 0;
-                if (lane == 0) { sel_e[o] = bi; sel_slot[o] = sl; sel_w[o] = s; }   // final if all are resident
-            }
+            if (pass == 0) all_resident = all_resident && !__any_sync(0xFFFFFFFFu, mine && sl < 0);
         }
     }
 }
@@ -185,10 +276,14 @@ __global__ void __launch_bounds__(256) route_select(const float* __restrict__ pa
                                                     int32_t* __restrict__ sel_e, int32_t* __restrict__ sel_slot,
                                                     float* __restrict__ sel_w) {
     pdl_trigger();
-    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    float bv[VPL];
+    load_bias<VPL>(bias, E, bv);
+    pdl_wait();
     if (t >= T) return;
+    int slot[VPL];
+    load_slots<VPL>(slot_of, E, slot);
     float lg[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) lg[i] = 0.0f;
@@ -218,7 +313,9 @@ __global__ void __launch_bounds__(256) route_select(const float* __restrict__ pa
             if (e < E) lg[i] += pz[e];
         }
     }
-    select_token<VPL>(lg, t, bias, slot_of, E, k, want_e, want_s, sel_e, sel_slot, sel_w);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) lg[i] += bv[i];
+    select_token<VPL>(lg, slot, t, E, k, want_e, want_s, sel_e, sel_slot, sel_w);
 }
 
 // One CTA of 8 warps per token (many K slices, small batches): warp w sums
@@ -233,9 +330,13 @@ __global__ void __launch_bounds__(256) route_select_cta(const float* __restrict_
                                                         float* __restrict__ sel_w) {
     __shared__ float part[8][VPL * 32];
     pdl_trigger();
-    pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x;
+    float bv[VPL];
+    int slot[VPL];
+    if (warp == 0) load_bias<VPL>(bias, E, bv);
+    pdl_wait();
+    if (warp == 0) load_slots<VPL>(slot_of, E, slot);
     float acc[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) acc[i] = 0.0f;
@@ -268,11 +369,14 @@ __global__ void __launch_bounds__(256) route_select_cta(const float* __restrict_
         lg[i] = part[0][lane + 32 * i];
 #pragma unroll
         for (int w = 1; w < 8; ++w) lg[i] += part[w][lane + 32 * i];
+        lg[i] += bv[i];
     }
-    select_token<VPL>(lg, t, bias, slot_of, E, k, want_e, want_s, sel_e, sel_slot, sel_w);
+    select_token<VPL>(lg, slot, t, E, k, want_e, want_s, sel_e, sel_slot, sel_w);
 }
 
 }  // namespace
+
+bool router_rows_eligible(int T, int d) { return T <= ROWS_MAX_T && d % 8 == 0 && d <= 8 * ROWS_MAX_CH * ROWS_THREADS; }
 
 int route_splits(int T, int E, int d) {
     const int gx = (E + BE - 1) / BE, gy = (T + BT - 1) / BT;
@@ -286,6 +390,11 @@ cudaError_t launch_route(const RouteLaunch& a, cudaStream_t s) {
     cudaError_t e;
     if (a.wsplit) {
         e = launch_router_tc(a.x, a.w, a.T, a.d, a.E, a.splits, a.wsplit, a.partial, a.err, s);
+    } else if (a.rows) {
+        moe_prof_begin(MK_ROUTER_LOGITS, s);
+        e = moe_launch(router_logits_rows, dim3(a.E), dim3(ROWS_THREADS), 0, s, a.x, a.w, a.T, a.d, a.E, a.partial);
+        moe_prof_end(MK_ROUTER_LOGITS, s);
+        moe_count_launches(1);
     } else {
         dim3 g1((a.E + BE - 1) / BE, (a.T + BT - 1) / BT, a.splits);
         moe_prof_begin(MK_ROUTER_LOGITS, s);
@@ -391,7 +500,8 @@ extern "C" moe_status moe_route_resident_noalloc(const void* hidden_bf16, const 
     if (E > 1024) return MOE_EUNSUPPORTED;
     const int splits = route_splits(T, E, d);
     if ((size_t)splits * T * E > kNoAllocPartials) return MOE_EUNSUPPORTED;   // beyond the fixed array
-    if (pointer_kind(hidden_bf16) < 0) return MOE_EINVAL;
+    const int hk = pointer_kind(hidden_bf16);
+    if (hk < 0) return MOE_EINVAL;
     float* partials = nullptr;
     if (noalloc_partials(&partials) != cudaSuccess) return MOE_ECUDA;
     RouteLaunch a{};
@@ -401,6 +511,7 @@ extern "C" moe_status moe_route_resident_noalloc(const void* hidden_bf16, const 
     a.slot_of = slot_of;
     a.T = T; a.d = d; a.E = E; a.k = k;
     a.splits = splits;
+    if (hk == 0 && router_rows_eligible(T, d)) { a.rows = 1; a.splits = 1; }
     a.want_e = want_e; a.want_s = want_s; a.sel_e = sel_e; a.sel_slot = sel_slot; a.sel_w = sel_w;
     a.partial = partials;      // every element read below is written earlier in the same call
     return launch_route(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK : MOE_ECUDA;

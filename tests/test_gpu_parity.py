@@ -74,7 +74,10 @@ def check_route(c, g, rows):
 # E % 16 == 0): ragged token tails, E below one 128-expert tile, one and two K slices.
 ROUTE_CASES = [(synth.TINY, 8), (RAGGED, 37), (SPARSE, 5), (synth.DECODE, 1), (synth.DECODE, 8),
                (synth.DECODE, 64), (synth.GLM, 16), (synth.TINY, 200), (ODD, 257), (RAGGED, 130),
-               (synth.DECODE, 65), (synth.DECODE, 300), (synth.GLM, 130)]
+               (synth.DECODE, 65), (synth.DECODE, 300), (synth.GLM, 130),
+               # up to 4 tokens: one CTA per expert row; 5 tokens: back to the K-sliced router
+               (synth.TINY, 1), (SPARSE, 3), (synth.DECODE, 2), (synth.DECODE, 4), (synth.GLM, 4), (ODD, 4),
+               (synth.DECODE, 5)]
 
 
 @pytest.mark.parametrize("cfg,T", ROUTE_CASES, ids=[f"{c.name.split()[0]}-T{T}" for c, T in ROUTE_CASES])
@@ -204,7 +207,11 @@ FFN_CASES = [(synth.TINY, 8, None), (RAGGED, 37, None), (SPARSE, 5, None), (synt
              # batches above 64 tokens: 128-row tiles, token-major gate/up, then down rows and the ordered combine
              (synth.TINY, 80, None), (RAGGED, 100, None), (synth.DECODE, 200, 4),
              # 8192 picks and more: the plan runs in several CTAs
-             (synth.TINY, 2048, None), (RAGGED, 2731, None)]
+             (synth.TINY, 2048, None), (RAGGED, 2731, None),
+             # at most 32 picks: the one-warp plan (x packed in the same launch when it is small);
+             # 33 picks: the block plan
+             (synth.TINY, 1, None), (synth.DECODE, 2, None), (synth.DECODE, 4, None), (synth.GLM, 4, None),
+             (RAGGED, 10, None), (RAGGED, 11, None)]
 
 
 @pytest.mark.parametrize("cfg,T,sample", FFN_CASES, ids=[f"{c.name.split()[0]}-T{T}" for c, T, _ in FFN_CASES])
