@@ -235,6 +235,17 @@ def test_ffn_parity(cfg, T, sample):
     assert np.all(got[empty] == 0)
 
 
+@pytest.mark.parametrize("T", [3, 9])
+def test_ffn_all_picks_padding(T):
+    """No pick anywhere (no expert resident, so the plan's work list is empty): exact zeros in place of
+    the NaN the output held, with the one-warp plan (3 tokens) and the block plan (9 tokens)."""
+    cfg = synth.TINY
+    c = make_case(cfg, T)
+    arena = device_arena(cfg, c.owner, c.n_slots)
+    got = gpu_ffn(c, arena, np.full((T, cfg.k), -1, np.int32), np.zeros((T, cfg.k), np.float32))
+    assert np.all(got == 0)
+
+
 def test_ffn_repeatable_bit_exact():
     c = make_case(synth.DECODE, 8)
     arena = device_arena(c.cfg, c.owner, c.n_slots)
