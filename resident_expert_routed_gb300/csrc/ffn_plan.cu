@@ -408,29 +408,15 @@ __global__ void __launch_bounds__(256) ffn_combine(const float* __restrict__ Y, 
     const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
     if (c >= d) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    // eight picks' loads at a time, none waiting on another's slot test (a padded pick's
-    // row is read but not used), then the sums in pick order
-    constexpr int KB = 8;
-    for (int j0 = 0; j0 < k; j0 += KB) {
-        int s[KB];
-        float w[KB];
-        float4 y[KB];
-#pragma unroll
-        for (int u = 0; u < KB; ++u) {
-            const size_t p = (size_t)t * k + j0 + u;
-            const bool in = j0 + u < k;
-            s[u] = in ? sel_slot[p] : -1;
-            w[u] = in ? sel_w[p] : 0.0f;
-            y[u] = in ? *reinterpret_cast<const float4*>(Y + p * d + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < KB; ++u) {
-            if (s[u] < 0 || s[u] >= S) continue;
-            acc.x = fmaf(w[u], y[u].x, acc.x);
-            acc.y = fmaf(w[u], y[u].y, acc.y);
-            acc.z = fmaf(w[u], y[u].z, acc.z);
-            acc.w = fmaf(w[u], y[u].w, acc.w);
-        }
+    for (int j = 0; j < k; ++j) {
+        const int s = sel_slot[(size_t)t * k + j];
+        if (s < 0 || s >= S) continue;
+        const float w = sel_w[(size_t)t * k + j];
+        const float4 y = *reinterpret_cast<const float4*>(Y + ((size_t)t * k + j) * d + c);
+        acc.x = fmaf(w, y.x, acc.x);
+        acc.y = fmaf(w, y.y, acc.y);
+        acc.z = fmaf(w, y.z, acc.z);
+        acc.w = fmaf(w, y.w, acc.w);
     }
     *reinterpret_cast<float4*>(out + (size_t)t * d + c) = acc;
 }
