@@ -18,7 +18,7 @@
 // The weight tiles are the MMA's A operand (M = 128) and the few routed rows
 // the B operand (N = 16..128), so a decode-sized tile still streams whole
 // weight tiles at full width. Roles:
-//   warp 4     lane 0, per stage: 32 KB of weight codes as contiguous bulk
+//   warp 4     lane 0, per stage: 64 KB of weight codes as contiguous bulk
 //              copies (the arena keeps codes in tile-major 16 KB blocks, already
 //              in the 128-byte swizzle) and TMA boxes of activation rows (their
 //              height the tile's row count rounded up);
@@ -109,7 +109,9 @@ __device__ __forceinline__ void scale_writer(int n_stages, const Load& load, uin
 // loads, per chunk, one 16 KB code block of the gate tile and one of the up
 // tile (rows f0..f0+127 and ffn+f0..ffn+f0+127) and accumulates them into two
 // TMEM accumulators, so that each epilogue thread holds g and u of the same
-// feature; the down GEMM loads one tile. Stages carry 32 KB of weights.
+// feature; the down GEMM loads one tile. Decode stages carry 64 KB of weights
+// (two chunks of gate and up, or four of one down tile); with twice the atoms
+// per stage the scale writers then look two stages ahead instead of four.
 template <int MODE, int BN, int NS, int KCH, int NBUF>
 struct Cfg {
     static constexpr int THREADS = 320;           // warps 0-3 epilogue, 4 TMA, 5 MMA, 6-9 scales
@@ -119,7 +121,7 @@ struct Cfg {
     static constexpr int B_CHUNK = BN * 128;
     static constexpr int B_BYTES = KCH * B_CHUNK;
     static constexpr int NV = (NMAT + 1) * 2 * KCH;        // scale atoms per stage (weights, then activations)
-    static constexpr int PF = 4;                           // stages of scales loaded ahead (registers: 4 NV uint4)
+    static constexpr int PF = NMAT * KCH >= 4 ? 2 : 4;     // stages of scales loaded ahead (registers: PF NV uint4)
     static constexpr int SF_COLS = 4 * NV;                 // TMEM columns of one stage's scales
     static constexpr int ACC_COLS = NMAT * BN;    // one accumulator buffer (gate, then up)
     static constexpr int OFF_A = 0;
@@ -132,7 +134,7 @@ struct Cfg {
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
     static_assert(BN == 16 || BN == 32 || BN == 64 || BN == 128, "BN");
-    static_assert(KCH == 1 || KCH == 2, "KCH");
+    static_assert(KCH == 1 || KCH == 2 || KCH == 4, "KCH");
     static_assert(NBUF == 1 || NBUF == 2, "NBUF");
     static_assert(TMEM_USED <= 512, "TMEM");
     static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -712,18 +714,22 @@ cudaError_t launch_tokens(const GemmMaps& maps, const GemmArgs& g, long max_item
 
 template <int MODE>
 cudaError_t launch_mode(const GemmMaps& maps, const GemmArgs& g, long max_items, int bn, cudaStream_t s) {
-    if constexpr (MODE == 1) {   // gate + up tiles per stage: 32 KB of weights at KCH = 1
+    // 64 KB of weights per stage: with fewer CTAs streaming than SMs, one SM takes about
+    // 100 GB/s from HBM through five 32 KB stages and 140-160 GB/s through three 64 KB ones
+    // (microbench/bulk_stream_rate.cu), which is what the CTAs left in a partial last round,
+    // or in a grid of few items, get.
+    if constexpr (MODE == 1) {   // gate + up tiles, two 256-element K chunks per stage
         switch (bn) {
-            case 16: return launch_one<MODE, 16, 5, 1, 2>(maps, g, max_items, s);
-            case 32: return launch_one<MODE, 32, 5, 1, 2>(maps, g, max_items, s);
-            case 64: return launch_one<MODE, 64, 5, 1, 2>(maps, g, max_items, s);
+            case 16: return launch_one<MODE, 16, 3, 2, 2>(maps, g, max_items, s);
+            case 32: return launch_one<MODE, 32, 3, 2, 2>(maps, g, max_items, s);
+            case 64: return launch_one<MODE, 64, 2, 2, 2>(maps, g, max_items, s);
             default: return launch_one<MODE, 128, 4, 1, 1>(maps, g, max_items, s);
         }
     }
-    else switch (bn) {      // one tile per stage: 32 KB of weights at KCH = 2
-        case 16: return launch_one<MODE, 16, 5, 2, 2>(maps, g, max_items, s);
-        case 32: return launch_one<MODE, 32, 5, 2, 2>(maps, g, max_items, s);
-        case 64: return launch_one<MODE, 64, 4, 2, 2>(maps, g, max_items, s);
+    else switch (bn) {      // one tile, four chunks per stage
+        case 16: return launch_one<MODE, 16, 3, 4, 2>(maps, g, max_items, s);
+        case 32: return launch_one<MODE, 32, 2, 4, 2>(maps, g, max_items, s);
+        case 64: return launch_one<MODE, 64, 2, 4, 2>(maps, g, max_items, s);
         default: return launch_one<MODE, 128, 3, 2, 2>(maps, g, max_items, s);
     }
 }
