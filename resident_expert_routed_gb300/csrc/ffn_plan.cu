@@ -200,6 +200,7 @@ __device__ __forceinline__ void plan_warp(const int32_t* __restrict__ sel_slot, 
 // same CTA then quantises x and writes the operand rows, which saves the pack
 // launch: x is complete here, since this kernel runs after its wait.
 constexpr int SMALL_PICKS = 1024;
+constexpr int SLOT_SCAN_MAX = 2048;                     // arenas up to this many slots plan by counting
 constexpr long FUSED_PACK_TASKS = 512;                  // (token, 32-block) tasks: T <= 4 at d = 4096
 static_assert(FUSED_PACK_TASKS <= SMALL_PICKS - 32, "the one-warp plan quantises one task per thread of warps 1..");
 
@@ -498,8 +499,11 @@ cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
     // batches of 8 tokens or more quantise x while the plan runs (large batches always: their plan ends
     // with plan_place, which signals after its wait)
     const int early = a.plan_ctas > 0 || a.T >= 8 ? 1 : 0;
+    // more than 32 picks over an arena of a few thousand slots at most: counting per slot (shared
+    // atomics, one scan over the slots) is cheaper than the small plan's sort, which wins on large arenas
+    const bool by_slot = a.plan_ctas == 0 && P > 32 && a.S <= SLOT_SCAN_MAX;
     // few tokens: the small plan also packs x (one launch fewer)
-    const bool fused = a.plan_ctas == 0 && P <= SMALL_PICKS && (long)a.T * (a.d / 32) <= FUSED_PACK_TASKS;
+    const bool fused = a.plan_ctas == 0 && P <= SMALL_PICKS && !by_slot && (long)a.T * (a.d / 32) <= FUSED_PACK_TASKS;
     const size_t smem = (size_t)a.S * sizeof(int32_t);
     static bool attr_set[64] = {};
     static bool attr_set_multi[64] = {};
@@ -532,7 +536,7 @@ cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s) {
                            a.pos_of_pair, a.pair_of_pos);
         moe_count_launches(2);
     } else {
-        if (P <= SMALL_PICKS)
+        if (P <= SMALL_PICKS && !by_slot)
             e = moe_launch(ffn_plan_small, dim3(1), dim3(SMALL_PICKS), 0, s, a.sel_slot, P, a.S, a.bn, a.pos_of_pair,
                            a.pair_of_pos, a.work, a.n_work, fused ? 0 : early, fused ? 1 : 0, a.x, a.T, a.k, a.d,
                            a.xp, a.xsp, a.err);

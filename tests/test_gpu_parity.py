@@ -235,6 +235,28 @@ def test_ffn_parity(cfg, T, sample):
     assert np.all(got[empty] == 0)
 
 
+@pytest.mark.parametrize("T", [8, 40, 256])
+def test_ffn_parity_large_arena(T):
+    """Arenas above 2048 slots: more than 32 picks plan by sorting (slot, pick) keys (up to 1024 picks)
+    instead of counting per slot. The tiny layer's residents spread over 2100 slots."""
+    cfg = synth.TINY
+    c = make_case(cfg, T)
+    n_slots = 2100
+    res = np.flatnonzero(c.slot_of >= 0)
+    slot_of = np.full(cfg.E, -1, np.int32)
+    slot_of[res] = 7 + 203 * np.arange(len(res))
+    owner = np.full(n_slots, -1, np.int32)
+    owner[slot_of[res]] = res
+    arena = device_arena(cfg, owner, n_slots)
+    ref_route = oracle.route(c.x, c.W, c.bias, slot_of, cfg.k)
+    sel_slot, sel_w = ref_route["sel_slot"], ref_route["sel_w"]
+    got = gpu_ffn(c, arena, sel_slot, sel_w.astype(np.float32))
+    sel_u, experts = oracle_experts(cfg, owner, sel_slot)
+    ref = oracle.ffn(c.x, sel_u, sel_w.astype(np.float32).astype(np.float64), experts, cfg.d, cfg.ffn)
+    ok, fro, mx = ffn_within_tolerance(got, ref)
+    assert ok, (fro, mx, np.abs(ref).max())
+
+
 @pytest.mark.parametrize("T", [3, 9])
 def test_ffn_all_picks_padding(T):
     """No pick anywhere (no expert resident, so the plan's work list is empty): exact zeros in place of
