@@ -117,13 +117,19 @@ typedef struct {
  * workspace: >= moe_workspace_bytes(T, k, d, ffn, E, S) bytes (any ffn, S).
  * hidden_bf16, w_router and workspace must be 16-byte aligned (MOE_EINVAL).
  * hidden_bf16 may be device memory or page-locked host memory (cudaHostAlloc,
- * cudaHostRegister), which the kernels read directly; pageable host memory is
- * refused (MOE_EINVAL).
- * Batches of more than 64 tokens with d % 64 == 0 and E % 16 == 0 in device
- * memory are scored on the tensor cores: W_r is split exactly into three bf16
- * parts in the workspace and the products are accumulated in fp32, so the
- * logits match the CUDA-core path up to fp32 rounding order. A batch in host
- * memory is always scored on the CUDA cores.
+ * cudaHostRegister); pageable host memory is refused (MOE_EINVAL). A batch of
+ * at most 4 tokens (d <= 8192) in host memory is first copied (once, by a
+ * kernel) into the workspace and scored from there, with the same kernels and
+ * results as from device memory; a larger one is read in place (there the
+ * K-sliced router's reads of it cost less than a separate copy).
+ * Up to 4 tokens in device memory (or staged) with d <= 8192, each expert's
+ * W_r row is read and summed whole by one CTA; up to 64 tokens, K is split
+ * into slices summed in a fixed order by the selection. Batches of more than
+ * 64 tokens with d % 64 == 0 and E % 16 == 0 in device memory are scored on
+ * the tensor cores: W_r is split exactly into three bf16 parts in the
+ * workspace and the products are accumulated in fp32, so the logits match the
+ * CUDA-core path up to fp32 rounding order. A batch of more than 64 tokens in
+ * host memory is scored on the CUDA cores.
  * Limits: 1 <= k <= 32, k <= E <= 1024, d % 32 == 0, T >= 1.
  */
 moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, const float* bias,

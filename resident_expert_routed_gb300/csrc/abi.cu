@@ -90,12 +90,15 @@ FfnCarve ffn_carve(int T, int k, int d, int F, int S) {
     return c;
 }
 
-// Routing workspace: the split-K partial logits of the CUDA-core router, or,
-// for batches the tensor-core router can take, the larger of that and its
-// three bf16 parts of W_r followed by its partials (a batch in host memory is
-// always scored by the CUDA-core router).
+// Routing workspace: the split-K partial logits of the CUDA-core router (then,
+// for batches the row-per-CTA router takes, room for such a batch in host
+// memory, copied there once and scored from there), or, for batches the
+// tensor-core router can take, the larger of that and its three bf16 parts of
+// W_r followed by its partials (a larger batch in host memory is scored by the
+// K-sliced CUDA-core router in place).
 size_t route_bytes(int T, int E, int d) {
-    const size_t simt = align_up((size_t)route_splits(T, E, d) * T * E * 4, 256);
+    size_t simt = align_up((size_t)route_splits(T, E, d) * T * E * 4, 256);
+    if (router_rows_eligible(T, d)) simt += align_up((size_t)T * d * 2, 256);   // a host batch, staged here
     if (!router_tc_eligible(T, E, d)) return simt;
     return std::max(simt, router_tc_split_bytes(E, d) + align_up((size_t)router_tc_splits(T, E, d) * T * E * 4, 256));
 }
@@ -264,10 +267,17 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
     if (E > 1024) return MOE_EUNSUPPORTED;
     if ((size_t)T * E > ((size_t)1 << 31)) return MOE_EUNSUPPORTED;
     if (ws_bytes < route_bytes(T, E, d)) return MOE_ENOMEM;
-    const int hk = pointer_kind(hidden_bf16);
+    int hk = pointer_kind(hidden_bf16);
     if (hk < 0) return MOE_EINVAL;
     RouteLaunch a{};
     a.x = static_cast<const uint16_t*>(hidden_bf16);
+    if (hk == 1 && router_rows_eligible(T, d)) {      // a few host tokens: one copy across the link, then HBM
+        void* staged = static_cast<uint8_t*>(workspace) + align_up((size_t)route_splits(T, E, d) * T * E * 4, 256);
+        const cudaError_t se = launch_stage_rows(hidden_bf16, staged, (size_t)T * d * 2, static_cast<cudaStream_t>(stream));
+        if (se != cudaSuccess) return cuda_status(se);
+        a.x = static_cast<const uint16_t*>(staged);
+        hk = 0;
+    }
     a.w = w_router;
     a.bias = bias;
     a.slot_of = slot_of;

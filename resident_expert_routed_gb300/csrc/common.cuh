@@ -278,6 +278,9 @@ struct RouteLaunch {
     int rows;               // 1: one CTA per expert row (few tokens in device memory; splits = 1)
 };
 bool router_rows_eligible(int T, int d);
+// A batch in page-locked host memory that the row-per-CTA router can take is copied once into the
+// routing workspace, after the partial logits, and scored from there.
+cudaError_t launch_stage_rows(const void* src, void* dst, size_t bytes, cudaStream_t s);
 bool router_tc_eligible(int T, int E, int d);
 int pointer_kind(const void* p);      // 0 device, 1 page-locked host, -1 pageable host
 int router_tc_splits(int T, int E, int d);

@@ -374,7 +374,27 @@ __global__ void __launch_bounds__(256) route_select_cta(const float* __restrict_
     select_token<VPL>(lg, slot, t, E, k, want_e, want_s, sel_e, sel_slot, sel_w);
 }
 
+// A batch in page-locked host memory, copied once into device memory (16-byte
+// chunks, grid-stride): the routing kernels then read it from HBM instead of
+// pulling it across the chip-to-chip link several times.
+__global__ void __launch_bounds__(256) stage_rows(const uint4* __restrict__ src, uint4* __restrict__ dst, long n16) {
+    pdl_trigger();
+    pdl_wait();
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (long)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
 }  // namespace
+
+cudaError_t launch_stage_rows(const void* src, void* dst, size_t bytes, cudaStream_t s) {
+    const long n16 = (long)(bytes / 16);
+    long grid = (n16 + 255) / 256;
+    if (grid > moe_sm_count()) grid = moe_sm_count();
+    const cudaError_t e = moe_launch(stage_rows, dim3((unsigned)grid), dim3(256), 0, s,
+                                     static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+    moe_count_launches(1);
+    return e;
+}
 
 bool router_rows_eligible(int T, int d) { return T <= ROWS_MAX_T && d % 8 == 0 && d <= 8 * ROWS_MAX_CH * ROWS_THREADS; }
 

@@ -369,9 +369,9 @@ def test_bad_slot_id_sets_error_word_and_is_skipped():
 
 
 def test_route_and_ffn_read_a_pinned_host_batch():
-    # a batch in page-locked host memory: the kernels read it directly (routing on the CUDA cores even above
-    # 64 tokens, where a device batch takes the tensor-core router); the FFN output, also written to pinned host
-    # memory, equals the device-buffer call's bit for bit
+    # a batch of more than 64 tokens in page-locked host memory: the kernels read it directly (routing on the
+    # CUDA cores, where a device batch takes the tensor-core router); the FFN output, also written to pinned
+    # host memory, equals the device-buffer call's bit for bit
     cfg, T = synth.TINY, 130
     c = make_case(cfg, T)
     arena = device_arena(cfg, c.owner, c.n_slots)
@@ -402,6 +402,35 @@ def test_route_and_ffn_read_a_pinned_host_batch():
     moe.moe_expert_ffn_mxfp4(host_x, sel_slot, sel_w, arena, out_host, ws)
     torch.cuda.synchronize()
     assert torch.equal(out_dev.cpu(), out_host)
+    assert moe.moe_device_status() == (moe.MOE_OK, 0)
+
+
+@pytest.mark.parametrize("cfg,T", [(synth.TINY, 1), (synth.DECODE, 2), (synth.DECODE, 4), (synth.DECODE, 5),
+                                   (synth.DECODE, 64), (RAGGED, 37)],
+                         ids=lambda v: getattr(v, "name", str(v)).split()[0])
+def test_small_host_batch_routes_like_a_device_batch(cfg, T):
+    """A batch in page-locked host memory: up to 4 tokens it is copied into the workspace first and scored
+    by the row-per-CTA router, above that the K-sliced router reads it in place; either way the routing
+    outputs equal those of the same batch in device memory, and the oracle's."""
+    c = make_case(cfg, T)
+    host_x = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    k = cfg.k
+    ws = torch.empty(moe.moe_workspace_bytes(T, k, cfg.d, cfg.ffn, cfg.E, c.n_slots), dtype=torch.uint8,
+                     device="cuda")
+    outs = {}
+    for name, x in (("device", hidden_dev(c.x)), ("host", host_x)):
+        o = [torch.full((T, k), -7, dtype=torch.int32, device="cuda"),
+             torch.full((T, k), float("nan"), dtype=torch.float32, device="cuda"),
+             torch.full((T, k), -7, dtype=torch.int32, device="cuda"),
+             torch.full((T, k), -7, dtype=torch.int32, device="cuda"),
+             torch.full((T, k), float("nan"), dtype=torch.float32, device="cuda")]
+        moe.moe_route_resident(x, to_dev(c.W), to_dev(c.bias), to_dev(c.slot_of), k, *o, ws)
+        torch.cuda.synchronize()
+        outs[name] = [v.cpu().numpy() for v in o]
+    for a, b in zip(outs["device"], outs["host"]):
+        assert np.array_equal(a, b)
+    g = dict(zip(("want_e", "want_s", "sel_e", "sel_slot", "sel_w"), outs["host"]))
+    check_route(c, g, np.arange(T))
     assert moe.moe_device_status() == (moe.MOE_OK, 0)
 
 
