@@ -150,7 +150,8 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
 moe_status moe_renormalise_weights(const int32_t* sel_slot, float* sel_w, int T, int k, void* stream);
 
 /*
- * moe_route_resident without a caller workspace (the paper has no counterpart:
+ * moe_route_resident without a caller workspace (nothing in the TideLM README
+ * corresponds to it:
  * this exists for callers of this library that cannot allocate device memory
  * when they route -- e.g. a serving loop whose memory budget was fixed at
  * start-up, or a plug-in whose host framework owns every allocation -- since
