@@ -24,6 +24,12 @@ SPARSE = synth.LayerConfig("sparse E16 k4 d256 F128 R2", E=16, k=4, d=256, ffn=1
 ODD = synth.LayerConfig("odd E48 k6 d320 F128 R30", E=48, k=6, d=320, ffn=128, resident=30, sigma=1.0,
                         seed=0x7EED00A2)
 
+# Routing only: the widest rows the row-per-CTA router takes (d = 8192), and one 32-element block wider.
+WIDE = synth.LayerConfig("wide E64 k4 d8192 F128 R40", E=64, k=4, d=8192, ffn=128, resident=40, sigma=1.0,
+                         seed=0x7EED00A3)
+WIDER = synth.LayerConfig("wider E64 k4 d8224 F128 R40", E=64, k=4, d=8224, ffn=128, resident=40, sigma=1.0,
+                          seed=0x7EED00A4)
+
 
 @dataclasses.dataclass
 class Case:

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import synth
-from tests.cases import (ODD, RAGGED, SPARSE, device_arena, ffn_within_tolerance, hidden_dev, make_case,
+from tests.cases import (ODD, RAGGED, SPARSE, WIDE, WIDER, device_arena, ffn_within_tolerance, hidden_dev, make_case,
                          near_tie_tokens, oracle_experts, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -77,7 +77,9 @@ ROUTE_CASES = [(synth.TINY, 8), (RAGGED, 37), (SPARSE, 5), (synth.DECODE, 1), (s
                (synth.DECODE, 65), (synth.DECODE, 300), (synth.GLM, 130),
                # up to 4 tokens: one CTA per expert row; 5 tokens: back to the K-sliced router
                (synth.TINY, 1), (SPARSE, 3), (synth.DECODE, 2), (synth.DECODE, 4), (synth.GLM, 4), (ODD, 4),
-               (synth.DECODE, 5)]
+               (synth.DECODE, 5),
+               # the row-per-CTA router's width limit: d = 8192 takes it, d = 8224 the K-sliced router
+               (WIDE, 1), (WIDE, 4), (WIDER, 4)]
 
 
 @pytest.mark.parametrize("cfg,T", ROUTE_CASES, ids=[f"{c.name.split()[0]}-T{T}" for c, T in ROUTE_CASES])
