@@ -11,8 +11,13 @@
 //   each slot a segment of positions padded to a multiple of the tile height
 //   BN, gives every pick a position in its slot's segment, and writes the GEMM
 //   work list: (slot, first position, rows) per tile of at most BN rows.
+//   ffn_plan_small computes the same from a sort of (slot, pick) keys, with
+//   work in proportion to the picks (arenas of thousands of slots), in one
+//   warp for at most 32 picks (and then also packs x for a few tokens).
 //   Large batches split it: plan_count (per-CTA histograms), plan_scan (one
 //   CTA: per-CTA offsets within each slot, segments, work list), plan_place.
+// ffn_prefetch_first (side stream): L2 prefetch of the first K chunks of the
+//   weight tiles the gate/up GEMM's CTAs stream first.
 // ffn_pack: quantises every token row of x to MXFP4 once (OCP MX v1.0:
 //   exponent floor(log2 amax) - 2, round to nearest even, saturate at 6; two
 //   codes per byte, even element low) and writes it into row `position` of

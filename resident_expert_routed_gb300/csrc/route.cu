@@ -9,11 +9,13 @@
 // Two kernels:
 //   router_logits_partial  fp32 register-tiled GEMM over a K slice:
 //                          partial[z, t, e] = sum_{i in slice z} x[t,i] W[e,i]
-//   (router_logits_rows    a few tokens in device memory: one CTA per expert
-//                          row, the whole sum over i, no K slices)
-//   route_select           one warp per token: sum the slices in a fixed order
-//                          (+ bias), softmax, wanted and resident top-k by
-//                          warp-shuffle arg-max rounds.
+//   (router_logits_rows    up to 4 tokens: one CTA per expert row, the whole
+//                          sum over i, no K slices; a batch in host memory is
+//                          first copied to the workspace by stage_rows)
+//   route_select           one warp per token (one CTA with many slices): sum
+//                          the slices in a fixed order (+ bias), softmax,
+//                          wanted and resident top-k by redux.sync arg-max
+//                          rounds.
 // The K split keeps >= ~256 CTAs streaming W_r at decode sizes; the partials
 // are small and stay in L2.
 #include <mutex>
