@@ -181,8 +181,7 @@ struct moe_hot_ring {
 
 namespace {
 
-cudaError_t launch_batch(bool install, moe_hot_ring* r, const RingBatch& b, int32_t* slot_of, int32_t* owner,
-                         cudaStream_t s) {
+cudaError_t launch_batch(bool install, const RingBatch& b, int32_t* slot_of, int32_t* owner, cudaStream_t s) {
     if (b.n == 0) return cudaSuccess;
     cudaError_t e;
     if (install) {
@@ -232,7 +231,7 @@ extern "C" moe_status moe_hot_ring_step(moe_hot_ring* r, const int32_t* heavy_fl
     // 1. install what the previous call copied
     if (r->pending.n > 0) {
         if (cudaStreamWaitEvent(s, r->copied, 0) != cudaSuccess) return MOE_ECUDA;
-        if (launch_batch(true, r, r->pending, slot_of, owner, s) != cudaSuccess) return MOE_ECUDA;
+        if (launch_batch(true, r->pending, slot_of, owner, s) != cudaSuccess) return MOE_ECUDA;
         r->pending.n = 0;
     }
     // 2. this step's heavy-miss list
@@ -257,7 +256,7 @@ extern "C" moe_status moe_hot_ring_step(moe_hot_ring* r, const int32_t* heavy_fl
         ++b.n;
     }
     if (b.n == 0) return MOE_OK;
-    if (launch_batch(false, r, b, slot_of, owner, s) != cudaSuccess || cudaEventRecord(r->evicted, s) != cudaSuccess ||
+    if (launch_batch(false, b, slot_of, owner, s) != cudaSuccess || cudaEventRecord(r->evicted, s) != cudaSuccess ||
         cudaStreamWaitEvent(cs, r->evicted, 0) != cudaSuccess)
         return MOE_ECUDA;
     uint8_t* base = static_cast<uint8_t*>(r->arena.base);
