@@ -159,7 +159,12 @@ moe_status moe_renormalise_weights(const int32_t* sel_slot, float* sel_w, int T,
  * moe_route_resident, minus the workspace; it allocates nothing. It always
  * scores on the CUDA cores, so for batches that moe_route_resident scores on
  * the tensor cores (above 64 tokens) the logits can differ in the last fp32
- * bits, and a pick at a near-tie can differ.
+ * bits, and a pick at a near-tie can differ. A batch in page-locked host
+ * memory is read in place by the K-sliced router at every size (there is no
+ * workspace to copy it into): each K slice reads its rows across the
+ * chip-to-chip link, and for up to 4 tokens, which moe_route_resident copies
+ * to the device and sums row by row, the fp32 summation order differs, with
+ * the same last-bit and near-tie caveat.
  * The split-K partial logits live in one fixed device array of 4 MiB
  * (2^20 fp32) inside the library, held by every GPU that loads the library
  * until the process exits; a call whose partials would not fit

@@ -113,6 +113,40 @@ def near_tie_tokens(scores: np.ndarray, mask: np.ndarray, k: int, rel: float = 1
     return out
 
 
+def clear_ranks(scores_row: np.ndarray, mask: np.ndarray, k: int, rel: float = 1e-5) -> np.ndarray:
+    """For the oracle's ranking of the masked experts by score (descending), which of the first k ranks are
+    separated from both neighbours (the previous rank and the next one, the (k+1)-th included) by more than
+    `rel` relative: at those ranks the expert is fixed whatever the rounding order of the scores."""
+    r = np.sort(scores_row[mask])[::-1][:k + 1]
+    n = min(k, len(r))
+    clear = np.zeros(k, bool)
+    for j in range(n):
+        above = j == 0 or r[j - 1] - r[j] > rel * r[j - 1]
+        below = j + 1 >= len(r) or r[j] - r[j + 1] > rel * r[j]
+        clear[j] = above and below
+    return clear
+
+
+def covering_rows(sel_slot: np.ndarray, extra: int = 8, seed: int = 11) -> np.ndarray:
+    """A sample of token rows that routes to every slot the batch uses: for each used slot (rarest first) not
+    yet covered, the LAST token that picks it (its pick sits at the end of the slot's rows, i.e. in the last,
+    usually partial, tile of that slot), plus `extra` seeded rows. Sorted, without repeats."""
+    T = sel_slot.shape[0]
+    slots, counts = np.unique(sel_slot[sel_slot >= 0], return_counts=True)
+    covered = np.zeros(int(sel_slot.max(initial=-1)) + 1, bool)
+    rows = set()
+    for s in slots[np.argsort(counts, kind="stable")]:
+        if covered[s]:
+            continue
+        t = int(np.flatnonzero((sel_slot == s).any(axis=1))[-1])
+        rows.add(t)
+        row = sel_slot[t]
+        covered[row[row >= 0]] = True
+    rng = np.random.default_rng(seed)
+    rows.update(int(v) for v in rng.choice(T, size=min(extra, T), replace=False))
+    return np.array(sorted(rows), np.int64)
+
+
 def ring_case(cfg: synth.LayerConfig, n_ring: int, T: int = 8, stream: int = 0):
     """A drifted case with cfg.resident main slots + n_ring ring slots (device arena), its tables, and a
     pinned host store of every absent expert's record (the stand-in for the drive): returns

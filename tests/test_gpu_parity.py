@@ -14,8 +14,9 @@ import torch
 
 import oracle
 import synth
-from tests.cases import (ODD, RAGGED, SPARSE, WIDE, WIDER, device_arena, ffn_within_tolerance, hidden_dev, make_case,
-                         near_tie_tokens, oracle_experts, to_dev)
+from tests import oracle_pool
+from tests.cases import (ODD, RAGGED, SPARSE, WIDE, WIDER, clear_ranks, device_arena, ffn_within_tolerance,
+                         covering_rows, hidden_dev, make_case, near_tie_tokens, oracle_experts, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -38,14 +39,17 @@ def gpu_route(c, T_rows=None):
     return {kk: v.cpu().numpy() for kk, v in dev.items()}
 
 
-def check_route(c, g, rows):
-    """Compare GPU routing on token rows `rows` with the oracle on those rows."""
+def check_route(c, g, rows, ref=None):
+    """Compare GPU routing on token rows `rows` with the oracle on those rows (`ref`: the oracle's routing of
+    exactly those rows, when the caller already has it)."""
     cfg = c.cfg
-    ref = oracle.route(c.x[rows], c.W, c.bias, c.slot_of, cfg.k)
+    if ref is None:
+        ref = oracle.route(c.x[rows], c.W, c.bias, c.slot_of, cfg.k)
     resident = c.slot_of >= 0
     tie_sel = near_tie_tokens(ref["scores"], resident, cfg.k)
     tie_want = near_tie_tokens(ref["scores"], np.ones(cfg.E, bool), cfg.k)
     n_checked = 0
+    n_ranks = 0
     for i, t in enumerate(rows):
         s = ref["scores"][i]
         if not tie_want[i]:
@@ -53,6 +57,13 @@ def check_route(c, g, rows):
         if not tie_sel[i]:
             assert set(g["sel_e"][t]) == set(ref["sel_e"][i]), (t, g["sel_e"][t], ref["sel_e"][i])
             n_checked += 1
+        # ordered: at every rank clear of its neighbours by more than 1e-5 relative, the same expert (and slot)
+        for key_e, mask in (("want_e", np.ones(cfg.E, bool)), ("sel_e", resident)):
+            clear = clear_ranks(s, mask, cfg.k)
+            assert np.array_equal(g[key_e][t][clear], ref[key_e][i][clear]), (t, key_e, g[key_e][t], ref[key_e][i])
+            n_ranks += int(clear.sum())
+        clear = clear_ranks(s, resident, cfg.k)
+        assert np.array_equal(g["sel_slot"][t][clear], ref["sel_slot"][i][clear]), t
         # order: non-increasing oracle score (up to fp32 ties); weights and slots follow the expert
         for key_e, key_w in (("want_e", "want_s"), ("sel_e", "sel_w")):
             es = g[key_e][t]
@@ -67,6 +78,8 @@ def check_route(c, g, rows):
         nres = int(resident.sum())
         assert np.count_nonzero(se >= 0) == min(cfg.k, nres)
     assert n_checked >= len(rows) - max(2, len(rows) // 50)
+    # most ranks are compared in order (only near-equal neighbours are left to the set comparison)
+    assert n_ranks >= 0.8 * len(rows) * (cfg.k + min(cfg.k, int(resident.sum())))
     return ref
 
 
@@ -89,12 +102,58 @@ def test_route_parity(cfg, T):
     check_route(c, g, np.arange(T))
 
 
-def test_route_parity_prefill_sampled():
-    # full prefill batch (8192 tokens, the bench's launch shape); the oracle checks a seeded sample
+def test_route_parity_prefill_full_batch():
+    # the whole 8192-token prefill batch in the bench's launch shape (tensor-core router), every row against
+    # the oracle (run on several host cores)
     c = make_case(synth.PREFILL, 8192)
     g = gpu_route(c)
-    rows = np.sort(synth.seeded_permutation(7, synth.T_SAMPLE, 1, 8192)[:96])
-    check_route(c, g, rows)
+    ref = oracle_pool.route_rows(c.x, c.W, c.bias, c.slot_of, c.cfg.k)
+    check_route(c, g, np.arange(8192), ref)
+
+
+def test_prefill_chunk_demand_and_heavy_misses():
+    """The 8192-token prefill chunk, with the bias drifted after the resident set was fixed so that misses and
+    heavy misses occur: the chunk's demand update over all 8192 tokens within 1e-5 of the oracle's, its miss
+    shares within 1e-5, and its heavy-miss list (share >= 0.2, at most 16) bit-exact against the oracle
+    routing every token (README item 3; the chunk is the unit of one list)."""
+    cfg, T = synth.PREFILL, 8192
+    c = make_case(cfg, T, drift=True)
+    g = gpu_route(c)
+    ref = oracle_pool.route_rows(c.x, c.W, c.bias, c.slot_of, cfg.k)
+    check_route(c, g, np.arange(T), ref)
+    D = torch.zeros((1, cfg.E), dtype=torch.int64, device="cuda")
+    M = torch.zeros((1, cfg.E), dtype=torch.float32, device="cuda")
+    moe.moe_demand_accumulate(to_dev(g["want_e"]), to_dev(g["want_s"]), to_dev(c.slot_of), 0, D, M)
+    Mg = M.clone()
+    flat = torch.full((16,), -7, dtype=torch.int32, device="cuda")
+    share = torch.zeros(16, dtype=torch.float32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_hot_miss_select(M, 0.2, 16, flat, share, n)
+    torch.cuda.synchronize()
+    # the oracle's own picks; tokens at a wanted near-tie (k-th / (k+1)-th within 1e-5) keep the GPU's picks
+    tie = near_tie_tokens(ref["scores"], np.ones(cfg.E, bool), cfg.k)
+    assert tie.sum() <= T // 100
+    want = np.where(tie[:, None], g["want_e"], ref["want_e"])
+    ws = np.take_along_axis(ref["scores"], want.astype(np.int64), axis=1)
+    Dref, Mref = np.zeros((1, cfg.E)), np.zeros((1, cfg.E))
+    oracle.demand(want, ws, c.slot_of, 0, Dref, Mref)
+    adds = np.zeros((1, cfg.E))
+    np.add.at(adds[0], want.ravel(), 1)
+    Dg = D.cpu().numpy().astype(np.float64) / 2.0 ** 40
+    assert np.all(np.abs(Dg - Dref) <= 1e-5 * Dref + adds * 2.0 ** -41 + 1e-15)
+    assert abs(Dg.sum() - ws.sum()) <= 1e-5 * ws.sum()       # demand adds up to the wanted picks' scores
+    Mgn = Mg.cpu().numpy().astype(np.float64)
+    assert np.array_equal(Mgn > 0, Mref > 0) and np.allclose(Mgn, Mref, rtol=1e-5, atol=0)
+    ids_ref, sh_ref = oracle.hot_miss_select(Mref.copy(), 0.2, 16)
+    assert len(ids_ref) > 0                                   # the drifted chunk has heavy misses
+    cand = np.sort(Mref.ravel()[Mref.ravel() >= 0.2])[::-1]
+    assert not (len(cand) > 16 and abs(cand[15] - cand[16]) <= 1e-5 * cand[15])
+    assert not np.any(np.abs(Mref - 0.2) <= 1e-5 * 0.2)
+    nn_ = int(n.item())
+    assert nn_ == len(ids_ref)
+    assert list(flat.cpu().numpy()[:nn_]) == list(ids_ref)
+    assert np.allclose(share.cpu().numpy()[:nn_], sh_ref, rtol=1e-5, atol=0)
+    assert not M.any()                                        # shares reset for the next chunk
 
 
 def test_route_drifted_has_substitutions():
@@ -204,10 +263,13 @@ def gpu_ffn(c, arena, sel_slot, sel_w):
     return out.cpu().numpy().astype(np.float64)
 
 
+# sample: None = every token row; "cover" = rows that together route to every slot the batch uses (the last
+# token of each slot, so the last tile of each slot is read too) plus a few seeded rows
 FFN_CASES = [(synth.TINY, 8, None), (RAGGED, 37, None), (SPARSE, 5, None), (synth.DECODE, 1, None),
-             (synth.DECODE, 8, None), (synth.DECODE, 64, 6), (synth.GLM, 16, 4), (synth.PREFILL, 8192, 3),
+             (synth.DECODE, 8, None), (synth.DECODE, 64, None), (synth.GLM, 16, None), (synth.GLM, 64, None),
+             (synth.PREFILL, 8192, "cover"),
              # batches above 64 tokens: 128-row tiles, token-major gate/up, then down rows and the ordered combine
-             (synth.TINY, 80, None), (RAGGED, 100, None), (synth.DECODE, 200, 4),
+             (synth.TINY, 80, None), (RAGGED, 100, None), (synth.DECODE, 200, "cover"),
              # 8192 picks and more: the plan runs in several CTAs
              (synth.TINY, 2048, None), (RAGGED, 2731, None),
              # at most 32 picks: the one-warp plan (x packed in the same launch when it is small);
@@ -221,15 +283,22 @@ def test_ffn_parity(cfg, T, sample):
     c = make_case(cfg, T)
     arena = device_arena(cfg, c.owner, c.n_slots)
     ref_route = oracle.route(c.x, c.W, c.bias, c.slot_of, cfg.k) if T <= 64 or cfg.d <= 512 else None
-    if ref_route is None:            # prefill: the GPU router's picks (checked by the route tests)
+    if ref_route is None:            # large batches: the GPU router's picks (checked by the route tests)
         g = gpu_route(c)
         sel_slot, sel_w = g["sel_slot"], g["sel_w"].astype(np.float64)
     else:
         sel_slot, sel_w = ref_route["sel_slot"], ref_route["sel_w"]
     got = gpu_ffn(c, arena, sel_slot, sel_w.astype(np.float32))
-    rows = np.arange(T) if sample is None else np.sort(synth.seeded_permutation(11, synth.T_SAMPLE, T, T)[:sample])
-    sel_u, experts = oracle_experts(cfg, c.owner, sel_slot[rows])
-    ref = oracle.ffn(c.x[rows], sel_u, sel_w[rows].astype(np.float32).astype(np.float64), experts, cfg.d, cfg.ffn)
+    rows = np.arange(T) if sample is None else covering_rows(sel_slot)
+    if sample == "cover":            # every used slot is checked
+        used = np.unique(sel_slot[sel_slot >= 0])
+        assert np.array_equal(np.unique(sel_slot[rows][sel_slot[rows] >= 0]), used)
+    w32 = sel_w[rows].astype(np.float32).astype(np.float64)
+    if cfg.d >= 1024 and len(rows) > 2:          # big experts: token groups on several host cores
+        ref = oracle_pool.ffn(cfg, c.x[rows], sel_slot[rows], w32, c.owner)
+    else:
+        sel_u, experts = oracle_experts(cfg, c.owner, sel_slot[rows])
+        ref = oracle.ffn(c.x[rows], sel_u, w32, experts, cfg.d, cfg.ffn)
     ok, fro, mx = ffn_within_tolerance(got[rows], ref)
     assert ok, (fro, mx, np.abs(ref).max())
     # tokens whose picks are all padding get exact zeros
