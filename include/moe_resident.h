@@ -384,6 +384,35 @@ moe_status moe_demand_load(uint64_t* demand, int L, int E, const char* path, voi
  */
 moe_status moe_device_status(void* stream, uint32_t* bits);
 
+/*
+ * Bound on every wait inside the library's pipelined kernels (the expert
+ * FFN's GEMMs and the tensor-core router), in nanoseconds of wall-clock time
+ * counted from the wait's first failed try; ns = 0 restores the default, 2 s.
+ * A healthy wait ends in microseconds; the bound exists so that a broken
+ * pipeline cannot hang the GPU (failure detection in the spirit of the
+ * colibri cluster page, "timeouts": every wait of that cluster is bounded and
+ * ends in an error rather than a stall). When a wait
+ * runs out, its CTA stops issuing work, waits (at most 0.2 s more) for the
+ * bulk copies and tensor-core operations it has already issued, frees its
+ * tensor memory and exits; MOE_DEV_TIMEOUT is set in the device error word
+ * (moe_device_status then returns MOE_ETIMEOUT) and that call's outputs are
+ * not valid. Later calls are unaffected. Process-wide; read when a call
+ * launches its kernels, so a CUDA graph keeps the value it was captured with.
+ */
+moe_status moe_set_wait_limit(uint64_t ns);
+uint64_t   moe_get_wait_limit(void);
+
+/*
+ * Failure-detection check of the bounded waits: launches one CTA set up like
+ * the pipelined kernels (tensor memory allocated, an MMA thread, warps waiting
+ * on an mbarrier) whose wait can never be satisfied -- nothing arrives on its
+ * barrier. It gives up after the bound in force (moe_set_wait_limit), drains,
+ * frees its tensor memory and sets MOE_DEV_TIMEOUT, as a stalled pipeline
+ * would; moe_device_status then returns MOE_ETIMEOUT. Takes that long to end:
+ * set a short bound first (e.g. 1 ms) and restore it afterwards.
+ */
+moe_status moe_wait_selftest(void* stream);
+
 /* Static English text for a status code. */
 const char* moe_status_str(moe_status s);
 

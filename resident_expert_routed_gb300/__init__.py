@@ -32,7 +32,8 @@ EXPORTS = ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accum
            "moe_device_status", "moe_status_str", "moe_kernel_launches", "moe_profile_enable",
            "moe_profile_kernel_count", "moe_profile_read", "moe_profile_reset", "moe_demand_decay",
            "moe_demand_save", "moe_demand_load", "moe_hot_ring_create", "moe_hot_ring_step", "moe_hot_ring_destroy",
-           "moe_hot_read_sync", "moe_renormalise_weights", "moe_expert_ffn_prefetch")
+           "moe_hot_read_sync", "moe_renormalise_weights", "moe_expert_ffn_prefetch", "moe_set_wait_limit",
+           "moe_get_wait_limit", "moe_wait_selftest")
 
 
 class MoeError(RuntimeError):
@@ -94,12 +95,16 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.moe_hot_read_sync.argtypes = [_P, _P, _P, _P, _P, ctypes.POINTER(MoeArena), _I, _I, _I, _F, _P, _P, _P]
     L.moe_demand_save.argtypes = [_P, _I, _I, ctypes.c_char_p, _P]
     L.moe_demand_load.argtypes = [_P, _I, _I, ctypes.c_char_p, _P]
+    L.moe_set_wait_limit.argtypes = [ctypes.c_uint64]
+    L.moe_get_wait_limit.restype = ctypes.c_uint64
+    L.moe_get_wait_limit.argtypes = []
+    L.moe_wait_selftest.argtypes = [_P]
     for name in ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accumulate", "moe_hot_miss_select",
                  "moe_expert_ffn_mxfp4",
                  "moe_arena_replan", "moe_ring_install", "moe_device_status", "moe_profile_enable",
                  "moe_profile_read", "moe_demand_decay", "moe_demand_save", "moe_demand_load", "moe_hot_ring_create",
                  "moe_hot_ring_step", "moe_hot_ring_destroy", "moe_hot_read_sync", "moe_renormalise_weights",
-                 "moe_expert_ffn_prefetch"):
+                 "moe_expert_ffn_prefetch", "moe_set_wait_limit", "moe_wait_selftest"):
         L[name].restype = _I
     _lib = L
     return L
@@ -220,6 +225,20 @@ def moe_device_status(stream=None) -> tuple[int, int]:
     bits = ctypes.c_uint32(0)
     st = load().moe_device_status(_stream(stream), ctypes.byref(bits))
     return st, bits.value
+
+
+def moe_set_wait_limit(ns: int) -> None:
+    """Bound (wall-clock ns) on every wait of the pipelined kernels launched from now on; 0 = the default 2 s."""
+    _check("moe_set_wait_limit", load().moe_set_wait_limit(int(ns)))
+
+
+def moe_get_wait_limit() -> int:
+    return int(load().moe_get_wait_limit())
+
+
+def moe_wait_selftest(stream=None) -> None:
+    """Launch the stalled-wait check (see the header); afterwards moe_device_status reports MOE_ETIMEOUT."""
+    _check("moe_wait_selftest", load().moe_wait_selftest(_stream(stream)))
 
 
 def moe_kernel_launches() -> int:

@@ -20,6 +20,7 @@ size_t replan_workspace(int n);
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_wait_limit_ns{MOE_WAIT_LIMIT_NS};
 
 // One error word per device; its device address is looked up once per device.
 __device__ uint32_t g_err_word;
@@ -189,6 +190,8 @@ static void prof_drain() {   // caller holds g_prof_mu
 
 void moe_count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+uint64_t moe_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 int moe_sm_count() {
     const int dev = current_device();
     if (dev < 0) return 148;
@@ -217,6 +220,19 @@ const char* moe_status_str(moe_status s) {
 }
 
 uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status moe_set_wait_limit(uint64_t ns) {
+    g_wait_limit_ns.store(ns == 0 ? MOE_WAIT_LIMIT_NS : ns, std::memory_order_relaxed);
+    return MOE_OK;
+}
+
+uint64_t moe_get_wait_limit(void) { return moe_wait_limit_ns(); }
+
+moe_status moe_wait_selftest(void* stream) {
+    uint32_t* err = err_word();
+    if (!err) return MOE_ECUDA;
+    return cuda_status(launch_wait_selftest(err, moe_wait_limit_ns(), static_cast<cudaStream_t>(stream)));
+}
 
 moe_status moe_profile_enable(int on) {
     g_prof_on.store(on != 0);
@@ -287,6 +303,7 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
     a.partial = static_cast<float*>(workspace);
     a.err = err_word();
     if (!a.err) return MOE_ECUDA;
+    a.wait_ns = moe_wait_limit_ns();
     if (hk == 0 && router_rows_eligible(T, d)) {      // few tokens: whole rows, no K slices
         a.rows = 1;
         a.splits = 1;
@@ -383,6 +400,7 @@ moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot
     a.work_max = c.work_max;
     a.pad_max = c.pad_max;
     a.err = err;
+    a.wait_ns = moe_wait_limit_ns();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_ffn_plan(a, s);
     if (e == cudaSuccess) e = launch_ffn_gemms(a, s, nullptr);

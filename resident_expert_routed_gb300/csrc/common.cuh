@@ -16,10 +16,15 @@
 
 #define MOE_DEV __device__ __forceinline__
 
-// Wall-clock bound on any spin-wait inside a kernel (ns). A healthy wait ends
-// in microseconds; this only exists so that a broken pipeline returns with
-// MOE_DEV_TIMEOUT instead of hanging the GPU.
+// Default wall-clock bound on any spin-wait inside a kernel (ns); the host
+// passes the bound in force (moe_set_wait_limit) to every pipelined kernel. A
+// healthy wait ends in microseconds; the bound only exists so that a broken
+// pipeline returns with MOE_DEV_TIMEOUT instead of hanging the GPU.
 #define MOE_WAIT_LIMIT_NS 2000000000ull
+// After a wait has run out, a kernel still waits for the bulk copies and
+// tensor-core operations it has already issued (they complete on their own)
+// before it frees its tensor memory and exits; those waits use this bound.
+#define MOE_DRAIN_LIMIT_NS 200000000ull
 
 // ------------------------------------------------------------------ basic
 
@@ -110,6 +115,14 @@ MOE_DEV unsigned long long block_inclusive_scan_u64(unsigned long long v, unsign
     return v;
 }
 
+// 1 if any of the 16 bytes is 0xFF (an e8m0 scale byte that encodes NaN), else 0: a byte of w is 0xFF
+// exactly when that byte of ~w is zero, and (z - 0x01..01) & ~z & 0x80..80 is non-zero exactly when z has a
+// zero byte.
+MOE_DEV uint32_t has_ff_byte(const uint4& v) {
+    auto one = [](uint32_t w) { return ((~w) - 0x01010101u) & w & 0x80808080u; };
+    return (one(v.x) | one(v.y) | one(v.z) | one(v.w)) != 0u ? 1u : 0u;
+}
+
 MOE_DEV void record_error(uint32_t* err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }
@@ -142,18 +155,17 @@ MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity. Returns false (after
-// raising the CTA's abort flag) when the wall-clock limit passes or another
-// role of the CTA has already aborted.
-MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    uint64_t t0 = 0;
-    for (uint32_t it = 0;; ++it) {
+// raising the CTA's abort flag) when `limit_ns` of wall-clock time pass or
+// another role of the CTA has already aborted. The clock starts at the first
+// failed try and is read every 16 tries.
+MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 255u) {
+        if ((it & 15u) == 0u) {
             if (*abort_flag) return false;
-            uint64_t now = global_timer_ns();
-            if (t0 == 0) {
-                t0 = now;
-            } else if (now - t0 > MOE_WAIT_LIMIT_NS) {
+            if (global_timer_ns() - t0 >= limit_ns) {
                 *abort_flag = 1;
                 return false;
             }
@@ -163,9 +175,34 @@ MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
 
 // The same wait for all 32 lanes of a warp; the outcome is made warp-uniform
 // so that a time-out can never split a warp across different sync points.
-MOE_DEV bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    const bool ok = mbar_wait(bar, parity, abort_flag);
+MOE_DEV bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, limit_ns);
     return __all_sync(0xFFFFFFFFu, ok) != 0;
+}
+
+// Wait for an operation this thread issued itself (a bulk copy's bytes, a
+// tcgen05.commit) after an abort: ignores the abort flag, bounded by
+// MOE_DRAIN_LIMIT_NS.
+MOE_DEV bool mbar_drain(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 0u && global_timer_ns() - t0 >= MOE_DRAIN_LIMIT_NS) return false;
+    }
+}
+
+// A producer that has issued `issued` stage fills (fill i into stage i % ns,
+// each completing one phase of full[i % ns]) and stops early: wait until the
+// bytes of the last fill of every stage have landed. Earlier fills of a stage
+// have completed already (the producer waited for their stage to be consumed
+// before refilling it).
+MOE_DEV void drain_stage_fills(uint64_t* full, int ns, uint32_t issued) {
+    for (int s = 0; s < ns; ++s) {
+        if (issued <= (uint32_t)s) break;
+        const uint32_t last = (uint32_t)s + (uint32_t)ns * ((issued - 1u - (uint32_t)s) / (uint32_t)ns);
+        (void)mbar_drain(&full[s], (last / (uint32_t)ns) & 1u);
+    }
 }
 
 MOE_DEV void fence_barrier_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
@@ -214,6 +251,13 @@ MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;"
 MOE_DEV void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+
+// After an abort: wait (bounded) until every tcgen05 operation this thread
+// has issued has completed. `bar` is an mbarrier of count 1 used only for this.
+MOE_DEV void tc_drain(uint64_t* bar) {
+    tc_commit(bar);
+    (void)mbar_drain(bar, 0);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, e2m1 x e2m1 with e8m0 block-32 scales from TMEM.
@@ -275,6 +319,7 @@ struct RouteLaunch {
     float* partial;
     void* wsplit;           // non-null: tensor-core router, W split into three bf16 parts here
     uint32_t* err;          // device error word (tensor-core router's bounded waits)
+    uint64_t wait_ns;       // bound on each wait of the tensor-core router
     int rows;               // 1: one CTA per expert row (few tokens in device memory; splits = 1)
 };
 bool router_rows_eligible(int T, int d);
@@ -286,7 +331,7 @@ int pointer_kind(const void* p);      // 0 device, 1 page-locked host, -1 pageab
 int router_tc_splits(int T, int E, int d);
 size_t router_tc_split_bytes(int E, int d);
 cudaError_t launch_router_tc(const uint16_t* x, const float* W, int T, int d, int E, int splits, void* wsplit,
-                             float* partial, uint32_t* err, cudaStream_t s);
+                             float* partial, uint32_t* err, uint64_t wait_ns, cudaStream_t s);
 cudaError_t launch_route(const RouteLaunch& a, cudaStream_t s);
 int route_splits(int T, int E, int d);
 
@@ -316,11 +361,13 @@ struct FfnLaunch {
     int plan_ctas;          // 0: one-CTA plan
     int work_max, pad_max;
     uint32_t* err;
+    uint64_t wait_ns;       // bound on each wait of the GEMM pipelines
 };
 cudaError_t launch_ffn_plan(const FfnLaunch& a, cudaStream_t s);
 cudaError_t launch_ffn_prefetch(const int32_t* sel_slot, int P, const moe_arena& ar, cudaStream_t s);
 cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches);
 cudaError_t launch_ffn_combine(const FfnLaunch& a, cudaStream_t s);
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t wait_ns, cudaStream_t s);
 
 cudaError_t launch_replan(const unsigned long long* demand, int n, int n_main, int n_slots, int32_t* slot_of,
                           int32_t* owner, int32_t* loads, int32_t* n_loads, void* ws, cudaStream_t s,
@@ -355,6 +402,9 @@ cudaError_t moe_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // The device error word of the current device (abi.cu); null if it cannot be found.
 uint32_t* moe_err_word();
+
+// The bound on every wait of the pipelined kernels now in force (moe_set_wait_limit; abi.cu).
+uint64_t moe_wait_limit_ns();
 
 // Kernel launch counter kept by abi.cu.
 void moe_count_launches(int n);

@@ -32,9 +32,11 @@
 //   warps 0-3  epilogue: tcgen05.ld of their 32-lane quadrant of the
 //              (double-buffered) accumulators, then the per-mode epilogue.
 // The grid is persistent (one CTA per SM) over the flattened (tile, 128-row
-// weight block) items. Every wait is bounded (MOE_WAIT_LIMIT_NS); on expiry
-// the CTA raises its abort flag, every role leaves its loop, TMEM is freed and
-// the device error word gets MOE_DEV_TIMEOUT.
+// weight block) items. Every wait is bounded (the host's moe_set_wait_limit,
+// 2 s by default); on expiry the CTA raises its abort flag, every role leaves
+// its loop, the producer waits for the bytes of the copies it has issued and
+// the MMA thread for its MMAs, TMEM is freed and the device error word gets
+// MOE_DEV_TIMEOUT.
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -64,6 +66,7 @@ struct GemmArgs {
     uint8_t* hsp;                // gate/up output: down activation scale atoms
     float* Y;                    // down output [T*k, d] (per-pick rows)
     uint32_t* err;
+    uint64_t wait_ns;            // bound on each pipeline wait
 };
 
 // Scale factors reach TMEM through registers, not tcgen05.cp: the copy that
@@ -77,7 +80,8 @@ struct GemmArgs {
 // (zeros past the end of K).
 template <int NV, int PF, int NS, typename Load>
 __device__ __forceinline__ void scale_writer(int n_stages, const Load& load, uint64_t* empty, uint64_t* sfull,
-                                             uint32_t sf_base, int sf_cols, volatile int* abort_flag) {
+                                             uint32_t sf_base, int sf_cols, volatile int* abort_flag,
+                                             uint64_t wait_ns) {
     static_assert(NV % 2 == 0, "atoms are written in pairs");
     const int lane = threadIdx.x & 31;
     uint4 v[PF][NV];
@@ -91,7 +95,7 @@ __device__ __forceinline__ void scale_writer(int n_stages, const Load& load, uin
             if (g >= n_stages) break;
             const int s = g % NS;
             const uint32_t r = (uint32_t)(g / NS);
-            if (!warp_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
+            if (!warp_wait(&empty[s], (r & 1) ^ 1, abort_flag, wait_ns)) { ok_run = false; break; }
             tc_fence_after();
             const uint32_t sfc = sf_base + s * sf_cols;
 #pragma unroll
@@ -127,7 +131,7 @@ struct Cfg {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + NS * A_BYTES;
     static constexpr int OFF_BAR = OFF_B + NS * B_BYTES;
-    static constexpr int N_BARS = 3 * NS + 2 * NBUF;
+    static constexpr int N_BARS = 3 * NS + 2 * NBUF + 1;   // full, empty, sfull per stage; accf, acce; drain
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
     static constexpr int TMEM_USED = NBUF * ACC_COLS + SF_COLS * NS;
@@ -150,6 +154,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     uint64_t* sfull = empty + NS;
     uint64_t* accf = sfull + NS;
     uint64_t* acce = accf + NBUF;
+    uint64_t* drain = acce + NBUF;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -158,6 +163,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sfull[s], 4); }
         for (int b = 0; b < NBUF; ++b) { mbar_init(&accf[b], 1); mbar_init(&acce[b], 4); }
+        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
         for (int i = 0; i < 4; ++i) prefetch_tmap(&maps.b[i]);
@@ -168,6 +174,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    uint32_t issued = 0;                             // stage fills issued by the producer thread
     pdl_wait();                                      // the work list is the plan kernel's output
     const int n_items = *a.n_work * a.m_tiles;
     const int nc = (a.K + 255) / 256;                 // 256-element chunks along K
@@ -177,7 +184,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     if (warp == 4) {
         // ------------------------------------------------------------ TMA producer (one thread)
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t& it = issued;
             bool ok_run = true;
             int4 w_next = blockIdx.x < n_items ? a.work[blockIdx.x / a.m_tiles] : make_int4(0, 0, 0, 0);
             for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x) {
@@ -196,7 +203,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                 for (int st = 0; st < nst; ++st, ++it) {
                     const int s = (int)(it % NS);
                     const uint32_t r = it / NS;
-                    if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
+                    if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, a.wait_ns)) { ok_run = false; break; }
                     uint8_t* As = smem + C::OFF_A + s * C::A_BYTES;
                     uint8_t* Bs = smem + C::OFF_B + s * C::B_BYTES;
                     const int c0 = st * KCH;
@@ -233,11 +240,11 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                 const uint32_t id0 = idesc_mxf4(N, 0, 0), id1 = idesc_mxf4(N, 2, 2);
                 const int b = (int)(j % NBUF);
                 const uint32_t u = j / NBUF;
-                if (!mbar_wait(&acce[b], (u & 1) ^ 1, abort_flag)) break;
+                if (!mbar_wait(&acce[b], (u & 1) ^ 1, abort_flag, a.wait_ns)) break;
                 tc_fence_after();
                 const uint32_t dt = tmem + b * C::ACC_COLS;
                 for (int st = 0; st < nst; ++st) {
-                    if (!mbar_wait(&full[s], ph, abort_flag) || !mbar_wait(&sfull[s], ph, abort_flag)) {
+                    if (!mbar_wait(&full[s], ph, abort_flag, a.wait_ns) || !mbar_wait(&sfull[s], ph, abort_flag, a.wait_ns)) {
                         ok_run = false;
                         break;
                     }
@@ -279,6 +286,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     } else if (warp >= 6) {
         // ------------------------------------------------------------ scale factors -> TMEM
         const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        uint32_t nan_seen = 0;                            // an e8m0 weight scale byte 0xFF (NaN) was loaded
         auto load = [&](int g, uint4 (&v)[C::NV]) {
 #pragma unroll
             for (int q = 0; q < C::NV; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
@@ -299,13 +307,16 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             for (int m = 0; m <= C::NMAT; ++m)
 #pragma unroll
                 for (int q = 0; q < 2 * KCH; ++q)
-                    if (q < ats)
+                    if (q < ats) {
                         v[m * 2 * KCH + q] =
                             *reinterpret_cast<const uint4*>(src[m] + (size_t)(at0 + q) * 512 + lane * 16);
+                        if (m < C::NMAT) nan_seen |= has_ff_byte(v[m * 2 * KCH + q]);
+                    }
         };
         scale_writer<C::NV, C::PF, NS>(my_items * nst, load, empty, sfull,
                                        tmem + ((uint32_t)((warp & 3) * 32) << 16) + NBUF * C::ACC_COLS, C::SF_COLS,
-                                       abort_flag);
+                                       abort_flag, a.wait_ns);
+        if (__any_sync(0xFFFFFFFFu, nan_seen) && lane == 0 && warp == 6) record_error(a.err, MOE_DEV_NAN_SCALE);
     } else {
         // ------------------------------------------------------------ epilogue (warps 0..3)
         uint32_t j = 0;
@@ -325,7 +336,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     pp[q] = col < nv ? a.pair_of_pos[pos0 + col] : 0;
                 }
             }
-            if (!warp_wait(&accf[b], u & 1, abort_flag)) break;
+            if (!warp_wait(&accf[b], u & 1, abort_flag, a.wait_ns)) break;
             tc_fence_after();
             const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16) + b * C::ACC_COLS;
             if (MODE == 1) {
@@ -383,6 +394,12 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
 
     tc_fence_before();
     __syncthreads();
+    if (*abort_flag) {               // final after the barrier: nothing new is issued past it
+        if (warp == 4 && lane == 0) drain_stage_fills(full, NS, issued);
+        if (warp == 5 && lane == 0) tc_drain(drain);
+        tc_fence_before();
+        __syncthreads();
+    }
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
@@ -417,7 +434,7 @@ struct CfgTok {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + NS * A_BYTES;
     static constexpr int OFF_BAR = OFF_B + NS * B_BYTES;
-    static constexpr int N_BARS = 3 * NS + 2;
+    static constexpr int N_BARS = 3 * NS + 3;           // full, empty, sfull per stage; accf, acce, drain
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;
     static constexpr int TMEM_USED = 256 + SF_COLS * NS;
@@ -439,6 +456,7 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
     uint64_t* sfull = empty + NS;
     uint64_t* accf = sfull + NS;
     uint64_t* acce = accf + 1;
+    uint64_t* drain = acce + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -448,6 +466,7 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
         for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sfull[s], 4); }
         mbar_init(accf, 1);
         mbar_init(acce, 8);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&maps.b[3]);
@@ -458,6 +477,7 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    uint32_t issued = 0;                             // stage fills issued by the producer thread
     pdl_wait();                                      // the work list is the plan kernel's output
     const int n_items = *a.n_work * a.m_tiles;
     const int nc = (a.K + 255) / 256;
@@ -466,7 +486,7 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
     if (warp == 4) {
         // ------------------------------------------------------------ TMA producer (one thread)
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t& it = issued;
             bool ok_run = true;
             int4 w_next = blockIdx.x < n_items ? a.work[blockIdx.x / a.m_tiles] : make_int4(0, 0, 0, 0);
             for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x) {
@@ -481,7 +501,7 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
                 for (int kc = 0; kc < nc; ++kc, ++it) {
                     const int s = (int)(it % NS);
                     const uint32_t r = it / NS;
-                    if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) { ok_run = false; break; }
+                    if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, a.wait_ns)) { ok_run = false; break; }
                     uint8_t* As = smem + C::OFF_A + s * C::A_BYTES;
                     uint8_t* Bs = smem + C::OFF_B + s * C::B_BYTES;
                     mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
@@ -502,10 +522,10 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
             const uint64_t b_base = smem_desc_sw128(smem_u32(smem + C::OFF_B));
             constexpr uint32_t id0 = idesc_mxf4(256, 0, 0), id1 = idesc_mxf4(256, 2, 2);
             for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x, ++j) {
-                if (!mbar_wait(acce, (j & 1) ^ 1, abort_flag)) break;
+                if (!mbar_wait(acce, (j & 1) ^ 1, abort_flag, a.wait_ns)) break;
                 tc_fence_after();
                 for (int kc = 0; kc < nc; ++kc) {
-                    if (!mbar_wait(&full[s], ph, abort_flag) || !mbar_wait(&sfull[s], ph, abort_flag)) {
+                    if (!mbar_wait(&full[s], ph, abort_flag, a.wait_ns) || !mbar_wait(&sfull[s], ph, abort_flag, a.wait_ns)) {
                         ok_run = false;
                         break;
                     }
@@ -536,6 +556,7 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
         // stage g of this CTA is K chunk g % nc of its item g / nc; atoms in column
         // order: activations q = 0, 1, then (gate, up) per q
         const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        uint32_t nan_seen = 0;                            // an e8m0 weight scale byte 0xFF (NaN) was loaded
         auto load = [&](int g, uint4 (&v)[6]) {
 #pragma unroll
             for (int q = 0; q < 6; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
@@ -556,10 +577,13 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
                 v[q] = *reinterpret_cast<const uint4*>(sa + o);
                 v[2 + 2 * q] = *reinterpret_cast<const uint4*>(sg + o);
                 v[3 + 2 * q] = *reinterpret_cast<const uint4*>(su + o);
+                nan_seen |= has_ff_byte(v[2 + 2 * q]) | has_ff_byte(v[3 + 2 * q]);
             }
         };
         scale_writer<6, C::PF, NS>(my_items * nc, load, empty, sfull,
-                                   tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256, C::SF_COLS, abort_flag);
+                                   tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256, C::SF_COLS, abort_flag,
+                                   a.wait_ns);
+        if (__any_sync(0xFFFFFFFFu, nan_seen) && lane == 0 && warp == 6) record_error(a.err, MOE_DEV_NAN_SCALE);
     } else {
         // ------------------------------------------------------------ epilogue: lane = routed row
         uint32_t j = 0;
@@ -567,7 +591,7 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
             const int4 w = a.work[item / a.m_tiles];
             const int mt = item % a.m_tiles;
             const int pos0 = w.y, nv = w.z;
-            if (!warp_wait(accf, j & 1, abort_flag)) break;
+            if (!warp_wait(accf, j & 1, abort_flag, a.wait_ns)) break;
             tc_fence_after();
             const int quad = warp & 3;                              // TMEM lane quadrant of this warp
             const int row = quad * 32 + lane;
@@ -616,11 +640,59 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
 
     tc_fence_before();
     __syncthreads();
+    if (*abort_flag) {               // final after the barrier: nothing new is issued past it
+        if (warp == 4 && lane == 0) drain_stage_fills(full, NS, issued);
+        if (warp == 5 && lane == 0) tc_drain(drain);
+        tc_fence_before();
+        __syncthreads();
+    }
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
     if (threadIdx.x == 0 && *abort_flag) record_error(a.err, MOE_DEV_TIMEOUT);
+}
+
+// A CTA shaped like the pipelines above (TMEM allocated by warp 5, an MMA
+// thread that has committed work, warps waiting on an mbarrier) whose wait can
+// never be satisfied: nothing arrives on `never`. Every wait gives up after
+// the bound in force and the CTA takes the same exit as a stalled pipeline
+// (drain, free TMEM, MOE_DEV_TIMEOUT), so a caller can check that a stall ends
+// in an error status instead of a hang.
+__global__ void __launch_bounds__(128, 1) wait_selftest(uint32_t* err, uint64_t wait_ns) {
+    __shared__ uint64_t bars[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_word;
+    uint64_t* never = &bars[0];
+    uint64_t* drain = &bars[1];
+    volatile int* abort_flag = &abort_word;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+        mbar_init(never, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) { tmem_alloc(&tmem_slot, 32); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_wait();
+    const uint32_t tmem = tmem_slot;
+    (void)warp_wait(never, 0, abort_flag, wait_ns);
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) {
+        if (warp == 1 && lane == 0) tc_drain(drain);
+        tc_fence_before();
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 32);
+    }
+    if (threadIdx.x == 0 && *abort_flag) record_error(err, MOE_DEV_TIMEOUT);
 }
 
 // ------------------------------------------------------------------ host side
@@ -736,6 +808,11 @@ cudaError_t launch_mode(const GemmMaps& maps, const GemmArgs& g, long max_items,
 
 }  // namespace
 
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t wait_ns, cudaStream_t s) {
+    moe_count_launches(1);
+    return moe_launch(wait_selftest, dim3(1), dim3(128), 0, s, err, wait_ns);
+}
+
 cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches) {
     const moe_arena& ar = *a.arena;
     const uint8_t* base = static_cast<const uint8_t*>(ar.base);
@@ -753,6 +830,7 @@ cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches
     g.n_work = a.n_work;
     g.pair_of_pos = a.pair_of_pos;
     g.err = a.err;
+    g.wait_ns = a.wait_ns;
 
     GemmArgs g1 = g;       // gate/up + SwiGLU
     g1.off_codes = ar.off_gu_codes;

@@ -411,7 +411,7 @@ int route_splits(int T, int E, int d) {
 cudaError_t launch_route(const RouteLaunch& a, cudaStream_t s) {
     cudaError_t e;
     if (a.wsplit) {
-        e = launch_router_tc(a.x, a.w, a.T, a.d, a.E, a.splits, a.wsplit, a.partial, a.err, s);
+        e = launch_router_tc(a.x, a.w, a.T, a.d, a.E, a.splits, a.wsplit, a.partial, a.err, a.wait_ns, s);
     } else if (a.rows) {
         moe_prof_begin(MK_ROUTER_LOGITS, s);
         e = moe_launch(router_logits_rows, dim3(a.E), dim3(ROWS_THREADS), 0, s, a.x, a.w, a.T, a.d, a.E, a.partial);
@@ -536,5 +536,6 @@ extern "C" moe_status moe_route_resident_noalloc(const void* hidden_bf16, const 
     if (hk == 0 && router_rows_eligible(T, d)) { a.rows = 1; a.splits = 1; }
     a.want_e = want_e; a.want_s = want_s; a.sel_e = sel_e; a.sel_slot = sel_slot; a.sel_w = sel_w;
     a.partial = partials;      // every element read below is written earlier in the same call
+    a.wait_ns = moe_wait_limit_ns();
     return launch_route(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }

@@ -40,7 +40,7 @@ constexpr int RT_NS = 3;
 constexpr int RT_TILE = 128 * 128;                 // 128 rows x 64 bf16 (128 bytes)
 constexpr int RT_STAGE = 4 * RT_TILE;              // x tile + three W tiles
 constexpr int RT_EPOCH = 2;                         // K chunks (24 MMAs) per accumulator epoch
-constexpr int RT_SMEM = RT_NS * RT_STAGE + (2 * RT_NS + 4) * 8 + 16 + 1024;
+constexpr int RT_SMEM = RT_NS * RT_STAGE + (2 * RT_NS + 5) * 8 + 16 + 1024;   // stages, barriers, TMEM slot + flag
 
 __global__ void __launch_bounds__(256) split_router_weights(const float* __restrict__ W, long n,
                                                             __nv_bfloat16* __restrict__ w1, __nv_bfloat16* __restrict__ w2,
@@ -80,14 +80,15 @@ struct RouterMaps {
 
 __global__ void __launch_bounds__(192, 1) router_logits_tc(const __grid_constant__ RouterMaps maps, int T, int E,
                                                            int kchunks, float* __restrict__ partial,
-                                                           uint32_t* err) {
+                                                           uint32_t* err, uint64_t wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + RT_NS * RT_STAGE);
     uint64_t* empty = full + RT_NS;
     uint64_t* acc_full = empty + RT_NS;      // [2] accumulator b holds a finished epoch
     uint64_t* acc_empty = acc_full + 2;      // [2] accumulator b has been drained
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    uint64_t* drain = acc_empty + 2;         // the MMA thread's own MMAs, after an abort
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * 128, e0 = blockIdx.y * 128, z = blockIdx.z;
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc(const __grid_constant
     if (threadIdx.x == 0) {
         for (int s = 0; s < RT_NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 128); }
+        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&maps.x);
@@ -108,13 +110,15 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc(const __grid_constant
     const uint32_t tmem = *tmem_slot;
     const int kc0 = z * kchunks;
     const int n_epochs = (kchunks + RT_EPOCH - 1) / RT_EPOCH;
+    uint32_t issued = 0;                     // stage fills issued by the producer thread
 
     if (warp == 4) {
         if (lane == 0) {
             for (int c = 0; c < kchunks; ++c) {
                 const int s = c % RT_NS;
                 const uint32_t r = c / RT_NS;
-                if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) break;
+                if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, wait_ns)) break;
+                ++issued;
                 uint8_t* st = smem + s * RT_STAGE;
                 const int x0 = (kc0 + c) * 64;
                 mbar_arrive_expect_tx(&full[s], RT_STAGE);
@@ -129,8 +133,8 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc(const __grid_constant
                 const uint32_t r = c / RT_NS;
                 const int ep = c / RT_EPOCH, b = ep & 1;
                 const bool first = c % RT_EPOCH == 0;
-                if (first && !mbar_wait(&acc_empty[b], ((ep >> 1) & 1) ^ 1, abort_flag)) break;
-                if (!mbar_wait(&full[s], r & 1, abort_flag)) break;
+                if (first && !mbar_wait(&acc_empty[b], ((ep >> 1) & 1) ^ 1, abort_flag, wait_ns)) break;
+                if (!mbar_wait(&full[s], r & 1, abort_flag, wait_ns)) break;
                 tc_fence_after();
                 const uint32_t st = smem_u32(smem + s * RT_STAGE);
                 const uint32_t d = tmem + (uint32_t)(b * 128);
@@ -151,7 +155,7 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc(const __grid_constant
         bool ok = true;
         for (int ep = 0; ep < n_epochs; ++ep) {
             const int b = ep & 1;
-            if (!warp_wait(&acc_full[b], (ep >> 1) & 1, abort_flag)) { ok = false; break; }
+            if (!warp_wait(&acc_full[b], (ep >> 1) & 1, abort_flag, wait_ns)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -184,6 +188,12 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc(const __grid_constant
     }
     tc_fence_before();
     __syncthreads();
+    if (*abort_flag) {                       // final after the barrier: nothing new is issued past it
+        if (warp == 4 && lane == 0) drain_stage_fills(full, RT_NS, issued);
+        if (warp == 5 && lane == 0) tc_drain(drain);
+        tc_fence_before();
+        __syncthreads();
+    }
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
@@ -230,7 +240,7 @@ int router_tc_splits(int T, int E, int d) {
 size_t router_tc_split_bytes(int E, int d) { return ((size_t)3 * E * d * 2 + 255) / 256 * 256; }
 
 cudaError_t launch_router_tc(const uint16_t* x, const float* W, int T, int d, int E, int splits, void* wsplit,
-                             float* partial, uint32_t* err, cudaStream_t s) {
+                             float* partial, uint32_t* err, uint64_t wait_ns, cudaStream_t s) {
     __nv_bfloat16* w1 = static_cast<__nv_bfloat16*>(wsplit);
     const long n = (long)E * d;
     long blocks = (n + 255) / 256;
@@ -252,7 +262,7 @@ cudaError_t launch_router_tc(const uint16_t* x, const float* W, int T, int d, in
         attr_set[dev] = true;
     }
     dim3 grid((T + 127) / 128, (E + 127) / 128, splits);
-    e = moe_launch(router_logits_tc, grid, dim3(192), RT_SMEM, s, maps, T, E, (d / 64) / splits, partial, err);
+    e = moe_launch(router_logits_tc, grid, dim3(192), RT_SMEM, s, maps, T, E, (d / 64) / splits, partial, err, wait_ns);
     moe_prof_end(MK_ROUTER_LOGITS, s);
     moe_count_launches(2);
     return e;

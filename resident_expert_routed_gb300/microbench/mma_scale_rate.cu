@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(160, 1) rate(int n_mma, unsigned long long* ns
                             i != 0);
         }
         tc_commit(bar);
-        const bool ok = mbar_wait(bar, 0, abort_flag);
+        const bool ok = mbar_wait(bar, 0, abort_flag, MOE_WAIT_LIMIT_NS);
         ns_out[blockIdx.x] = ok ? global_timer_ns() - t0 : 0ull;
     }
     tc_fence_before();
