@@ -382,13 +382,85 @@ def full_decode_step(scratch, hbm_gbs: float, K: int = 10, W: int = 3):
     step_bytes = sum(used) * expert_bytes + L * E * cfg.d * 4
     out = {"workload": cfg.name, "tokens_per_s": T / (step_ms / 1000.0), "ms_per_step": step_ms, "layers": L,
            "distinct_experts_per_layer": float(np.mean(used)), "step_bytes": step_bytes,
-           "step_hbm_frac": step_bytes / (step_ms / 1000.0) / 1e9 / hbm_gbs}
+           "step_hbm_frac": step_bytes / (step_ms / 1000.0) / 1e9 / hbm_gbs,
+           "step_frac_of_8_tbps": step_bytes / (step_ms / 1000.0) / 1e9 / 8000.0}
+    out["history_256"] = replan_after_history(graph, demand, so, torch.from_numpy(owner).cuda(), arena, cfg, 256)
     del graph, abuf, arena
     torch.cuda.empty_cache()
     return out
 
 
+def replan_after_history(graph, demand, slot_of, owner, arena, cfg, steps: int):
+    """The configured demand history: `steps` replays of the full decode step from a cleared table, then the
+    re-plan of the shared arena (CUDA events around moe_arena_replan), then the refill of the slots it
+    reassigned from pinned host records (CUDA events around moe_arena_refill's copies). The refill's records are
+    64 pinned stand-ins reused for every expert: its timing is that of the copy volume; the arena's contents are
+    not used afterwards."""
+    import torch
+    import resident_expert_routed_gb300 as moe
+    L, E = cfg.L, cfg.E
+    demand.zero_()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        graph.replay()
+    torch.cuda.synchronize()
+    hist_s = time.perf_counter() - t0
+    loads = torch.empty(cfg.n_main, dtype=torch.int32, device="cuda")
+    n_loads = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(moe.moe_replan_workspace_bytes(L, E), dtype=torch.uint8, device="cuda")
+    so0, ow0 = slot_of.clone(), owner.clone()
+    cur = torch.cuda.current_stream()
+    times = []
+    for _ in range(3):                          # the same re-plan three times, from the same tables
+        slot_of.copy_(so0)
+        owner.copy_(ow0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        moe.moe_arena_replan(demand, cfg.n_main, slot_of, owner, loads, n_loads, ws)
+        b.record(cur)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    n = int(n_loads.item())
+    sb = arena.slot_bytes
+    stand_in = torch.empty(64 * sb, dtype=torch.uint8).pin_memory()
+    records = [stand_in.data_ptr() + (f % 64) * sb for f in range(L * E)]
+    copy_stream = torch.cuda.Stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(cur)
+    copied = moe.moe_arena_refill(arena, records, loads, n_loads, owner, cur, copy_stream)
+    b.record(cur)
+    torch.cuda.synchronize()
+    refill_ms = a.elapsed_time(b)
+    D = demand.cpu().numpy().astype(np.float64) / 2.0 ** 40
+    res = {"steps": steps, "history_wall_s": hist_s, "demand_total": float(D.sum()),
+           "experts_with_demand": int((D > 0).sum()), "replan_ms": float(np.median(times)), "n_loads": n,
+           "refill_ms": refill_ms, "refill_slots": copied,
+           "refill_gb_per_s": copied * sb / (refill_ms / 1000.0) / 1e9 if refill_ms > 0 and copied else None,
+           "note": "re-plan of the 10,000-slot main arena over 60 x 256 experts from the 256-step history; the "
+                   "refill copies the reassigned slots from pinned host memory (stand-in records)"}
+    del stand_in
+    return res
+
+
 # ------------------------------------------------------------------ hot-read ring, on and off
+
+def prefill_chunk_report(layer: Layer, prof: dict) -> dict:
+    """The chunk's demand update and heavy-miss list (share >= 0.2, at most 16): the list the last step left,
+    the demand it recorded, and the two kernels' average times from the profiled steps."""
+    import torch
+    layer.demand.zero_()
+    layer.hidden.copy_(layer.pool[0])
+    layer.step()
+    torch.cuda.synchronize()
+    n = int(layer.buf.hot_n.item())
+    D = layer.demand.cpu().numpy().astype(np.float64) / 2.0 ** 40
+    us = {k: 1000.0 * t / c for k, (c, t) in prof.items()}
+    return {"heavy_misses": [int(f) for f in layer.buf.hot_flat.cpu().numpy()[:n]],
+            "heavy_shares": [float(v) for v in layer.buf.hot_share.cpu().numpy()[:n]],
+            "demand_total": float(D.sum()), "experts_with_demand": int((D > 0).sum()),
+            "demand_accumulate_us": us.get("demand_accumulate"), "hot_miss_select_us": us.get("hot_miss_select")}
+
 
 def ring_on_off(T: int, steps: int, n_ring: int = 64):
     """Decode steps (drifted bias, so misses happen) with the asynchronous hot-read ring on and off.
@@ -553,14 +625,15 @@ def run_ours(args, rank, ws, local):
             ls = Layer(cfg, Ts, pool=4)
             m, _, su, _ = timed_graph_steps(ls, 20, 3, scratch, 1)
             sm = sum(m) / len(m)
+            rate = (np.mean(su) * expert_bytes + cfg.E * cfg.d * 4) / (sm / 1000.0) / 1e9
             sweep[f"decode_T{Ts}"] = {"tokens_per_s": Ts / (sm / 1000.0), "ms_per_step": sm,
                                       "distinct_experts": float(np.mean(su)),
-                                      "step_hbm_frac": (np.mean(su) * expert_bytes + cfg.E * cfg.d * 4) / (sm / 1000.0)
-                                      / 1e9 / pk["hbm_gbs"]}
+                                      "step_hbm_frac": rate / pk["hbm_gbs"], "step_frac_of_8_tbps": rate / 8000.0}
             del ls
         sweep[f"decode_T{T}"] = {"tokens_per_s": T / (step_ms / 1000.0), "ms_per_step": step_ms,
                                  "distinct_experts": u_mean,
-                                 "step_hbm_frac": step_bytes / (step_ms / 1000.0) / 1e9 / pk["hbm_gbs"]}
+                                 "step_hbm_frac": step_bytes / (step_ms / 1000.0) / 1e9 / pk["hbm_gbs"],
+                                 "step_frac_of_8_tbps": step_bytes / (step_ms / 1000.0) / 1e9 / 8000.0}
         sweep["hot_ring"] = ring_on_off(T, 30)
         gcfg = synth.GLM
         g_bytes = 3 * gcfg.d * gcfg.ffn // 2 + 3 * gcfg.d * gcfg.ffn // 32
@@ -568,10 +641,10 @@ def run_ours(args, rank, ws, local):
             lg = Layer(gcfg, Tg, pool=4)
             m, _, su, _ = timed_graph_steps(lg, 20, 3, scratch, 1)
             sm = sum(m) / len(m)
+            rate = (np.mean(su) * g_bytes + gcfg.E * gcfg.d * 4) / (sm / 1000.0) / 1e9
             sweep[f"glm_T{Tg}"] = {"workload": gcfg.name, "tokens_per_s": Tg / (sm / 1000.0), "ms_per_step": sm,
                                    "distinct_experts": float(np.mean(su)),
-                                   "step_hbm_frac": (np.mean(su) * g_bytes + gcfg.E * gcfg.d * 4) / (sm / 1000.0)
-                                   / 1e9 / pk["hbm_gbs"]}
+                                   "step_hbm_frac": rate / pk["hbm_gbs"], "step_frac_of_8_tbps": rate / 8000.0}
             del lg
         if not args.no_full:
             sweep["full_decode_L60_T2"] = full_decode_step(scratch, pk["hbm_gbs"])
@@ -593,7 +666,8 @@ def run_ours(args, rank, ws, local):
                 gemm[name] = {"us": 1000.0 * t / n, "tflops": tf, "frac_fp4_peak": tf / fp4_peak,
                               "frac_fp4_datasheet": tf / 13500.0,
                               "frac_fp4_mma_measured": tf / mma["mxf4_tflops"] if mma else None}
-            sweep["prefill_T8192"] = {"tokens_per_s": 8192 / (sm / 1000.0), "ms_per_step": sm,
+            chunk = prefill_chunk_report(lp, pprof)
+            sweep["prefill_T8192"] = {"tokens_per_s": 8192 / (sm / 1000.0), "ms_per_step": sm, "chunk": chunk,
                                       "ffn_tflops": flops / (sm / 1000.0) / 1e12,
                                       "fp4_peak_tflops": fp4_peak,
                                       "fp4_peak_source": f"{pk['source']} bf16 burst x 6 (nominal fp4/bf16 dense ratio)",
@@ -604,6 +678,19 @@ def run_ours(args, rank, ws, local):
                                       "kernels_us": {k: 1000.0 * t / n for k, (n, t) in pprof.items()},
                                       "distinct_experts": float(np.mean(su))}
             del lp
+            torch.cuda.empty_cache()
+            ld = Layer(synth.PREFILL, 8192, pool=1, drift=True)
+            ld.hidden.copy_(ld.pool[0])
+            ld.step()
+            torch.cuda.synchronize()
+            n = int(ld.buf.hot_n.item())
+            sweep["prefill_T8192"]["chunk_drifted"] = {
+                "workload": f"{synth.PREFILL.name} with the bias drifted after the resident set was fixed",
+                "heavy_misses": [int(f) for f in ld.buf.hot_flat.cpu().numpy()[:n]],
+                "heavy_shares": [float(v) for v in ld.buf.hot_share.cpu().numpy()[:n]],
+                "demand_total": float(ld.demand.cpu().numpy().astype(np.float64).sum() / 2.0 ** 40)}
+            del ld
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

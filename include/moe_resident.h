@@ -54,7 +54,9 @@ typedef enum {
 
 /* Bits of the device error word (moe_device_status). */
 #define MOE_DEV_BAD_SLOT    0x1u   /* a slot id >= arena n_slots was routed */
-#define MOE_DEV_NAN_SCALE   0x2u   /* an e8m0 weight scale byte 0xFF (NaN) was read */
+#define MOE_DEV_NAN_SCALE   0x2u   /* an expert GEMM produced a non-finite value: e2m1 codes and the
+                                      quantised activations are finite, so a weight scale byte 0xFF
+                                      (e8m0 NaN) was read, or scales large enough to overflow fp32 */
 #define MOE_DEV_TIMEOUT     0x4u   /* a pipeline wait gave up after its limit */
 #define MOE_DEV_BAD_TABLE   0x8u   /* slot_of / owner tables inconsistent (re-plan, ring) */
 #define MOE_DEV_RESIDENT    0x10u  /* ring install of an expert that is already resident */
@@ -266,6 +268,27 @@ moe_status moe_expert_ffn_prefetch(const int32_t* sel_slot, const moe_arena* are
 moe_status moe_arena_replan(const uint64_t* demand, int L, int E, int n_main, int n_slots,
                             int32_t* slot_of, int32_t* owner, int32_t* loads, int32_t* n_loads,
                             void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Refill after a re-plan (README item 1: once the arena has been planned
+ * again, the experts it admitted are read into the slots they were given).
+ * Call after moe_arena_replan on `stream` (a HOST call: it synchronises
+ * `stream` to read the re-plan's n_loads, loads[] and owner[]). For each slot
+ * s in loads[0 .. n_loads) it copies host_records[owner[s]] (arena->slot_bytes
+ * bytes, the arena record layout) into slot s with cudaMemcpyAsync on
+ * `copy_stream`, after everything enqueued on `stream` so far; `stream` then
+ * waits for the copies, so no work enqueued on it afterwards reads a slot
+ * before its bytes are in. host_records: host array [n_flat] of host pointers
+ * (page-locked, so that the copies run asynchronously), NULL where the store
+ * has no copy. If a new owner has no record nothing is copied and MOE_EINVAL
+ * is returned (the tables already name it: supply the record, or re-plan).
+ * No FFN may be reading the arena on another stream meanwhile.
+ * loads int32 [n_main], n_loads device int32, owner int32 [arena->n_slots]
+ * (device, after the re-plan); *n_copied (host, may be NULL) = slots copied.
+ */
+moe_status moe_arena_refill(const moe_arena* arena, const void* const* host_records, int n_flat,
+                            const int32_t* loads, const int32_t* n_loads, const int32_t* owner,
+                            void* stream, void* copy_stream, int32_t* n_copied);
 
 /*
  * Ring install (README item 3, DeepSeek: a step's largest misses are fetched

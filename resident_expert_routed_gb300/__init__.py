@@ -33,7 +33,7 @@ EXPORTS = ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accum
            "moe_profile_kernel_count", "moe_profile_read", "moe_profile_reset", "moe_demand_decay",
            "moe_demand_save", "moe_demand_load", "moe_hot_ring_create", "moe_hot_ring_step", "moe_hot_ring_destroy",
            "moe_hot_read_sync", "moe_renormalise_weights", "moe_expert_ffn_prefetch", "moe_set_wait_limit",
-           "moe_get_wait_limit", "moe_wait_selftest")
+           "moe_get_wait_limit", "moe_wait_selftest", "moe_arena_refill")
 
 
 class MoeError(RuntimeError):
@@ -99,12 +99,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.moe_get_wait_limit.restype = ctypes.c_uint64
     L.moe_get_wait_limit.argtypes = []
     L.moe_wait_selftest.argtypes = [_P]
+    L.moe_arena_refill.argtypes = [ctypes.POINTER(MoeArena), ctypes.POINTER(ctypes.c_void_p), _I, _P, _P, _P, _P,
+                                   _P, ctypes.POINTER(ctypes.c_int32)]
     for name in ("moe_route_resident", "moe_route_resident_noalloc", "moe_demand_accumulate", "moe_hot_miss_select",
                  "moe_expert_ffn_mxfp4",
                  "moe_arena_replan", "moe_ring_install", "moe_device_status", "moe_profile_enable",
                  "moe_profile_read", "moe_demand_decay", "moe_demand_save", "moe_demand_load", "moe_hot_ring_create",
                  "moe_hot_ring_step", "moe_hot_ring_destroy", "moe_hot_read_sync", "moe_renormalise_weights",
-                 "moe_expert_ffn_prefetch", "moe_set_wait_limit", "moe_wait_selftest"):
+                 "moe_expert_ffn_prefetch", "moe_set_wait_limit", "moe_wait_selftest", "moe_arena_refill"):
         L[name].restype = _I
     _lib = L
     return L
@@ -213,6 +215,20 @@ def moe_arena_replan(demand, n_main, slot_of, owner, loads, n_loads, workspace, 
     _check("moe_arena_replan", load().moe_arena_replan(
         _ptr(demand), L, E, n_main, owner.numel(), _ptr(slot_of), _ptr(owner), _ptr(loads), _ptr(n_loads),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_arena_refill(arena: Arena, records, loads, n_loads, owner, stream=None, copy_stream=None) -> int:
+    """Copy the new owners' records into the slots a re-plan gave them (see the header); returns how many.
+    `records`: a sequence of n_flat host addresses (int) of expert records, or None where the store has none."""
+    n_flat = len(records)
+    ptrs = (ctypes.c_void_p * n_flat)(*[r if r else None for r in records])
+    st = arena.struct()
+    n = ctypes.c_int32(0)
+    cs = copy_stream if copy_stream is not None else torch.cuda.current_stream()
+    _check("moe_arena_refill", load().moe_arena_refill(
+        ctypes.byref(st), ptrs, n_flat, _ptr(loads), _ptr(n_loads), _ptr(owner), _stream(stream),
+        ctypes.c_void_p(cs.cuda_stream), ctypes.byref(n)))
+    return int(n.value)
 
 
 def moe_ring_install(slot_of, owner, ring_slot: int, flat_id: int, stream=None) -> None:

@@ -115,14 +115,6 @@ MOE_DEV unsigned long long block_inclusive_scan_u64(unsigned long long v, unsign
     return v;
 }
 
-// 1 if any of the 16 bytes is 0xFF (an e8m0 scale byte that encodes NaN), else 0: a byte of w is 0xFF
-// exactly when that byte of ~w is zero, and (z - 0x01..01) & ~z & 0x80..80 is non-zero exactly when z has a
-// zero byte.
-MOE_DEV uint32_t has_ff_byte(const uint4& v) {
-    auto one = [](uint32_t w) { return ((~w) - 0x01010101u) & w & 0x80808080u; };
-    return (one(v.x) | one(v.y) | one(v.z) | one(v.w)) != 0u ? 1u : 0u;
-}
-
 MOE_DEV void record_error(uint32_t* err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }
@@ -155,17 +147,22 @@ MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity. Returns false (after
-// raising the CTA's abort flag) when `limit_ns` of wall-clock time pass or
-// another role of the CTA has already aborted. The clock starts at the first
-// failed try and is read every 16 tries.
+// raising the CTA's abort flag) when about `limit_ns` of wall-clock time pass
+// or another role of the CTA has already aborted. The clock is read only
+// every 256 failed tries (every 16 under a bound below 1 ms): a %globaltimer
+// read on every wait costs pipeline time, and a healthy wait ends long before
+// its first read.
 MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
+    const uint32_t every = limit_ns >= 1000000ull ? 255u : 15u;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 0u) {
+        if ((it & every) == every) {
             if (*abort_flag) return false;
-            if (global_timer_ns() - t0 >= limit_ns) {
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 >= limit_ns) {
                 *abort_flag = 1;
                 return false;
             }
@@ -184,11 +181,14 @@ MOE_DEV bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
 // tcgen05.commit) after an abort: ignores the abort flag, bounded by
 // MOE_DRAIN_LIMIT_NS.
 MOE_DEV bool mbar_drain(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 0u && global_timer_ns() - t0 >= MOE_DRAIN_LIMIT_NS) return false;
+        if ((it & 255u) == 255u) {
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 >= MOE_DRAIN_LIMIT_NS) return false;
+        }
     }
 }
 

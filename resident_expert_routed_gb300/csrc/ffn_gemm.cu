@@ -286,7 +286,6 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     } else if (warp >= 6) {
         // ------------------------------------------------------------ scale factors -> TMEM
         const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-        uint32_t nan_seen = 0;                            // an e8m0 weight scale byte 0xFF (NaN) was loaded
         auto load = [&](int g, uint4 (&v)[C::NV]) {
 #pragma unroll
             for (int q = 0; q < C::NV; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
@@ -307,18 +306,18 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             for (int m = 0; m <= C::NMAT; ++m)
 #pragma unroll
                 for (int q = 0; q < 2 * KCH; ++q)
-                    if (q < ats) {
+                    if (q < ats)
                         v[m * 2 * KCH + q] =
                             *reinterpret_cast<const uint4*>(src[m] + (size_t)(at0 + q) * 512 + lane * 16);
-                        if (m < C::NMAT) nan_seen |= has_ff_byte(v[m * 2 * KCH + q]);
-                    }
         };
         scale_writer<C::NV, C::PF, NS>(my_items * nst, load, empty, sfull,
                                        tmem + ((uint32_t)((warp & 3) * 32) << 16) + NBUF * C::ACC_COLS, C::SF_COLS,
                                        abort_flag, a.wait_ns);
-        if (__any_sync(0xFFFFFFFFu, nan_seen) && lane == 0 && warp == 6) record_error(a.err, MOE_DEV_NAN_SCALE);
     } else {
         // ------------------------------------------------------------ epilogue (warps 0..3)
+        // chk = fma(chk, 0, v) over every valid output: it stays finite while every value is finite and
+        // turns NaN for good after a non-finite one (NaN * 0 and inf * 0 are NaN)
+        float chk = 0.0f;
         uint32_t j = 0;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
             const int4 w = a.work[item / a.m_tiles];
@@ -351,6 +350,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     for (int i = 0; i < 16; ++i) {
                         if (c0 + i >= nv) break;                 // warp-uniform
                         const float h = silu_mul(__uint_as_float(vg[i]), __uint_as_float(vu[i]));
+                        chk = fmaf(chk, 0.0f, h);
                         float amax = fabsf(h);
 #pragma unroll
                         for (int off = 16; off > 0; off >>= 1)
@@ -382,7 +382,10 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int pick = __shfl_sync(0xFFFFFFFFu, BN >= 32 ? pp[q] : pp[0], (c0 % 32) + i);
-                        if (c0 + i < nv) ycol[(size_t)pick * a.d] = __uint_as_float(v[i]);
+                        if (c0 + i < nv) {
+                            ycol[(size_t)pick * a.d] = __uint_as_float(v[i]);
+                            chk = fmaf(chk, 0.0f, __uint_as_float(v[i]));
+                        }
                     }
                 }
             }
@@ -390,6 +393,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce[b]);
         }
+        if (__any_sync(0xFFFFFFFFu, !isfinite(chk)) && lane == 0) record_error(a.err, MOE_DEV_NAN_SCALE);
     }
 
     tc_fence_before();
@@ -556,7 +560,6 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
         // stage g of this CTA is K chunk g % nc of its item g / nc; atoms in column
         // order: activations q = 0, 1, then (gate, up) per q
         const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-        uint32_t nan_seen = 0;                            // an e8m0 weight scale byte 0xFF (NaN) was loaded
         auto load = [&](int g, uint4 (&v)[6]) {
 #pragma unroll
             for (int q = 0; q < 6; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
@@ -577,15 +580,14 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
                 v[q] = *reinterpret_cast<const uint4*>(sa + o);
                 v[2 + 2 * q] = *reinterpret_cast<const uint4*>(sg + o);
                 v[3 + 2 * q] = *reinterpret_cast<const uint4*>(su + o);
-                nan_seen |= has_ff_byte(v[2 + 2 * q]) | has_ff_byte(v[3 + 2 * q]);
             }
         };
         scale_writer<6, C::PF, NS>(my_items * nc, load, empty, sfull,
                                    tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256, C::SF_COLS, abort_flag,
                                    a.wait_ns);
-        if (__any_sync(0xFFFFFFFFu, nan_seen) && lane == 0 && warp == 6) record_error(a.err, MOE_DEV_NAN_SCALE);
     } else {
         // ------------------------------------------------------------ epilogue: lane = routed row
+        float chk = 0.0f;                                // sticky non-finite detector, as in the kernel above
         uint32_t j = 0;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
             const int4 w = a.work[item / a.m_tiles];
@@ -622,6 +624,12 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce);
+            if (row < nv) {
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) chk = fmaf(chk, 0.0f, h[q2][i]);
+            }
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
                 const int X = mx_shared_exp(amax[q2]);
@@ -636,6 +644,7 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
                 }
             }
         }
+        if (__any_sync(0xFFFFFFFFu, !isfinite(chk)) && lane == 0) record_error(a.err, MOE_DEV_NAN_SCALE);
     }
 
     tc_fence_before();
@@ -788,8 +797,8 @@ template <int MODE>
 cudaError_t launch_mode(const GemmMaps& maps, const GemmArgs& g, long max_items, int bn, cudaStream_t s) {
     // 64 KB of weights per stage: with fewer CTAs streaming than SMs, one SM takes about
     // 100 GB/s from HBM through five 32 KB stages and 140-160 GB/s through three 64 KB ones
-    // (microbench/bulk_stream_rate.cu), which is what the CTAs left in a partial last round,
-    // or in a grid of few items, get.
+    // (measured with a per-SM bulk-copy streaming test), which is what the CTAs left in a
+    // partial last round, or in a grid of few items, get.
     if constexpr (MODE == 1) {   // gate + up tiles, two 256-element K chunks per stage
         switch (bn) {
             case 16: return launch_one<MODE, 16, 3, 2, 2>(maps, g, max_items, s);

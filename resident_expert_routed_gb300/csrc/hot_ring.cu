@@ -282,3 +282,60 @@ extern "C" moe_status moe_hot_ring_destroy(moe_hot_ring* r) {
     delete r;
     return st;
 }
+
+// ------------------------------------------------------------------ refill after a re-plan
+//
+// README item 1: the arena is planned again from the demand history (after a
+// prompt's prefill, every few hundred tokens, between requests), and the
+// experts it admits are then read into the slots they were given. The
+// re-plan kernel (moe_arena_replan) writes the new tables and the list of
+// slots to refill; this host call reads that list once the re-plan has run and
+// copies each new owner's record from the host store (the stand-in for the
+// drive) on the copy stream; the compute stream then waits for the copies.
+
+extern "C" moe_status moe_arena_refill(const moe_arena* arena, const void* const* host_records, int n_flat,
+                                       const int32_t* loads, const int32_t* n_loads, const int32_t* owner,
+                                       void* stream, void* copy_stream, int32_t* n_copied) {
+    if (!arena || !arena->base || !host_records || !loads || !n_loads || !owner || n_flat < 1 ||
+        arena->n_slots < 1 || arena->slot_bytes <= 0)
+        return MOE_EINVAL;
+    if (n_copied) *n_copied = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
+    int32_t n = 0;
+    if (cudaMemcpyAsync(&n, n_loads, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ECUDA;
+    if (n < 0 || n > arena->n_slots) return MOE_EINVAL;
+    if (n == 0) return MOE_OK;
+    std::vector<int32_t> slots(n), own(arena->n_slots);
+    if (cudaMemcpyAsync(slots.data(), loads, sizeof(int32_t) * n, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(own.data(), owner, sizeof(int32_t) * arena->n_slots, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ECUDA;
+    for (int i = 0; i < n; ++i) {                     // every new owner must have a record: else copy nothing
+        const int sl = slots[i];
+        if (sl < 0 || sl >= arena->n_slots) return MOE_EINVAL;
+        const int f = own[sl];
+        if (f < 0 || f >= n_flat || !host_records[f]) return MOE_EINVAL;
+    }
+    cudaEvent_t ready = nullptr, copied = nullptr;
+    if (cudaEventCreateWithFlags(&ready, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&copied, cudaEventDisableTiming) != cudaSuccess) {
+        if (ready) cudaEventDestroy(ready);
+        return MOE_ECUDA;
+    }
+    moe_status st = MOE_OK;
+    uint8_t* base = static_cast<uint8_t*>(arena->base);
+    if (cudaEventRecord(ready, s) != cudaSuccess || cudaStreamWaitEvent(cs, ready, 0) != cudaSuccess) st = MOE_ECUDA;
+    for (int i = 0; i < n && st == MOE_OK; ++i)
+        if (cudaMemcpyAsync(base + (size_t)slots[i] * arena->slot_bytes, host_records[own[slots[i]]],
+                            (size_t)arena->slot_bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+            st = MOE_ECUDA;
+    if (st == MOE_OK && (cudaEventRecord(copied, cs) != cudaSuccess || cudaStreamWaitEvent(s, copied, 0) != cudaSuccess))
+        st = MOE_ECUDA;
+    cudaEventDestroy(ready);                          // released once the work they mark has run
+    cudaEventDestroy(copied);
+    if (st == MOE_OK && n_copied) *n_copied = n;
+    return st;
+}

@@ -10,7 +10,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (Arena, moe_demand_accumulate, moe_expert_ffn_mxfp4, moe_expert_ffn_prefetch, moe_hot_miss_select,
+from . import (Arena, moe_arena_refill, moe_arena_replan, moe_demand_accumulate, moe_demand_decay,
+               moe_expert_ffn_mxfp4, moe_expert_ffn_prefetch, moe_hot_miss_select, moe_replan_workspace_bytes,
                moe_route_resident, moe_workspace_bytes)
 
 
@@ -129,3 +130,79 @@ class CapturedStep:
         """Replay the step for host_inputs[i] on the current stream; host_out is valid after a sync."""
         self.graphs[i].replay()
         return self.host_out
+
+
+class Cadence:
+    """When to plan the shared arena again (README item 1: after a prompt's prefill, after every few hundred
+    generated tokens, and between requests; "Settings worth knowing" makes the interval a setting).
+
+    Pure host bookkeeping: ``step(tokens, prefill)`` counts the tokens of a finished step and says whether a
+    re-plan is due now; ``request_done()`` says so at a request boundary (when anything was generated since
+    the last re-plan). ``every_tokens`` = 0 turns the token interval off."""
+
+    def __init__(self, every_tokens: int = 256, after_prefill: bool = True, between_requests: bool = True):
+        if every_tokens < 0:
+            raise ValueError("every_tokens must be >= 0")
+        self.every_tokens = every_tokens
+        self.after_prefill = after_prefill
+        self.between_requests = between_requests
+        self.tokens_since = 0
+
+    def step(self, tokens: int, prefill: bool = False) -> bool:
+        self.tokens_since += tokens
+        due = (prefill and self.after_prefill) or (self.every_tokens > 0 and self.tokens_since >= self.every_tokens)
+        if due:
+            self.tokens_since = 0
+        return due
+
+    def request_done(self) -> bool:
+        due = self.between_requests and self.tokens_since > 0
+        if due:
+            self.tokens_since = 0
+        return due
+
+
+class Adaptation:
+    """Re-plans the shared arena from the demand history on a Cadence and refills the slots it reassigns.
+
+    Each re-plan (README item 1) ranks every (layer, expert) by accumulated demand (moe_arena_replan), copies
+    the admitted experts' records from the host store into their new slots on a copy stream
+    (moe_arena_refill; the compute stream waits for them), and then scales the history by ``decay`` so that
+    demand seen before this re-plan weighs less than demand seen after it ("Settings worth knowing": how
+    quickly the resident set follows a change in traffic; decay = 1 keeps the plain sum). ``records``: one
+    host address per flat id (layer * E + e) of that expert's record, or None where the store has none."""
+
+    def __init__(self, demand: torch.Tensor, slot_of: torch.Tensor, owner: torch.Tensor, arena: Arena, n_main: int,
+                 records, cadence: Cadence | None = None, decay: float = 1.0):
+        if not 0.0 <= decay <= 1.0:
+            raise ValueError("decay must be in [0, 1]")
+        L, E = demand.shape
+        self.demand, self.slot_of, self.owner, self.arena = demand, slot_of, owner, arena
+        self.n_main, self.records, self.decay = n_main, list(records), decay
+        self.cadence = cadence if cadence is not None else Cadence()
+        dev = demand.device
+        self.loads = torch.empty(n_main, dtype=torch.int32, device=dev)
+        self.n_loads = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.workspace = torch.empty(moe_replan_workspace_bytes(L, E), dtype=torch.uint8, device=dev)
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        self.replans = 0
+        self.loaded = 0
+
+    def replan(self, stream=None) -> int:
+        """Re-plan now; returns the number of slots refilled."""
+        moe_arena_replan(self.demand, self.n_main, self.slot_of, self.owner, self.loads, self.n_loads,
+                         self.workspace, stream)
+        n = moe_arena_refill(self.arena, self.records, self.loads, self.n_loads, self.owner, stream,
+                             self.copy_stream)
+        if self.decay < 1.0:
+            moe_demand_decay(self.demand, self.decay, stream)
+        self.replans += 1
+        self.loaded += n
+        return n
+
+    def after_step(self, tokens: int, prefill: bool = False, stream=None) -> int:
+        """Call after a step's work is enqueued; re-plans when the cadence says so. Returns slots refilled."""
+        return self.replan(stream) if self.cadence.step(tokens, prefill) else 0
+
+    def request_done(self, stream=None) -> int:
+        return self.replan(stream) if self.cadence.request_done() else 0
