@@ -109,6 +109,45 @@ __device__ __forceinline__ void scale_writer(int n_stages, const Load& load, uin
     }
 }
 
+// The same hand-off with the scale atoms staged in shared memory: the
+// producer copies each stage's atoms with bulk copies that complete on the
+// stage's `full` barrier, so their global latency is hidden by the copy
+// pipeline like the operands' (loading them from global memory in the writer
+// warps, even four stages ahead, left the MMA thread waiting ~260 cycles per
+// stage on the 8192-token gate/up GEMM). Per stage: wait for the stage's
+// bytes, read this lane's 16-byte row of each atom (atom v[q] at smem atom
+// slot `slot_of_atom(q)`; atoms past the end of K are zeros), write them into
+// TMEM, tell the MMA thread. The TMEM columns of a stage are free by then: the
+// producer refilled the stage only after the MMAs that read them completed.
+template <int NV, int NS, typename Valid, typename Slot>
+__device__ __forceinline__ void scale_writer_smem(int n_stages, const Valid& valid, const Slot& slot_of_atom,
+                                                  uint64_t* full, uint64_t* sfull, const uint8_t* sf_smem,
+                                                  int sf_stage_bytes, uint32_t sf_base, int sf_cols,
+                                                  volatile int* abort_flag, uint64_t wait_ns) {
+    static_assert(NV % 2 == 0, "atoms are written in pairs");
+    const int lane = threadIdx.x & 31;
+    for (int g = 0; g < n_stages; ++g) {
+        const int s = g % NS;
+        const uint32_t r = (uint32_t)(g / NS);
+        if (!warp_wait(&full[s], r & 1, abort_flag, wait_ns)) break;
+        const uint8_t* src = sf_smem + s * sf_stage_bytes + lane * 16;
+        const int nvalid = valid(g);
+        uint4 v[NV];
+#pragma unroll
+        for (int q = 0; q < NV; ++q)
+            v[q] = slot_of_atom(q, nvalid) >= 0 ? *reinterpret_cast<const uint4*>(src + slot_of_atom(q, nvalid) * 512)
+                                                : make_uint4(0u, 0u, 0u, 0u);
+        tc_fence_after();
+        const uint32_t sfc = sf_base + s * sf_cols;
+#pragma unroll
+        for (int q = 0; q < NV; q += 2) tc_st_x8(sfc + 4 * q, v[q], v[q + 1]);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[s]);
+    }
+}
+
 // Per pipeline stage: KCH chunks of 256 elements along K. The gate/up GEMM
 // loads, per chunk, one 16 KB code block of the gate tile and one of the up
 // tile (rows f0..f0+127 and ffn+f0..ffn+f0+127) and accumulates them into two
@@ -116,7 +155,7 @@ __device__ __forceinline__ void scale_writer(int n_stages, const Load& load, uin
 // feature; the down GEMM loads one tile. Decode stages carry 64 KB of weights
 // (two chunks of gate and up, or four of one down tile); with twice the atoms
 // per stage the scale writers then look two stages ahead instead of four.
-template <int MODE, int BN, int NS, int KCH, int NBUF>
+template <int MODE, int BN, int NS, int KCH, int NBUF, bool STAGED = false>
 struct Cfg {
     static constexpr int THREADS = 320;           // warps 0-3 epilogue, 4 TMA, 5 MMA, 6-9 scales
     static constexpr int NMAT = MODE == 1 ? 2 : 1;
@@ -126,11 +165,16 @@ struct Cfg {
     static constexpr int B_BYTES = KCH * B_CHUNK;
     static constexpr int NV = (NMAT + 1) * 2 * KCH;        // scale atoms per stage (weights, then activations)
     static constexpr int PF = NMAT * KCH >= 4 ? 2 : 4;     // stages of scales loaded ahead (registers: PF NV uint4)
+    static_assert(PF >= 1, "scale look-ahead");
     static constexpr int SF_COLS = 4 * NV;                 // TMEM columns of one stage's scales
     static constexpr int ACC_COLS = NMAT * BN;    // one accumulator buffer (gate, then up)
+    // STAGED: each stage's scale atoms are copied into shared memory by the producer (weights first,
+    // then the activations', as in the register order) instead of loaded by the writer warps
+    static constexpr int SF_STAGE = STAGED ? NV * 512 : 0;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + NS * A_BYTES;
-    static constexpr int OFF_BAR = OFF_B + NS * B_BYTES;
+    static constexpr int OFF_SF = OFF_B + NS * B_BYTES;
+    static constexpr int OFF_BAR = OFF_SF + NS * SF_STAGE;
     static constexpr int N_BARS = 3 * NS + 2 * NBUF + 1;   // full, empty, sfull per stage; accf, acce; drain
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
@@ -144,9 +188,9 @@ struct Cfg {
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-template <int MODE, int BN, int NS, int KCH, int NBUF>
+template <int MODE, int BN, int NS, int KCH, int NBUF, bool STAGED>
 __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
-    using C = Cfg<MODE, BN, NS, KCH, NBUF>;
+    using C = Cfg<MODE, BN, NS, KCH, NBUF, STAGED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -208,13 +252,29 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     uint8_t* Bs = smem + C::OFF_B + s * C::B_BYTES;
                     const int c0 = st * KCH;
                     const int chunks = nc - c0 < KCH ? nc - c0 : KCH;
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)chunks * (C::NMAT * C::BLK + b_bytes));
+                    uint32_t sf_bytes = 0;
+                    if constexpr (STAGED) {
+                        const int at0 = 2 * KCH * st;
+                        sf_bytes = (uint32_t)(atoms - at0 < 2 * KCH ? atoms - at0 : 2 * KCH) * 512u;
+                    }
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)chunks * (C::NMAT * C::BLK + b_bytes) +
+                                                        (C::NMAT + 1) * sf_bytes);
                     bulk_load(As, codes0 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK, &full[s]);
                     if (C::NMAT == 2)
                         bulk_load(As + KCH * C::BLK, codes1 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK,
                                   &full[s]);
                     for (int q = 0; q < chunks; ++q)
                         tma_load_2d(Bs + q * C::B_CHUNK, &maps.b[hb], &full[s], (c0 + q) * 128, pos0);
+                    if constexpr (STAGED) {
+                        uint8_t* Ss = smem + C::OFF_SF + s * C::SF_STAGE;
+                        const size_t at0b = (size_t)(2 * KCH * st) * 512;
+                        const uint8_t* sc = rec + a.off_scales;
+                        bulk_load(Ss, sc + (size_t)tile0 * atoms * 512 + at0b, sf_bytes, &full[s]);
+                        if (C::NMAT == 2)
+                            bulk_load(Ss + 2 * KCH * 512, sc + (size_t)tile1 * atoms * 512 + at0b, sf_bytes, &full[s]);
+                        bulk_load(Ss + C::NMAT * 2 * KCH * 512, a.b_scales + (size_t)(pos0 / BN) * atoms * 512 + at0b,
+                                  sf_bytes, &full[s]);
+                    }
                 }
             }
         }
@@ -310,9 +370,20 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                         v[m * 2 * KCH + q] =
                             *reinterpret_cast<const uint4*>(src[m] + (size_t)(at0 + q) * 512 + lane * 16);
         };
-        scale_writer<C::NV, C::PF, NS>(my_items * nst, load, empty, sfull,
-                                       tmem + ((uint32_t)((warp & 3) * 32) << 16) + NBUF * C::ACC_COLS, C::SF_COLS,
-                                       abort_flag, a.wait_ns);
+        const uint32_t sf_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + NBUF * C::ACC_COLS;
+        if constexpr (STAGED) {
+            // staged in register order: atom q of matrix m (weights first, then activations) at slot q
+            auto valid = [&](int g) {
+                const int at0 = 2 * KCH * (g % nst);
+                return atoms - at0 < 2 * KCH ? atoms - at0 : 2 * KCH;
+            };
+            auto slot_of_atom = [](int q, int nvalid) { return (q % (2 * KCH)) < nvalid ? q : -1; };
+            scale_writer_smem<C::NV, NS>(my_items * nst, valid, slot_of_atom, full, sfull, smem + C::OFF_SF,
+                                         C::SF_STAGE, sf_base, C::SF_COLS, abort_flag, a.wait_ns);
+        } else {
+            scale_writer<C::NV, C::PF, NS>(my_items * nst, load, empty, sfull, sf_base, C::SF_COLS, abort_flag,
+                                           a.wait_ns);
+        }
     } else {
         // ------------------------------------------------------------ epilogue (warps 0..3)
         // chk = fma(chk, 0, v) over every valid output: it stays finite while every value is finite and
@@ -435,15 +506,16 @@ struct CfgTok {
     static constexpr int A_BYTES = BLK;                 // 128 activation rows x 256 e2m1
     static constexpr int B_BYTES = 2 * BLK;             // gate block, up block (256 rows)
     static constexpr int SF_COLS = 24;                  // activation 8, then per k-group: gate 4 | up 4
+    static constexpr int SF_STAGE = 6 * 512;            // staged atoms: activations q0 q1 | gate q0 q1 | up q0 q1
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + NS * A_BYTES;
-    static constexpr int OFF_BAR = OFF_B + NS * B_BYTES;
+    static constexpr int OFF_SF = OFF_B + NS * B_BYTES;
+    static constexpr int OFF_BAR = OFF_SF + NS * SF_STAGE;
     static constexpr int N_BARS = 3 * NS + 3;           // full, empty, sfull per stage; accf, acce, drain
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;
     static constexpr int TMEM_USED = 256 + SF_COLS * NS;
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
-    static constexpr int PF = 4;                        // stages of scales loaded ahead
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(TMEM_USED <= 512, "TMEM");
 };
@@ -502,16 +574,25 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
                 const uint8_t* rec = a.arena + (size_t)slot * a.slot_bytes;
                 const uint8_t* cg = rec + a.off_codes + (size_t)mt * nc * C::BLK;                  // gate tile
                 const uint8_t* cu = rec + a.off_codes + (size_t)(a.F / 128 + mt) * nc * C::BLK;    // up tile
+                const uint8_t* sg = rec + a.off_scales + (size_t)mt * atoms * 512;                 // their atoms
+                const uint8_t* su = rec + a.off_scales + (size_t)(a.F / 128 + mt) * atoms * 512;
+                const uint8_t* sa = a.b_scales + (size_t)(pos0 / BN) * atoms * 512;                // activations'
                 for (int kc = 0; kc < nc; ++kc, ++it) {
                     const int s = (int)(it % NS);
                     const uint32_t r = it / NS;
                     if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, a.wait_ns)) { ok_run = false; break; }
                     uint8_t* As = smem + C::OFF_A + s * C::A_BYTES;
                     uint8_t* Bs = smem + C::OFF_B + s * C::B_BYTES;
-                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
+                    uint8_t* Ss = smem + C::OFF_SF + s * C::SF_STAGE;
+                    const int at0 = 2 * kc;
+                    const uint32_t sf_bytes = (uint32_t)(atoms - at0 < 2 ? atoms - at0 : 2) * 512u;
+                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES + 3 * sf_bytes);
                     tma_load_2d(As, &maps.b[3], &full[s], kc * 128, pos0);
                     bulk_load(Bs, cg + (size_t)kc * C::BLK, C::BLK, &full[s]);
                     bulk_load(Bs + C::BLK, cu + (size_t)kc * C::BLK, C::BLK, &full[s]);
+                    bulk_load(Ss, sa + (size_t)at0 * 512, sf_bytes, &full[s]);
+                    bulk_load(Ss + 1024, sg + (size_t)at0 * 512, sf_bytes, &full[s]);
+                    bulk_load(Ss + 2048, su + (size_t)at0 * 512, sf_bytes, &full[s]);
                 }
             }
         }
@@ -557,34 +638,22 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
         }
     } else if (warp >= 6 && warp < 10) {
         // ------------------------------------------------------------ scale factors -> TMEM
-        // stage g of this CTA is K chunk g % nc of its item g / nc; atoms in column
-        // order: activations q = 0, 1, then (gate, up) per q
+        // stage g of this CTA is K chunk g % nc of its item g / nc; TMEM column order: activations
+        // q = 0, 1, then (gate, up) per q; staged in shared memory as activations q0 q1 | gate q0 q1 |
+        // up q0 q1 (one bulk copy per matrix)
         const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-        auto load = [&](int g, uint4 (&v)[6]) {
-#pragma unroll
-            for (int q = 0; q < 6; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
-            if (g >= my_items * nc) return;
-            const int li = g / nc, kc = g - li * nc;
-            const int item = blockIdx.x + li * gridDim.x;
-            const int wi = item / a.m_tiles;
-            const int4 w = a.work[wi];
-            const int mt = item - wi * a.m_tiles;
-            const uint8_t* sc = a.arena + (size_t)w.x * a.slot_bytes + a.off_scales;
-            const uint8_t* sa = a.b_scales + (size_t)(w.y / BN) * atoms * 512;
-            const uint8_t* sg = sc + (size_t)mt * atoms * 512;
-            const uint8_t* su = sc + (size_t)(a.F / 128 + mt) * atoms * 512;
-            const int at0 = 2 * kc;
-            const int ats = atoms - at0 < 2 ? atoms - at0 : 2;
-            for (int q = 0; q < ats; ++q) {
-                const size_t o = (size_t)(at0 + q) * 512 + lane * 16;
-                v[q] = *reinterpret_cast<const uint4*>(sa + o);
-                v[2 + 2 * q] = *reinterpret_cast<const uint4*>(sg + o);
-                v[3 + 2 * q] = *reinterpret_cast<const uint4*>(su + o);
-            }
+        auto valid = [&](int g) {
+            const int at0 = 2 * (g % nc);
+            return atoms - at0 < 2 ? atoms - at0 : 2;
         };
-        scale_writer<6, C::PF, NS>(my_items * nc, load, empty, sfull,
-                                   tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256, C::SF_COLS, abort_flag,
-                                   a.wait_ns);
+        auto slot_of_atom = [](int q, int nvalid) {
+            const int kq = q < 2 ? q : (q - 2) >> 1;            // k-group of this column pair
+            if (kq >= nvalid) return -1;
+            return q < 2 ? q : (((q - 2) & 1) == 0 ? 2 + kq : 4 + kq);
+        };
+        scale_writer_smem<6, NS>(my_items * nc, valid, slot_of_atom, full, sfull, smem + C::OFF_SF, C::SF_STAGE,
+                                 tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256, C::SF_COLS, abort_flag,
+                                 a.wait_ns);
     } else {
         // ------------------------------------------------------------ epilogue: lane = routed row
         float chk = 0.0f;                                // sticky non-finite detector, as in the kernel above
@@ -743,10 +812,10 @@ cudaError_t make_act_maps(CUtensorMap* m, const uint8_t* base, uint64_t row_byte
     return cudaSuccess;
 }
 
-template <int MODE, int BN, int NS, int KCH, int NBUF>
+template <int MODE, int BN, int NS, int KCH, int NBUF, bool STAGED = false>
 cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& g, long max_items, cudaStream_t s) {
-    using C = Cfg<MODE, BN, NS, KCH, NBUF>;
-    auto kern = ffn_gemm_kernel<MODE, BN, NS, KCH, NBUF>;
+    using C = Cfg<MODE, BN, NS, KCH, NBUF, STAGED>;
+    auto kern = ffn_gemm_kernel<MODE, BN, NS, KCH, NBUF, STAGED>;
     static int occ_cache[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -795,13 +864,16 @@ cudaError_t launch_tokens(const GemmMaps& maps, const GemmArgs& g, long max_item
 
 template <int MODE>
 cudaError_t launch_mode(const GemmMaps& maps, const GemmArgs& g, long max_items, int bn, cudaStream_t s) {
+    // Scale atoms staged in shared memory (STAGED) where the stages leave room and it measured
+    // faster: the 16-row gate/up tiles (one token: 53.5 -> 51 us per layer step) and the
+    // token-major gate/up kernel; the 64-row and down tiles were no faster staged.
     // 64 KB of weights per stage: with fewer CTAs streaming than SMs, one SM takes about
     // 100 GB/s from HBM through five 32 KB stages and 140-160 GB/s through three 64 KB ones
     // (measured with a per-SM bulk-copy streaming test), which is what the CTAs left in a
     // partial last round, or in a grid of few items, get.
     if constexpr (MODE == 1) {   // gate + up tiles, two 256-element K chunks per stage
         switch (bn) {
-            case 16: return launch_one<MODE, 16, 3, 2, 2>(maps, g, max_items, s);
+            case 16: return launch_one<MODE, 16, 3, 2, 2, true>(maps, g, max_items, s);    // atoms staged
             case 32: return launch_one<MODE, 32, 3, 2, 2>(maps, g, max_items, s);
             case 64: return launch_one<MODE, 64, 2, 2, 2>(maps, g, max_items, s);
             default: return launch_one<MODE, 128, 4, 1, 1>(maps, g, max_items, s);
