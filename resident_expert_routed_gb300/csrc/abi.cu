@@ -229,6 +229,7 @@ moe_status moe_set_wait_limit(uint64_t ns) {
 uint64_t moe_get_wait_limit(void) { return moe_wait_limit_ns(); }
 
 moe_status moe_wait_selftest(void* stream) {
+    MOE_RANGE("moe_wait_selftest");
     uint32_t* err = err_word();
     if (!err) return MOE_ECUDA;
     return cuda_status(launch_wait_selftest(err, moe_wait_limit_ns(), static_cast<cudaStream_t>(stream)));
@@ -276,6 +277,7 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
                               const int32_t* slot_of, int T, int d, int E, int k, int32_t* want_e, float* want_s,
                               int32_t* sel_e, int32_t* sel_slot, float* sel_w, void* workspace, size_t ws_bytes,
                               void* stream) {
+    MOE_RANGE("moe_route_resident");
     if (!hidden_bf16 || !w_router || !slot_of || !want_e || !want_s || !sel_e || !sel_slot || !sel_w || !workspace)
         return MOE_EINVAL;
     if (T < 1 || d < 32 || d % 32 || E < 1 || k < 1 || k > 32 || k > E) return MOE_EINVAL;
@@ -318,6 +320,7 @@ moe_status moe_route_resident(const void* hidden_bf16, const float* w_router, co
 
 moe_status moe_demand_accumulate(const int32_t* want_e, const float* want_s, const int32_t* slot_of, int T, int k,
                                  int layer, int L, int E, uint64_t* demand, float* miss_max, void* stream) {
+    MOE_RANGE("moe_demand_accumulate");
     if (!want_e || !want_s || !slot_of || !demand || !miss_max) return MOE_EINVAL;
     if (T < 1 || k < 1 || k > 32 || E < 1 || L < 1 || layer < 0 || layer >= L) return MOE_EINVAL;
     if (E > 1024) return MOE_EUNSUPPORTED;
@@ -328,6 +331,7 @@ moe_status moe_demand_accumulate(const int32_t* want_e, const float* want_s, con
 
 moe_status moe_hot_miss_select(float* miss_max, int L, int E, float threshold, int cap, int32_t* out_flat,
                                float* out_share, int32_t* n_out, void* stream) {
+    MOE_RANGE("moe_hot_miss_select");
     if (!miss_max || !n_out || L < 1 || E < 1 || cap < 0) return MOE_EINVAL;
     if (cap > 0 && (!out_flat || !out_share)) return MOE_EINVAL;
     if (cap > 1024 || (long)L * E > (1L << 24)) return MOE_EUNSUPPORTED;
@@ -356,6 +360,7 @@ static moe_status arena_status(const moe_arena* arena, int T, int k) {
 }
 
 moe_status moe_expert_ffn_prefetch(const int32_t* sel_slot, const moe_arena* arena, int T, int k, void* stream) {
+    MOE_RANGE("moe_expert_ffn_prefetch");
     if (!sel_slot || !arena) return MOE_EINVAL;
     const moe_status as = arena_status(arena, T, k);
     if (as != MOE_OK) return as;
@@ -366,6 +371,7 @@ moe_status moe_expert_ffn_prefetch(const int32_t* sel_slot, const moe_arena* are
 moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot, const float* sel_w,
                                 const moe_arena* arena, int T, int k, float* out, void* workspace, size_t ws_bytes,
                                 void* stream) {
+    MOE_RANGE("moe_expert_ffn_mxfp4");
     if (!hidden_bf16 || !sel_slot || !sel_w || !arena || !out || !workspace) return MOE_EINVAL;
     const moe_status as = arena_status(arena, T, k);
     if (as != MOE_OK) return as;
@@ -411,6 +417,7 @@ moe_status moe_expert_ffn_mxfp4(const void* hidden_bf16, const int32_t* sel_slot
 moe_status moe_arena_replan(const uint64_t* demand, int L, int E, int n_main, int n_slots, int32_t* slot_of,
                             int32_t* owner, int32_t* loads, int32_t* n_loads, void* workspace, size_t ws_bytes,
                             void* stream) {
+    MOE_RANGE("moe_arena_replan");
     if (!demand || !slot_of || !owner || !loads || !n_loads || !workspace) return MOE_EINVAL;
     if (L < 1 || E < 1 || n_main < 1 || n_slots < n_main) return MOE_EINVAL;
     if ((long)L * E > (1L << 22)) return MOE_EUNSUPPORTED;
@@ -425,6 +432,7 @@ moe_status moe_arena_replan(const uint64_t* demand, int L, int E, int n_main, in
 
 moe_status moe_ring_install(int32_t* slot_of, int32_t* owner, int ring_slot, int flat_id, int n_flat, int n_slots,
                             void* stream) {
+    MOE_RANGE("moe_ring_install");
     if (!slot_of || !owner || n_flat < 1 || n_slots < 1) return MOE_EINVAL;
     if (ring_slot < 0 || ring_slot >= n_slots || flat_id < 0 || flat_id >= n_flat) return MOE_EINVAL;
     uint32_t* err = err_word();
@@ -454,6 +462,7 @@ moe_status moe_device_status(void* stream, uint32_t* bits) {
 // ------------------------------------------------------------------ demand history: decay and persistence
 
 moe_status moe_demand_decay(uint64_t* demand, int64_t n, float factor, void* stream) {
+    MOE_RANGE("moe_demand_decay");
     if (n < 0 || !(factor >= 0.0f && factor <= 1.0f) || (n > 0 && !demand)) return MOE_EINVAL;
     if (n == 0) return MOE_OK;
     const unsigned long long q = (unsigned long long)std::nearbyint((double)factor * 4294967296.0);
@@ -474,6 +483,7 @@ static_assert(sizeof(DemandHeader) == 24, "demand file header");
 }  // namespace
 
 moe_status moe_demand_save(const uint64_t* demand, int L, int E, const char* path, void* stream) {
+    MOE_RANGE("moe_demand_save");
     if (!demand || !path || L < 1 || E < 1) return MOE_EINVAL;
     const size_t n = (size_t)L * E;
     std::vector<uint64_t> host(n);
@@ -498,6 +508,7 @@ moe_status moe_demand_save(const uint64_t* demand, int L, int E, const char* pat
 }
 
 moe_status moe_demand_load(uint64_t* demand, int L, int E, const char* path, void* stream) {
+    MOE_RANGE("moe_demand_load");
     if (!demand || !path || L < 1 || E < 1) return MOE_EINVAL;
     FILE* f = std::fopen(path, "rb");
     if (!f) return MOE_EIO;

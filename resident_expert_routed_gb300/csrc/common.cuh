@@ -12,9 +12,23 @@
 #include <utility>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/moe_resident.h"
 
 #define MOE_DEV __device__ __forceinline__
+
+// Tracing: every entry point of the C ABI opens an NVTX range named after it
+// for the duration of the host call (the enqueue, or the whole call for those
+// that synchronise), so a timeline tool shows which library call issued which
+// kernels. Without a tool attached NVTX calls return at once.
+struct MoeRange {
+    explicit MoeRange(const char* name) { nvtxRangePushA(name); }
+    ~MoeRange() { nvtxRangePop(); }
+    MoeRange(const MoeRange&) = delete;
+    MoeRange& operator=(const MoeRange&) = delete;
+};
+#define MOE_RANGE(name) MoeRange moe_range_guard_(name)
 
 // Default wall-clock bound on any spin-wait inside a kernel (ns); the host
 // passes the bound in force (moe_set_wait_limit) to every pipelined kernel. A

@@ -149,6 +149,7 @@ extern "C" moe_status moe_hot_read_sync(const uint64_t* store, const uint64_t* d
                                         int32_t* slot_of, int32_t* owner, const moe_arena* arena, int layer,
                                         int L, int E, float threshold, int32_t* budget, int32_t* swap,
                                         void* stream) {
+    MOE_RANGE("moe_hot_read_sync");
     if (!store || !demand || !miss_max || !slot_of || !owner || !arena || !arena->base || !budget || !swap)
         return MOE_EINVAL;
     if (L < 1 || E < 1 || layer < 0 || layer >= L || arena->slot_bytes <= 0 || arena->slot_bytes % 16 ||
@@ -225,6 +226,7 @@ extern "C" moe_status moe_hot_ring_create(const moe_arena* arena, int ring_first
 extern "C" moe_status moe_hot_ring_step(moe_hot_ring* r, const int32_t* heavy_flat, const int32_t* n_heavy,
                                         int32_t* slot_of, int32_t* owner, void* stream, void* copy_stream,
                                         int32_t* n_fetched) {
+    MOE_RANGE("moe_hot_ring_step");
     if (!r || !heavy_flat || !n_heavy || !slot_of || !owner) return MOE_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
     if (n_fetched) *n_fetched = 0;
@@ -296,6 +298,7 @@ extern "C" moe_status moe_hot_ring_destroy(moe_hot_ring* r) {
 extern "C" moe_status moe_arena_refill(const moe_arena* arena, const void* const* host_records, int n_flat,
                                        const int32_t* loads, const int32_t* n_loads, const int32_t* owner,
                                        void* stream, void* copy_stream, int32_t* n_copied) {
+    MOE_RANGE("moe_arena_refill");
     if (!arena || !arena->base || !host_records || !loads || !n_loads || !owner || n_flat < 1 ||
         arena->n_slots < 1 || arena->slot_bytes <= 0)
         return MOE_EINVAL;

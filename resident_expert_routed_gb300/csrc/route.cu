@@ -468,6 +468,7 @@ __global__ void __launch_bounds__(256) renormalise_weights(const int32_t* __rest
 }  // namespace
 
 extern "C" moe_status moe_renormalise_weights(const int32_t* sel_slot, float* sel_w, int T, int k, void* stream) {
+    MOE_RANGE("moe_renormalise_weights");
     if (!sel_slot || !sel_w || T < 1 || k < 1 || k > 32) return MOE_EINVAL;
     const cudaError_t e = moe_launch(renormalise_weights, dim3((T + 255) / 256), dim3(256), 0,
                                      static_cast<cudaStream_t>(stream), sel_slot, sel_w, T, k);
@@ -515,6 +516,7 @@ extern "C" moe_status moe_route_resident_noalloc(const void* hidden_bf16, const 
                                                  const int32_t* slot_of, int T, int d, int E, int k,
                                                  int32_t* want_e, float* want_s, int32_t* sel_e, int32_t* sel_slot,
                                                  float* sel_w, void* stream) {
+    MOE_RANGE("moe_route_resident_noalloc");
     if (!hidden_bf16 || !w_router || !slot_of || !want_e || !want_s || !sel_e || !sel_slot || !sel_w)
         return MOE_EINVAL;
     if (T < 1 || d < 32 || d % 32 || E < 1 || k < 1 || k > 32 || k > E) return MOE_EINVAL;
