@@ -419,7 +419,9 @@ moe_status moe_device_status(void* stream, uint32_t* bits);
  * bulk copies and tensor-core operations it has already issued, frees its
  * tensor memory and exits; MOE_DEV_TIMEOUT is set in the device error word
  * (moe_device_status then returns MOE_ETIMEOUT) and that call's outputs are
- * not valid. Later calls are unaffected. Process-wide; read when a call
+ * not valid. The call's later kernels still run on its unfinished
+ * intermediates, so other bits (MOE_DEV_NAN_SCALE) may be set beside
+ * MOE_DEV_TIMEOUT. Later calls are unaffected. Process-wide; read when a call
  * launches its kernels, so a CUDA graph keeps the value it was captured with.
  */
 moe_status moe_set_wait_limit(uint64_t ns);

@@ -128,9 +128,13 @@ def test_pipelines_give_up_under_a_short_bound_then_recover():
     outcomes = []
     try:
         moe.moe_set_wait_limit(1)
+        # after a pipeline gave up, the call's later kernels read unfinished intermediates (e.g. the down
+        # GEMM the gate/up GEMM's missing activation scales), so a non-finite bit may come with the timeout
+        after_timeout = moe.MOE_DEV_TIMEOUT | moe.MOE_DEV_NAN_SCALE
         for _ in range(3):
             _, (st, bits) = _ffn(c, arena, sel_slot, sel_w)
-            assert st in (moe.MOE_OK, moe.MOE_ETIMEOUT) and bits & ~moe.MOE_DEV_TIMEOUT == 0, (st, bits)
+            assert (st, bits) == (moe.MOE_OK, 0) or (st == moe.MOE_ETIMEOUT and bits & moe.MOE_DEV_TIMEOUT and
+                                                      bits & ~after_timeout == 0), (st, bits)
             outcomes.append(st)
         # the tensor-core router (more than 64 tokens) under the same bound
         cp = make_case(synth.PREFILL, 256)
