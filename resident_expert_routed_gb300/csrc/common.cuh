@@ -238,6 +238,23 @@ MOE_DEV void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_
                  : "memory");
 }
 
+// L2 policy that evicts the lines it covers first (createpolicy, the whole
+// access): for data read once, so that it does not push out what later
+// kernels reuse.
+MOE_DEV uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// bulk_load with an L2 cache policy (l2_evict_first_policy for weights streamed once).
+MOE_DEV void bulk_load_hint(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // Bulk prefetch of global bytes into L2 (16-byte aligned, a multiple of 16 bytes; no completion).
 MOE_DEV void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)

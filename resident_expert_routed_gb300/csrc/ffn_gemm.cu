@@ -67,6 +67,7 @@ struct GemmArgs {
     float* Y;                    // down output [T*k, d] (per-pick rows)
     uint32_t* err;
     uint64_t wait_ns;            // bound on each pipeline wait
+    int evict_first;             // weights read once (decode tiles): stream them with an L2 evict-first policy
 };
 
 // Scale factors reach TMEM through registers, not tcgen05.cp: the copy that
@@ -230,6 +231,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
         if (lane == 0) {
             uint32_t& it = issued;
             bool ok_run = true;
+            const uint64_t policy = l2_evict_first_policy();
             int4 w_next = blockIdx.x < n_items ? a.work[blockIdx.x / a.m_tiles] : make_int4(0, 0, 0, 0);
             for (int item = blockIdx.x; item < n_items && ok_run; item += gridDim.x) {
                 const int4 w = w_next;
@@ -259,10 +261,17 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     }
                     mbar_arrive_expect_tx(&full[s], (uint32_t)chunks * (C::NMAT * C::BLK + b_bytes) +
                                                         (C::NMAT + 1) * sf_bytes);
-                    bulk_load(As, codes0 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK, &full[s]);
-                    if (C::NMAT == 2)
-                        bulk_load(As + KCH * C::BLK, codes1 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK,
-                                  &full[s]);
+                    if (a.evict_first) {
+                        bulk_load_hint(As, codes0 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK, &full[s], policy);
+                        if (C::NMAT == 2)
+                            bulk_load_hint(As + KCH * C::BLK, codes1 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK,
+                                           &full[s], policy);
+                    } else {
+                        bulk_load(As, codes0 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK, &full[s]);
+                        if (C::NMAT == 2)
+                            bulk_load(As + KCH * C::BLK, codes1 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK,
+                                      &full[s]);
+                    }
                     for (int q = 0; q < chunks; ++q)
                         tma_load_2d(Bs + q * C::B_CHUNK, &maps.b[hb], &full[s], (c0 + q) * 128, pos0);
                     if constexpr (STAGED) {
@@ -912,6 +921,11 @@ cudaError_t launch_ffn_gemms(const FfnLaunch& a, cudaStream_t s, int* n_launches
     g.pair_of_pos = a.pair_of_pos;
     g.err = a.err;
     g.wait_ns = a.wait_ns;
+    // Decode tiles (up to 64 rows) read each weight tile once per call: streamed evict-first so that
+    // the 100-200 MB of weights a decode layer reads do not push the following small kernels' code and
+    // data (routing tables, logits, activations) out of L2. Large batches reuse each weight tile
+    // across their token tiles and keep the default policy.
+    g.evict_first = a.bn <= 64 ? 1 : 0;
 
     GemmArgs g1 = g;       // gate/up + SwiGLU
     g1.off_codes = ar.off_gu_codes;
