@@ -418,7 +418,8 @@ __global__ void __launch_bounds__(256) ffn_combine(const float* __restrict__ Y, 
         const int s = sel_slot[(size_t)t * k + j];
         if (s < 0 || s >= S) continue;
         const float w = sel_w[(size_t)t * k + j];
-        const float4 y = *reinterpret_cast<const float4*>(Y + ((size_t)t * k + j) * d + c);
+        // streaming load (read once): Y is the largest stream at prefill and need not stay in L2
+        const float4 y = __ldcs(reinterpret_cast<const float4*>(Y + ((size_t)t * k + j) * d + c));
         acc.x = fmaf(w, y.x, acc.x);
         acc.y = fmaf(w, y.y, acc.y);
         acc.z = fmaf(w, y.z, acc.z);
