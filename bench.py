@@ -319,7 +319,7 @@ def e2e_steps(layer: Layer, K: int, scratch):
 def full_decode_step(scratch, hbm_gbs: float, K: int = 10, W: int = 3):
     """The 60-layer decode step (2 tokens, E256 k8 d4096 F2048, one arena of 10,000 main + 64 ring slots shared
     by all layers, the main slots a seeded sample of the 15,360 (layer, expert) ids), replayed from one CUDA graph:
-    per layer the step (with the demand work and prefetch on a side stream, joined before the next layer reuses
+    per layer the step (with the demand work on a side stream, joined before the next layer reuses
     the routing buffers), then the step's heavy-miss list."""
     import torch
     import resident_expert_routed_gb300 as moe

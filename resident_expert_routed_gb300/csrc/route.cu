@@ -166,17 +166,6 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Arg-max across the warp of (value, index): larger value wins, ties to the
-// lower index; two warp reductions (redux.sync) instead of a shuffle tree.
-// `has` false: this lane offers nothing. Returns the winning index, or -1
-// when no lane offers anything.
-__device__ __forceinline__ int warp_argmax(float v, int idx, bool has) {
-    const uint32_t u = has ? ordered_key(v) : 0u;
-    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, u);
-    const uint32_t w = __reduce_min_sync(0xFFFFFFFFu, (has && u == m) ? (uint32_t)idx : 0xFFFFFFFFu);
-    return m == 0u ? -1 : (int)w;
-}
-
 // The bias and slot of the experts a lane holds (lane + 32 i), padding past E.
 // The bias is read before the kernel's wait (no kernel of this library writes
 // it); the slot table after it (ring installs and re-plans rewrite it).
@@ -199,26 +188,76 @@ __device__ __forceinline__ void load_slots(const int32_t* __restrict__ slot_of, 
     }
 }
 
+// The float whose ordered_key is u (u != 0); -0 comes back as +0.
+__device__ __forceinline__ float key_value(uint32_t u) {
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
+// (key, expert) a ranks ahead of b: larger key first, ties to the lower expert index.
+__device__ __forceinline__ bool ahead(uint32_t ka, int ea, uint32_t kb, int eb) {
+    return ka > kb || (ka == kb && ea < eb);
+}
+
+// Bitonic sorting network over a lane's N (key, expert, slot) triples, all in
+// registers (every index is a compile-time constant): afterwards entry 0 ranks
+// ahead of entry 1 and so on.
+template <int N>
+__device__ __forceinline__ void sort_ahead(uint32_t (&key)[N], int (&ex)[N], int (&sl)[N]) {
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const int j = i ^ stride;
+                if (j > i && ahead(key[j], ex[j], key[i], ex[i]) == ((i & size) == 0)) {
+                    const uint32_t tk = key[i]; key[i] = key[j]; key[j] = tk;
+                    const int te = ex[i]; ex[i] = ex[j]; ex[j] = te;
+                    const int ts = sl[i]; sl[i] = sl[j]; sl[j] = ts;
+                }
+            }
+}
+
+// Drops a lane's head entry (the warp's pick of this round) when `mine`.
+template <int N>
+__device__ __forceinline__ void pop_head(bool mine, uint32_t (&key)[N], int (&ex)[N], int (&sl)[N]) {
+#pragma unroll
+    for (int q = 0; q + 1 < N; ++q) {
+        key[q] = mine ? key[q + 1] : key[q];
+        ex[q] = mine ? ex[q + 1] : ex[q];
+        sl[q] = mine ? sl[q + 1] : sl[q];
+    }
+    key[N - 1] = mine ? 0u : key[N - 1];
+}
+
 // Softmax over all E, wanted top-k over all experts and resident top-k, for
 // one token whose logits (bias added) lg[i] (expert lane + 32 i) one warp
 // holds. Order by logit (monotone in the score), ties to the lower expert
-// index. The winning lane of each round writes the pick.
+// index. Each lane sorts its own experts once; every round then takes the
+// warp's best head (two redux.sync reductions: the largest key, then the
+// lowest expert index among the lanes holding it, with its resident bit) and
+// the winning lane drops its head and writes the pick. The first k rounds
+// give the wanted list and, in the same order, the resident picks among them;
+// when fewer than k of those are resident the lanes mask out non-resident
+// experts, sort again and continue until k resident picks (or none left).
 template <int VPL>
 __device__ __forceinline__ void select_token(float (&lg)[VPL], const int (&slot)[VPL], int t, int E, int k,
                                              int32_t* __restrict__ want_e, float* __restrict__ want_s,
                                              int32_t* __restrict__ sel_e, int32_t* __restrict__ sel_slot,
                                              float* __restrict__ sel_w) {
     const int lane = threadIdx.x & 31;
-    const float NEG = -__int_as_float(0x7F800000);   // -inf
+    uint32_t key[VPL];
+    int ex[VPL], sl[VPL];
 #pragma unroll
-    for (int i = 0; i < VPL; ++i)
-        if (lane + 32 * i >= E) lg[i] = NEG;
-    // softmax over all E: max, then sum of exp(l - max)
-    float mx = NEG;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) mx = fmaxf(mx, lg[i]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+    for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = e < E ? ordered_key(lg[i]) : 0u;
+        ex[i] = e;
+        sl[i] = slot[i];
+    }
+    sort_ahead<VPL>(key, ex, sl);
+    // softmax over all E: max (the best key), then sum of exp(l - max) in lane and warp order
+    const float mx = key_value(__reduce_max_sync(0xFFFFFFFFu, key[0]));
     float z = 0.0f;
 #pragma unroll
     for (int i = 0; i < VPL; ++i)
@@ -227,44 +266,41 @@ __device__ __forceinline__ void select_token(float (&lg)[VPL], const int (&slot)
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
     const float inv_z = 1.0f / z;
 
-    // pass 0: wanted top-k over all experts; pass 1: resident top-k, skipped when every wanted pick
-    // is resident (then the two lists are the same)
-    bool all_resident = true;
-    for (int pass = 0; pass < 2; ++pass) {
-        if (pass == 1 && all_resident) break;
-        uint32_t taken = 0;
-        for (int j = 0; j < k; ++j) {
-            float bv = NEG;
-            int bi = 0x7FFFFFFF, bq = 0;
-            bool has = false;
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                const int e = lane + 32 * i;
-                const bool ok = e < E && !((taken >> i) & 1u) && (pass == 0 || slot[i] >= 0);
-                if (ok && (!has || lg[i] > bv)) { bv = lg[i]; bi = e; bq = i; has = true; }
-            }
-            const int win = warp_argmax(bv, bi, has);
-            const size_t o = (size_t)t * k + j;
-            if (win < 0) {                    // fewer resident experts than k
-                if (lane == 0) { sel_e[o] = -1; sel_slot[o] = -1; sel_w[o] = 0.0f; }
-                continue;
-            }
-            const bool mine = win == bi && has;
-            int sl = -1;
-            if (mine) {
-                taken |= 1u << bq;
-#pragma unroll
-                for (int q = 0; q < VPL; ++q) if (q == bq) sl = slot[q];
-                const float s = expf(bv - mx) * inv_z;
-                if (pass == 0) {
-                    want_e[o] = win; want_s[o] = s;
-                    sel_e[o] = win; sel_slot[o] = sl; sel_w[o] = s;     // final if all are resident
-                } else {
-                    sel_e[o] = win; sel_slot[o] = sl; sel_w[o] = s;
-                }
-            }
-            if (pass == 0) all_resident = all_resident && !__any_sync(0xFFFFFFFFu, mine && sl < 0);
+    const size_t row = (size_t)t * k;
+    int ns = 0;                                           // resident picks so far
+    for (int j = 0; j < k; ++j) {
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, key[0]);
+        if (m == 0u) break;                               // fewer experts than k
+        // lowest expert index among the heads equal to m, its non-resident bit in bit 0
+        const uint32_t w = __reduce_min_sync(
+            0xFFFFFFFFu, key[0] == m ? ((uint32_t)ex[0] << 1) | (sl[0] < 0 ? 1u : 0u) : 0xFFFFFFFFu);
+        const bool mine = key[0] == m && (uint32_t)ex[0] == (w >> 1);
+        if (mine) {
+            const float s = expf(key_value(m) - mx) * inv_z;
+            want_e[row + j] = ex[0]; want_s[row + j] = s;
+            if (!(w & 1u)) { sel_e[row + ns] = ex[0]; sel_slot[row + ns] = sl[0]; sel_w[row + ns] = s; }
         }
+        ns += (w & 1u) ? 0 : 1;
+        pop_head<VPL>(mine, key, ex, sl);
+    }
+    if (ns == k) return;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) key[i] = sl[i] < 0 ? 0u : key[i];
+    sort_ahead<VPL>(key, ex, sl);
+    for (; ns < k; ++ns) {
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, key[0]);
+        if (m == 0u) {                                    // fewer resident experts than k
+            if (lane == 0)
+                for (; ns < k; ++ns) { sel_e[row + ns] = -1; sel_slot[row + ns] = -1; sel_w[row + ns] = 0.0f; }
+            break;
+        }
+        const uint32_t w = __reduce_min_sync(0xFFFFFFFFu, key[0] == m ? (uint32_t)ex[0] : 0xFFFFFFFFu);
+        const bool mine = key[0] == m && (uint32_t)ex[0] == w;
+        if (mine) {
+            const float s = expf(key_value(m) - mx) * inv_z;
+            sel_e[row + ns] = ex[0]; sel_slot[row + ns] = sl[0]; sel_w[row + ns] = s;
+        }
+        pop_head<VPL>(mine, key, ex, sl);
     }
 }
 

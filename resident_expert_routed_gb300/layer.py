@@ -36,18 +36,22 @@ class LayerBuffers:
 
 def layer_step(hidden: torch.Tensor, w_router: torch.Tensor, bias, slot_of: torch.Tensor, arena: Arena,
                demand: torch.Tensor, miss_max: torch.Tensor, layer: int, buf: LayerBuffers, stream=None,
-               side=None, out: torch.Tensor | None = None) -> torch.Tensor:
+               side=None, out: torch.Tensor | None = None, prefetch: bool = False) -> torch.Tensor:
     """route -> demand -> expert FFN; returns the output (fp32 [T, d]): buf.out, or `out` when given.
 
     `hidden` and `out` may be pinned host tensors: the kernels then read the
     batch and write the output in host memory directly.
 
-    With a second stream `side`, the L2 prefetch of the weights the FFN reads
-    first and the demand update run there, beside the expert FFN (they read
-    only the routing outputs). The caller then runs ``step_end`` on `side` too
-    and calls ``join(stream, side)`` before the routing outputs in `buf` are
-    written again (the next layer's step when layers share `buf`, else the next
-    step's) and before it reads the tables.
+    With a second stream `side`, the demand update runs there, beside the
+    expert FFN (it reads only the routing outputs), and so does the L2
+    prefetch of the weights the FFN reads first when `prefetch` is set. The
+    caller then runs ``step_end`` on `side` too and calls ``join(stream,
+    side)`` before the routing outputs in `buf` are written again (the next
+    layer's step when layers share `buf`, else the next step's) and before it
+    reads the tables. The prefetch is off by default: it pays only for a
+    single token through one layer with a cold L2 (about 1 us of 50); from
+    two tokens on, and through consecutive layers, it competes with the
+    gate/up GEMM for HBM and the step is slower.
     """
     main = torch.cuda.current_stream() if stream is None else stream
     moe_route_resident(hidden, w_router, bias, slot_of, buf.k, buf.want_e, buf.want_s, buf.sel_e, buf.sel_slot,
@@ -56,7 +60,8 @@ def layer_step(hidden: torch.Tensor, w_router: torch.Tensor, bias, slot_of: torc
         moe_demand_accumulate(buf.want_e, buf.want_s, slot_of, layer, demand, miss_max, main)
     else:
         side.wait_stream(main)
-        moe_expert_ffn_prefetch(buf.sel_slot, arena, side)
+        if prefetch:
+            moe_expert_ffn_prefetch(buf.sel_slot, arena, side)
         moe_demand_accumulate(buf.want_e, buf.want_s, slot_of, layer, demand, miss_max, side)
     dst = buf.out if out is None else out
     moe_expert_ffn_mxfp4(hidden, buf.sel_slot, buf.sel_w, arena, dst, buf.workspace, main)
@@ -64,7 +69,7 @@ def layer_step(hidden: torch.Tensor, w_router: torch.Tensor, bias, slot_of: torc
 
 
 def join(stream, side) -> None:
-    """The main stream waits for the side stream's work (prefetch, demand update, heavy-miss list)."""
+    """The main stream waits for the side stream's work (demand update, heavy-miss list, prefetch)."""
     (torch.cuda.current_stream() if stream is None else stream).wait_stream(side)
 
 

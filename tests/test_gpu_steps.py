@@ -258,8 +258,9 @@ def test_full_decode_256_step_history_and_replan():
 
 @pytest.mark.parametrize("T", [8, 130])
 def test_side_stream_step_matches_one_stream(T):
-    # the demand update and heavy-miss list on a second stream, forked after routing and joined at the
-    # end of the step, eagerly and under CUDA graph capture: every output equals the one-stream step's
+    # the demand update and heavy-miss list (with and without the L2 prefetch) on a second stream, forked
+    # after routing and joined at the end of the step, eagerly and under CUDA graph capture: every output
+    # equals the one-stream step's
     from resident_expert_routed_gb300.layer import join
     cfg = synth.TINY
     x = [hidden_dev(synth.hidden_bf16(cfg.seed, T, cfg.d, stream=s)) for s in range(3)]
@@ -272,7 +273,7 @@ def test_side_stream_step_matches_one_stream(T):
     arena = _arena(cfg, n_slots, owner)
     so = to_dev(slot_of)
 
-    def run(side, graph):
+    def run(side, graph, prefetch=False):
         buf = LayerBuffers(T, cfg.k, cfg.E, cfg.d, cfg.ffn, n_slots)
         demand = torch.zeros((1, cfg.E), dtype=torch.int64, device="cuda")
         miss = torch.zeros((1, cfg.E), dtype=torch.float32, device="cuda")
@@ -281,7 +282,7 @@ def test_side_stream_step_matches_one_stream(T):
         outs = []
 
         def step():
-            layer_step(hidden, W, b, so, arena, demand, miss, 0, buf, main, side)
+            layer_step(hidden, W, b, so, arena, demand, miss, 0, buf, main, side, prefetch=prefetch)
             step_end(miss, buf, 0.2, main if side is None else side)
             if side is not None:
                 join(main, side)
@@ -314,8 +315,8 @@ def test_side_stream_step_matches_one_stream(T):
         return outs
 
     ref = run(None, False)
-    for side, graph in ((torch.cuda.Stream(), False), (torch.cuda.Stream(), True)):
-        got = run(side, graph)
+    for graph, prefetch in ((False, False), (True, False), (False, True), (True, True)):
+        got = run(torch.cuda.Stream(), graph, prefetch)
         for r, g in zip(ref, got):
             for a, c in zip(r, g):
                 assert torch.equal(a, c)
