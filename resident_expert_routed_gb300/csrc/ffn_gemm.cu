@@ -111,13 +111,15 @@ __device__ __forceinline__ void scale_writer(int n_stages, const Load& load, uin
 }
 
 // The same hand-off with the scale atoms staged in shared memory: the
-// producer copies each stage's atoms with bulk copies that complete on the
-// stage's `full` barrier, so their global latency is hidden by the copy
-// pipeline like the operands' (loading them from global memory in the writer
-// warps, even four stages ahead, left the MMA thread waiting ~260 cycles per
-// stage on the 8192-token gate/up GEMM). Per stage: wait for the stage's
-// bytes, read this lane's 16-byte row of each atom (atom v[q] at smem atom
-// slot `slot_of_atom(q)`; atoms past the end of K are zeros), write them into
+// producer copies each stage's atoms with bulk copies that complete on a
+// barrier of the stage (`full`, or in the token-major kernel a barrier of
+// their own, issued before the operands, so that the writers fill TMEM while
+// the 48 KB of operands are still arriving), so their global latency is hidden
+// by the copy pipeline like the operands' (loading them from global memory in
+// the writer warps, even four stages ahead, left the MMA thread waiting ~260
+// cycles per stage on the 8192-token gate/up GEMM). Per stage: wait for the
+// atoms, read this lane's 16-byte row of each (atom v[q] at smem atom slot
+// `slot_of_atom(q)`; atoms past the end of K are zeros), write them into
 // TMEM, tell the MMA thread. The TMEM columns of a stage are free by then: the
 // producer refilled the stage only after the MMAs that read them completed.
 template <int NV, int NS, typename Valid, typename Slot>
@@ -520,7 +522,7 @@ struct CfgTok {
     static constexpr int OFF_B = OFF_A + NS * A_BYTES;
     static constexpr int OFF_SF = OFF_B + NS * B_BYTES;
     static constexpr int OFF_BAR = OFF_SF + NS * SF_STAGE;
-    static constexpr int N_BARS = 3 * NS + 3;           // full, empty, sfull per stage; accf, acce, drain
+    static constexpr int N_BARS = 4 * NS + 3;           // full, empty, sfull, satoms per stage; accf, acce, drain
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;
     static constexpr int TMEM_USED = 256 + SF_COLS * NS;
@@ -539,7 +541,8 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* empty = full + NS;
     uint64_t* sfull = empty + NS;
-    uint64_t* accf = sfull + NS;
+    uint64_t* satoms = sfull + NS;      // the stage's scale atoms alone (the writers' wait)
+    uint64_t* accf = satoms + NS;
     uint64_t* acce = accf + 1;
     uint64_t* drain = acce + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -548,7 +551,9 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sfull[s], 4); }
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sfull[s], 4); mbar_init(&satoms[s], 1);
+        }
         mbar_init(accf, 1);
         mbar_init(acce, 8);
         mbar_init(drain, 1);
@@ -595,13 +600,16 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
                     uint8_t* Ss = smem + C::OFF_SF + s * C::SF_STAGE;
                     const int at0 = 2 * kc;
                     const uint32_t sf_bytes = (uint32_t)(atoms - at0 < 2 ? atoms - at0 : 2) * 512u;
-                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES + 3 * sf_bytes);
+                    // the scale atoms first, on their own barrier: the writers move them into TMEM while
+                    // the operands are still arriving
+                    mbar_arrive_expect_tx(&satoms[s], 3 * sf_bytes);
+                    bulk_load(Ss, sa + (size_t)at0 * 512, sf_bytes, &satoms[s]);
+                    bulk_load(Ss + 1024, sg + (size_t)at0 * 512, sf_bytes, &satoms[s]);
+                    bulk_load(Ss + 2048, su + (size_t)at0 * 512, sf_bytes, &satoms[s]);
+                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
                     tma_load_2d(As, &maps.b[3], &full[s], kc * 128, pos0);
                     bulk_load(Bs, cg + (size_t)kc * C::BLK, C::BLK, &full[s]);
                     bulk_load(Bs + C::BLK, cu + (size_t)kc * C::BLK, C::BLK, &full[s]);
-                    bulk_load(Ss, sa + (size_t)at0 * 512, sf_bytes, &full[s]);
-                    bulk_load(Ss + 1024, sg + (size_t)at0 * 512, sf_bytes, &full[s]);
-                    bulk_load(Ss + 2048, su + (size_t)at0 * 512, sf_bytes, &full[s]);
                 }
             }
         }
@@ -660,7 +668,7 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
             if (kq >= nvalid) return -1;
             return q < 2 ? q : (((q - 2) & 1) == 0 ? 2 + kq : 4 + kq);
         };
-        scale_writer_smem<6, NS>(my_items * nc, valid, slot_of_atom, full, sfull, smem + C::OFF_SF, C::SF_STAGE,
+        scale_writer_smem<6, NS>(my_items * nc, valid, slot_of_atom, satoms, sfull, smem + C::OFF_SF, C::SF_STAGE,
                                  tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256, C::SF_COLS, abort_flag,
                                  a.wait_ns);
     } else {
@@ -678,30 +686,33 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
             const int pos = pos0 + row;
             const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
             const int fb0 = warp < 4 ? 0 : 2;
-            // 2 of the 4 blocks of 32 features: SwiGLU of both into registers, then the
-            // accumulator is released to the next item's MMAs before the MXFP4 blocks are
-            // formed and stored
-            float h[2][32];
-            float amax[2] = {0.0f, 0.0f};
+            // 2 of the 4 blocks of 32 features: the raw gate and up values of both are read
+            // from TMEM (eight loads in flight at once) and the accumulator is released to the
+            // next item's MMAs before any SwiGLU: its two MUFU operations per value would
+            // otherwise hold the accumulator for ~2,000 cycles per tile
+            uint32_t r[8][16];                  // block q2: gate lo, gate hi, up lo, up hi at 4 q2 ..
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
                 const int fb = fb0 + q2;
-                uint32_t g0[16], g1[16], u0[16], u1[16];
-                tc_ld_x16(trow + 32 * fb, g0);
-                tc_ld_x16(trow + 32 * fb + 16, g1);
-                tc_ld_x16(trow + 128 + 32 * fb, u0);
-                tc_ld_x16(trow + 128 + 32 * fb + 16, u1);
-                tc_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    h[q2][i] = silu_mul(__uint_as_float(i < 16 ? g0[i] : g1[i - 16]),
-                                        __uint_as_float(i < 16 ? u0[i] : u1[i - 16]));
-                    amax[q2] = fmaxf(amax[q2], fabsf(h[q2][i]));
-                }
+                tc_ld_x16(trow + 32 * fb, r[4 * q2 + 0]);
+                tc_ld_x16(trow + 32 * fb + 16, r[4 * q2 + 1]);
+                tc_ld_x16(trow + 128 + 32 * fb, r[4 * q2 + 2]);
+                tc_ld_x16(trow + 128 + 32 * fb + 16, r[4 * q2 + 3]);
             }
+            tc_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce);
+            float h[2][32];
+            float amax[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    h[q2][i] = silu_mul(__uint_as_float(r[4 * q2 + (i >> 4)][i & 15]),
+                                        __uint_as_float(r[4 * q2 + 2 + (i >> 4)][i & 15]));
+                    amax[q2] = fmaxf(amax[q2], fabsf(h[q2][i]));
+                }
             if (row < nv) {
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2)
@@ -728,7 +739,7 @@ __global__ void __launch_bounds__(448, 1) ffn_gate_up_tokens_kernel(const __grid
     tc_fence_before();
     __syncthreads();
     if (*abort_flag) {               // final after the barrier: nothing new is issued past it
-        if (warp == 4 && lane == 0) drain_stage_fills(full, NS, issued);
+        if (warp == 4 && lane == 0) { drain_stage_fills(full, NS, issued); drain_stage_fills(satoms, NS, issued); }
         if (warp == 5 && lane == 0) tc_drain(drain);
         tc_fence_before();
         __syncthreads();
