@@ -178,7 +178,8 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + NS * A_BYTES;
     static constexpr int OFF_SF = OFF_B + NS * B_BYTES;
     static constexpr int OFF_BAR = OFF_SF + NS * SF_STAGE;
-    static constexpr int N_BARS = 3 * NS + 2 * NBUF + 1;   // full, empty, sfull per stage; accf, acce; drain
+    // full, empty, sfull (and, staged, satoms: the scale atoms alone) per stage; accf, acce; drain
+    static constexpr int N_BARS = (STAGED ? 4 : 3) * NS + 2 * NBUF + 1;
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
     static constexpr int TMEM_USED = NBUF * ACC_COLS + SF_COLS * NS;
@@ -199,7 +200,8 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* empty = full + NS;
     uint64_t* sfull = empty + NS;
-    uint64_t* accf = sfull + NS;
+    uint64_t* satoms = sfull + NS;                   // staged: the stage's scale atoms (the writers' wait)
+    uint64_t* accf = satoms + (STAGED ? NS : 0);
     uint64_t* acce = accf + NBUF;
     uint64_t* drain = acce + NBUF;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -208,7 +210,10 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sfull[s], 4); }
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sfull[s], 4);
+            if (STAGED) mbar_init(&satoms[s], 1);
+        }
         for (int b = 0; b < NBUF; ++b) { mbar_init(&accf[b], 1); mbar_init(&acce[b], 4); }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -258,11 +263,22 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     const int chunks = nc - c0 < KCH ? nc - c0 : KCH;
                     uint32_t sf_bytes = 0;
                     if constexpr (STAGED) {
+                        // the scale atoms first, on their own barrier: the writers move them into TMEM while
+                        // the stage's 64 KB of weights are still arriving
                         const int at0 = 2 * KCH * st;
                         sf_bytes = (uint32_t)(atoms - at0 < 2 * KCH ? atoms - at0 : 2 * KCH) * 512u;
+                        uint8_t* Ss = smem + C::OFF_SF + s * C::SF_STAGE;
+                        const size_t at0b = (size_t)at0 * 512;
+                        const uint8_t* sc = rec + a.off_scales;
+                        mbar_arrive_expect_tx(&satoms[s], (C::NMAT + 1) * sf_bytes);
+                        bulk_load(Ss, sc + (size_t)tile0 * atoms * 512 + at0b, sf_bytes, &satoms[s]);
+                        if (C::NMAT == 2)
+                            bulk_load(Ss + 2 * KCH * 512, sc + (size_t)tile1 * atoms * 512 + at0b, sf_bytes,
+                                      &satoms[s]);
+                        bulk_load(Ss + C::NMAT * 2 * KCH * 512, a.b_scales + (size_t)(pos0 / BN) * atoms * 512 + at0b,
+                                  sf_bytes, &satoms[s]);
                     }
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)chunks * (C::NMAT * C::BLK + b_bytes) +
-                                                        (C::NMAT + 1) * sf_bytes);
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)chunks * (C::NMAT * C::BLK + b_bytes));
                     if (a.evict_first) {
                         bulk_load_hint(As, codes0 + (size_t)c0 * C::BLK, (uint32_t)chunks * C::BLK, &full[s], policy);
                         if (C::NMAT == 2)
@@ -276,16 +292,6 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     }
                     for (int q = 0; q < chunks; ++q)
                         tma_load_2d(Bs + q * C::B_CHUNK, &maps.b[hb], &full[s], (c0 + q) * 128, pos0);
-                    if constexpr (STAGED) {
-                        uint8_t* Ss = smem + C::OFF_SF + s * C::SF_STAGE;
-                        const size_t at0b = (size_t)(2 * KCH * st) * 512;
-                        const uint8_t* sc = rec + a.off_scales;
-                        bulk_load(Ss, sc + (size_t)tile0 * atoms * 512 + at0b, sf_bytes, &full[s]);
-                        if (C::NMAT == 2)
-                            bulk_load(Ss + 2 * KCH * 512, sc + (size_t)tile1 * atoms * 512 + at0b, sf_bytes, &full[s]);
-                        bulk_load(Ss + C::NMAT * 2 * KCH * 512, a.b_scales + (size_t)(pos0 / BN) * atoms * 512 + at0b,
-                                  sf_bytes, &full[s]);
-                    }
                 }
             }
         }
@@ -389,7 +395,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                 return atoms - at0 < 2 * KCH ? atoms - at0 : 2 * KCH;
             };
             auto slot_of_atom = [](int q, int nvalid) { return (q % (2 * KCH)) < nvalid ? q : -1; };
-            scale_writer_smem<C::NV, NS>(my_items * nst, valid, slot_of_atom, full, sfull, smem + C::OFF_SF,
+            scale_writer_smem<C::NV, NS>(my_items * nst, valid, slot_of_atom, satoms, sfull, smem + C::OFF_SF,
                                          C::SF_STAGE, sf_base, C::SF_COLS, abort_flag, a.wait_ns);
         } else {
             scale_writer<C::NV, C::PF, NS>(my_items * nst, load, empty, sfull, sf_base, C::SF_COLS, abort_flag,
@@ -481,7 +487,10 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     tc_fence_before();
     __syncthreads();
     if (*abort_flag) {               // final after the barrier: nothing new is issued past it
-        if (warp == 4 && lane == 0) drain_stage_fills(full, NS, issued);
+        if (warp == 4 && lane == 0) {
+            drain_stage_fills(full, NS, issued);
+            if (STAGED) drain_stage_fills(satoms, NS, issued);
+        }
         if (warp == 5 && lane == 0) tc_drain(drain);
         tc_fence_before();
         __syncthreads();
