@@ -193,16 +193,22 @@ __device__ __forceinline__ float key_value(uint32_t u) {
     return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
 }
 
-// (key, expert) a ranks ahead of b: larger key first, ties to the lower expert index.
-__device__ __forceinline__ bool ahead(uint32_t ka, int ea, uint32_t kb, int eb) {
-    return ka > kb || (ka == kb && ea < eb);
+// Rank of (key, expert): larger key first, ties to the lower expert index, as
+// one 64-bit value (the key above the inverted index), so that a comparison
+// is a single unsigned compare.
+__device__ __forceinline__ unsigned long long rank64(uint32_t key, int e) {
+    return ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
 }
 
 // Bitonic sorting network over a lane's N (key, expert, slot) triples, all in
-// registers (every index is a compile-time constant): afterwards entry 0 ranks
-// ahead of entry 1 and so on.
+// registers (every index is a compile-time constant) and without branches
+// (each compare-exchange is three selects): afterwards entry 0 ranks ahead of
+// entry 1 and so on.
 template <int N>
 __device__ __forceinline__ void sort_ahead(uint32_t (&key)[N], int (&ex)[N], int (&sl)[N]) {
+    unsigned long long r[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) r[i] = rank64(key[i], ex[i]);
 #pragma unroll
     for (int size = 2; size <= N; size <<= 1)
 #pragma unroll
@@ -210,12 +216,19 @@ __device__ __forceinline__ void sort_ahead(uint32_t (&key)[N], int (&ex)[N], int
 #pragma unroll
             for (int i = 0; i < N; ++i) {
                 const int j = i ^ stride;
-                if (j > i && ahead(key[j], ex[j], key[i], ex[i]) == ((i & size) == 0)) {
-                    const uint32_t tk = key[i]; key[i] = key[j]; key[j] = tk;
-                    const int te = ex[i]; ex[i] = ex[j]; ex[j] = te;
-                    const int ts = sl[i]; sl[i] = sl[j]; sl[j] = ts;
+                if (j > i) {
+                    const bool sw = (r[j] > r[i]) == ((i & size) == 0);   // j must come first
+                    const unsigned long long ri = r[i], rj = r[j];
+                    const int si = sl[i], sj = sl[j];
+                    r[i] = sw ? rj : ri; r[j] = sw ? ri : rj;
+                    sl[i] = sw ? sj : si; sl[j] = sw ? si : sj;
                 }
             }
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        key[i] = (uint32_t)(r[i] >> 32);
+        ex[i] = (int)(0xFFFFFFFFu - (uint32_t)r[i]);
+    }
 }
 
 // Drops a lane's head entry (the warp's pick of this round) when `mine`.
@@ -307,7 +320,7 @@ __device__ __forceinline__ void select_token(float (&lg)[VPL], const int (&slot)
 // One warp per token (few K slices): the slices are summed in slice order;
 // U slices' loads are issued together.
 template <int VPL>
-__global__ void __launch_bounds__(256) route_select(const float* __restrict__ partial, int splits,
+__global__ void __launch_bounds__(256, 1) route_select(const float* __restrict__ partial, int splits,
                                                     const float* __restrict__ bias,
                                                     const int32_t* __restrict__ slot_of, int T, int E, int k,
                                                     int32_t* __restrict__ want_e, float* __restrict__ want_s,
