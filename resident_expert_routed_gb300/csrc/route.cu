@@ -249,12 +249,16 @@ __device__ __forceinline__ void pop_head(bool mine, uint32_t (&key)[N], int (&ex
 // index. Each lane sorts its own experts once; every round then takes the
 // warp's best head (two redux.sync reductions: the largest key, then the
 // lowest expert index among the lanes holding it, with its resident bit) and
-// the winning lane drops its head and writes the pick. The first k rounds
-// give the wanted list and, in the same order, the resident picks among them;
-// when fewer than k of those are resident the lanes mask out non-resident
-// experts, sort again and continue until k resident picks (or none left).
+// the winning lane drops its head. Every lane knows each round's key and
+// expert, so lane j records the j-th wanted pick and lane q the q-th resident
+// one, and all picks' weights and stores follow the rounds at once (the
+// resident picks' slots read from slot_of). The first k rounds give the
+// wanted list and, in the same order, the resident picks among them; when
+// fewer than k of those are resident the lanes mask out non-resident experts,
+// sort again and continue until k resident picks (or none left).
 template <int VPL>
 __device__ __forceinline__ void select_token(float (&lg)[VPL], const int (&slot)[VPL], int t, int E, int k,
+                                             const int32_t* __restrict__ slot_of,
                                              int32_t* __restrict__ want_e, float* __restrict__ want_s,
                                              int32_t* __restrict__ sel_e, int32_t* __restrict__ sel_slot,
                                              float* __restrict__ sel_w) {
@@ -279,41 +283,47 @@ __device__ __forceinline__ void select_token(float (&lg)[VPL], const int (&slot)
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
     const float inv_z = 1.0f / z;
 
-    const size_t row = (size_t)t * k;
-    int ns = 0;                                           // resident picks so far
+    uint32_t w_key = 0u, r_key = 0u;                      // this lane's wanted / resident pick
+    int w_e = -1, r_e = -1;
+    int nw = 0, ns = 0;                                   // wanted and resident picks so far
     for (int j = 0; j < k; ++j) {
         const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, key[0]);
         if (m == 0u) break;                               // fewer experts than k
         // lowest expert index among the heads equal to m, its non-resident bit in bit 0
         const uint32_t w = __reduce_min_sync(
             0xFFFFFFFFu, key[0] == m ? ((uint32_t)ex[0] << 1) | (sl[0] < 0 ? 1u : 0u) : 0xFFFFFFFFu);
-        const bool mine = key[0] == m && (uint32_t)ex[0] == (w >> 1);
-        if (mine) {
-            const float s = expf(key_value(m) - mx) * inv_z;
-            want_e[row + j] = ex[0]; want_s[row + j] = s;
-            if (!(w & 1u)) { sel_e[row + ns] = ex[0]; sel_slot[row + ns] = sl[0]; sel_w[row + ns] = s; }
+        const int e = (int)(w >> 1);
+        if (lane == j) { w_key = m; w_e = e; }
+        if (!(w & 1u)) {
+            if (lane == ns) { r_key = m; r_e = e; }
+            ++ns;
         }
-        ns += (w & 1u) ? 0 : 1;
-        pop_head<VPL>(mine, key, ex, sl);
+        ++nw;
+        pop_head<VPL>(key[0] == m && ex[0] == e, key, ex, sl);
     }
-    if (ns == k) return;
+    if (ns < k) {
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) key[i] = sl[i] < 0 ? 0u : key[i];
-    sort_ahead<VPL>(key, ex, sl);
-    for (; ns < k; ++ns) {
-        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, key[0]);
-        if (m == 0u) {                                    // fewer resident experts than k
-            if (lane == 0)
-                for (; ns < k; ++ns) { sel_e[row + ns] = -1; sel_slot[row + ns] = -1; sel_w[row + ns] = 0.0f; }
-            break;
+        for (int i = 0; i < VPL; ++i) key[i] = sl[i] < 0 ? 0u : key[i];
+        sort_ahead<VPL>(key, ex, sl);
+        for (; ns < k; ++ns) {
+            const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, key[0]);
+            if (m == 0u) break;                           // fewer resident experts than k
+            const uint32_t w = __reduce_min_sync(0xFFFFFFFFu, key[0] == m ? (uint32_t)ex[0] : 0xFFFFFFFFu);
+            if (lane == ns) { r_key = m; r_e = (int)w; }
+            pop_head<VPL>(key[0] == m && (uint32_t)ex[0] == w, key, ex, sl);
         }
-        const uint32_t w = __reduce_min_sync(0xFFFFFFFFu, key[0] == m ? (uint32_t)ex[0] : 0xFFFFFFFFu);
-        const bool mine = key[0] == m && (uint32_t)ex[0] == w;
-        if (mine) {
-            const float s = expf(key_value(m) - mx) * inv_z;
-            sel_e[row + ns] = ex[0]; sel_slot[row + ns] = sl[0]; sel_w[row + ns] = s;
-        }
-        pop_head<VPL>(mine, key, ex, sl);
+    }
+    // the picks' weights and outputs, one lane per pick; resident positions past the last pick are padding
+    const size_t row = (size_t)t * k;
+    if (lane < nw) {
+        want_e[row + lane] = w_e;
+        want_s[row + lane] = expf(key_value(w_key) - mx) * inv_z;
+    }
+    if (lane < k) {
+        const bool real = lane < ns;
+        sel_e[row + lane] = real ? r_e : -1;
+        sel_slot[row + lane] = real ? slot_of[r_e] : -1;
+        sel_w[row + lane] = real ? expf(key_value(r_key) - mx) * inv_z : 0.0f;
     }
 }
 
@@ -366,7 +376,7 @@ __global__ void __launch_bounds__(256, 1) route_select(const float* __restrict__
     }
 #pragma unroll
     for (int i = 0; i < VPL; ++i) lg[i] += bv[i];
-    select_token<VPL>(lg, slot, t, E, k, want_e, want_s, sel_e, sel_slot, sel_w);
+    select_token<VPL>(lg, slot, t, E, k, slot_of, want_e, want_s, sel_e, sel_slot, sel_w);
 }
 
 // One CTA of 8 warps per token (many K slices, small batches): warp w sums
@@ -422,7 +432,7 @@ __global__ void __launch_bounds__(256) route_select_cta(const float* __restrict_
         for (int w = 1; w < 8; ++w) lg[i] += part[w][lane + 32 * i];
         lg[i] += bv[i];
     }
-    select_token<VPL>(lg, slot, t, E, k, want_e, want_s, sel_e, sel_slot, sel_w);
+    select_token<VPL>(lg, slot, t, E, k, slot_of, want_e, want_s, sel_e, sel_slot, sel_w);
 }
 
 // A batch in page-locked host memory, copied once into device memory (16-byte
