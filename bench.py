@@ -99,7 +99,8 @@ class Layer:
 
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 50 ms while running (a default timed region of 50
-    steps lasts well under a second, steps with their L2 flushes included)."""
+    steps lasts well under a second, steps with their L2 flushes included); only samples taken after the
+    sampler is running, i.e. inside the region, are summarised."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
@@ -108,6 +109,14 @@ class ClockSampler:
         self.idx = gpu_index
         self.proc = None
         self.path = None
+        self.skip = 0
+
+    def _lines(self) -> int:
+        try:
+            with open(self.path) as f:
+                return sum(1 for line in f if line.strip())
+        except OSError:
+            return 0
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -118,6 +127,14 @@ class ClockSampler:
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        # the sampler's start-up can take longer than a short timed region: wait (at most 5 s) until it has
+        # written its first line, and summarise only the lines written after that (taken while timing)
+        t0 = time.perf_counter()
+        while self.proc is not None and self._lines() == 0 and time.perf_counter() - t0 < 5.0:
+            if self.proc.poll() is not None:
+                break
+            time.sleep(0.01)
+        self.skip = self._lines()
         return self
 
     def __exit__(self, *exc):
@@ -131,7 +148,8 @@ class ClockSampler:
     def summary(self):
         rows = []
         try:
-            for line in open(self.path):
+            lines = [line for line in open(self.path) if line.strip()]
+            for line in lines[self.skip:]:
                 f = [x.strip() for x in line.split(",")]
                 if len(f) >= 9:
                     rows.append(f)
