@@ -75,3 +75,30 @@ def test_reference_arm_under_torchrun_prints_once():
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["steps"] == 1 and line["warmup"] == 3
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["value"] > 0
+
+
+def test_clock_sampler_counts_only_samples_taken_while_timing(tmp_path, monkeypatch):
+    """The sampler waits for its tool's first line and summarises only the lines written after it: a slow start
+    of the tool must not leave a short timed region unsampled, and its idle first sample must not count."""
+    import time
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text(
+        "#!/bin/sh\n"
+        "echo '0, 120, 2070, 100.0, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+        "sleep 0.3\n"
+        "while true; do\n"
+        "  echo '0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Active'\n"
+        "  sleep 0.05\n"
+        "done\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    sys.path.insert(0, ROOT)
+    import bench
+    clk = bench.ClockSampler(0)
+    with clk:
+        assert clk.skip == 1                      # the idle line written before the region
+        time.sleep(0.6)
+    out = clk.summary()
+    assert out["samples"] >= 3
+    assert out["sm_mhz"] == 2070.0 and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"]
